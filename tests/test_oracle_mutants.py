@@ -1,0 +1,112 @@
+"""The oracle's pins catch plausible mistakes.
+
+Each case plants one mistake in a private copy of the oracle's C source,
+compiles that copy on the CPU, and checks that the pin suite below rejects
+it.  The oracle itself is never modified.
+"""
+import subprocess
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from all_reduce_reduction_gb300 import workload as wl
+from _util import DT_CODE, as_uint, decode64, golden, hex_array, spacing
+
+MUTANTS = {
+    "acc_starts_at_positive_zero": (
+        "float acc = load_widened(dtype, in[0], i);\n    int k;\n    for (k = 1; k < R; ++k) {",
+        "float acc = 0.0f;\n    int k;\n    for (k = 0; k < R; ++k) {"),
+    "last_rank_dropped": ("for (k = 1; k < R; ++k) {", "for (k = 1; k < R - 1; ++k) {"),
+    "ranks_folded_in_reverse": [
+        ("float acc = load_widened(dtype, in[0], i);", "float acc = load_widened(dtype, in[R - 1], i);"),
+        ("float x = load_widened(dtype, in[k], i);", "float x = load_widened(dtype, in[R - 1 - k], i);")],
+    "wrong_sign": ("acc = acc + x;", "acc = acc - x;"),
+    "element_index_shifted": ("float x = load_widened(dtype, in[k], i);",
+                              "float x = load_widened(dtype, in[k], i ? i - 1 : i);"),
+    "rounded_every_add": ("acc = acc + x;",
+                          "acc = acc + x;\n        if (dtype == OR_BF16) acc = oracle_bf16_to_f32(oracle_f32_to_bf16(acc));"),
+    "ties_to_odd": ("(D == 0x8000u && (K & 1u) != 0u)", "(D == 0x8000u && (K & 1u) == 0u)"),
+    "bf16_truncates": ("        K += 1u;\n    return (uint16_t)((sign >> 16) | K);",
+                       "        K += 0u;\n    return (uint16_t)((sign >> 16) | K);"),
+    "fp16_flushes_subnormals": ("    if (q < 1024u)                     /* only reachable with Q == -24 */\n        return (uint16_t)(sign | q);",
+                                "    if (q < 1024u)\n        return (uint16_t)sign;"),
+    "fp16_ties_away": ("if (rest > half || (rest == half && (q & 1u) != 0u))", "if (rest >= half)"),
+    "fp16_decode_bias_off": ("mag = ldexpf((float)(1024u + m), (int)e - 25);",
+                             "mag = ldexpf((float)(1024u + m), (int)e - 24);"),
+    "packet_bytes_big_endian": ("payload |= byte << (8 * j);", "payload |= byte << (8 * (3 - j));"),
+    "flag_in_low_half": ("pkts[p] = ((uint64_t)flag << 32) | (uint64_t)payload;",
+                         "pkts[p] = ((uint64_t)payload << 32) | (uint64_t)flag;"),
+}
+
+
+def _pins_pass(lib) -> bool:
+    """A compact run of the oracle's pins against a given build; False as
+    soon as one fails."""
+    # hand-derived fold cases
+    for case in golden("fold_cases.json")["cases"]:
+        dt = case["dtype"]
+        ins = [hex_array([h], dt) for h in case["inputs"]]
+        out = oracle.allreduce(ins, DT_CODE[dt], lib=lib)[0]
+        if int(as_uint(out, dt)[0]) != int(case["expected"], 16):
+            return False
+    # exact integer sums and the binary64 bound
+    for dt in ("bf16", "fp16", "fp32"):
+        ts = wl.make_inputs(91, 7, 513, dt, "integer")
+        exact = sum(t.to(torch.int64) for t in ts).to(torch.float64).to(wl.TORCH_DTYPE[dt])
+        out = oracle.allreduce([wl.bits(t) for t in ts], DT_CODE[dt], lib=lib)[0]
+        if not np.array_equal(as_uint(out, dt), as_uint(wl.bits(exact), dt)):
+            return False
+        ins = [wl.bits(t) for t in wl.make_inputs(90, 16, 1025, dt, "loguniform")]
+        x = np.stack([decode64(a, dt) for a in ins])
+        s = x.sum(axis=0)
+        y = decode64(oracle.allreduce(ins, DT_CODE[dt], lib=lib)[0], dt)
+        tol = spacing(s, dt) + 16 * 2.0 ** -24 * np.abs(x).sum(axis=0)
+        fin = np.isfinite(y)
+        if np.any(np.abs(y[fin] - s[fin]) > tol[fin]):
+            return False
+    # conversions against torch on a sample (subnormals and ties included)
+    rng = np.random.default_rng(7)
+    f = rng.integers(0, 1 << 32, size=1 << 18, dtype=np.uint64).astype(np.uint32)
+    f = np.concatenate([f, np.arange(0, 1 << 16, dtype=np.uint32) << np.uint32(8)]).view(np.float32)
+    f = f[np.isfinite(f)]
+    for dt, td in ((0, torch.bfloat16), (1, torch.float16)):
+        ours = oracle.round_f32(f, dt, lib=lib)
+        ref = torch.from_numpy(f).to(td).view(torch.int16).numpy().view(np.uint16)
+        if not np.array_equal(ours, ref):
+            return False
+        pats = np.arange(1 << 16, dtype=np.uint32).astype(np.uint16)
+        w = oracle.widen(pats, dt, lib=lib)
+        ref = torch.from_numpy(pats.view(np.int16)).view(td).float().numpy()
+        ok = ~np.isnan(ref)
+        if not np.array_equal(w[ok].view(np.uint32), ref[ok].view(np.uint32)):
+            return False
+    # packets
+    for case in golden("ll_packets.json")["cases"]:
+        dt = case["dtype"]
+        x = hex_array(case["elements"], dt)
+        pk = oracle.ll_pack(x, DT_CODE[dt], int(case["flag"], 16), lib=lib)
+        if [int(p) for p in pk] != [int(h, 16) for h in case["packets"]]:
+            return False
+    return True
+
+
+def test_pins_accept_the_oracle(oracle_lib):
+    assert _pins_pass(oracle_lib)
+
+
+@pytest.mark.parametrize("name", sorted(MUTANTS))
+def test_pins_reject_mutant(tmp_path, name):
+    edits = MUTANTS[name]
+    if isinstance(edits, tuple):
+        edits = [edits]
+    src = open(oracle.SRC).read()
+    for old, new in edits:
+        assert src.count(old) == 1, "mutation anchor not found: " + name
+        src = src.replace(old, new)
+    path = tmp_path / "mutant.c"
+    path.write_text(src)
+    so = str(tmp_path / ("lib_%s.so" % name))
+    subprocess.check_call(["gcc", *oracle.CFLAGS, "-w", "-o", so, str(path), "-lm"])
+    assert not _pins_pass(oracle.load(so)), "pins missed the planted mistake " + name
