@@ -1,1 +1,226 @@
-"""GB300-native virtual-rank sum all-reduce (binding is added with the CUDA library)."""
+"""GB300-native sum all-reduce over R virtual ranks held in one GPU's HBM.
+
+This module is a thin ctypes binding of the C ABI declared in
+``include/ar.h`` (library ``libar_gb300.so``, built in-tree by
+``all_reduce_reduction_gb300.build``).  Every function has the name of the C
+entry point it calls and only marshals arguments: device buffers may be given
+as integers (device addresses) or as objects with ``data_ptr()`` (torch CUDA
+tensors); a stream as an integer ``cudaStream_t``, an object with
+``cuda_stream`` (``torch.cuda.Stream``), or ``None`` for torch's current
+stream.  All work runs in the library's CUDA kernels; there is no CPU path.
+If the library is missing, the first call raises ``RuntimeError``.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(HERE, "libar_gb300.so")
+
+# enum ar_dtype / ar_algo / ar_proto / ar_status_code (include/ar.h)
+AR_BF16, AR_FP16, AR_FP32 = 0, 1, 2
+AR_ONE_SHOT, AR_TWO_SHOT = 0, 1
+AR_LL, AR_HB = 0, 1
+AR_OK = 0
+AR_ERR_INVALID = 1
+AR_ERR_UNSUPPORTED = 2
+AR_ERR_CUDA = 3
+AR_ERR_NOMEM = 4
+AR_ERR_TIMEOUT = 5
+AR_ERR_FLAG_MISMATCH = 6
+AR_MAX_RANKS = 32
+AR_LL_MAX_BYTES = 64 << 20
+
+DTYPES = {"bf16": AR_BF16, "fp16": AR_FP16, "fp32": AR_FP32}
+ALGOS = {"one_shot": AR_ONE_SHOT, "two_shot": AR_TWO_SHOT}
+PROTOS = {"ll": AR_LL, "hb": AR_HB}
+
+
+class ArError(RuntimeError):
+    """A nonzero ar_status_code returned by the library."""
+
+    def __init__(self, code: int, where: str):
+        self.code = code
+        super().__init__("%s: %s" % (where, ar_strerror(code)))
+
+
+class ar_info(ctypes.Structure):
+    _fields_ = [
+        ("R", ctypes.c_int),
+        ("dtype", ctypes.c_int),
+        ("N", ctypes.c_size_t),
+        ("elem_size", ctypes.c_size_t),
+        ("ll_capable", ctypes.c_int),
+        ("ll_packets_per_rank", ctypes.c_size_t),
+        ("scratch_bytes", ctypes.c_size_t),
+        ("num_sms", ctypes.c_int),
+        ("ll_ctas_per_rank_max", ctypes.c_int),
+        ("tma_tile_bytes", ctypes.c_int),
+        ("tma_stages", ctypes.c_int),
+        ("timeout_ns", ctypes.c_uint64),
+    ]
+
+    def as_dict(self) -> dict:
+        return {name: getattr(self, name) for name, _ in self._fields_}
+
+
+_lock = threading.Lock()
+_lib = None
+
+# exported entry points: name -> (argtypes, restype)
+_VP, _SZ, _I, _U32, _U64 = ctypes.c_void_p, ctypes.c_size_t, ctypes.c_int, ctypes.c_uint32, ctypes.c_uint64
+_VPP = ctypes.POINTER(ctypes.c_void_p)
+SIGNATURES = {
+    "ar_create": ([_I, _SZ, _I, ctypes.POINTER(_VP)], _I),
+    "ar_destroy": ([_VP], _I),
+    "ar_allreduce": ([_VP, _VPP, _VPP, _I, _I, _VP], _I),
+    "ar_reduce_scatter": ([_VP, _VPP, _VPP, _VP], _I),
+    "ar_all_gather": ([_VP, _VPP, _VP], _I),
+    "ar_ll_pack": ([_VP, _VP, _VP, _SZ, _U32, _VP], _I),
+    "ar_ll_unpack": ([_VP, _VP, _VP, _SZ, _U32, _VP], _I),
+    "ar_status": ([_VP, _VP], _I),
+    "ar_set_timeout": ([_VP, _U64], _I),
+    "ar_debug_drop_rank": ([_VP, _I], _I),
+    "ar_round": ([_I, _VP, _VP, _SZ, _VP], _I),
+    "ar_get_info": ([_VP, ctypes.POINTER(ar_info)], _I),
+    "ar_strerror": ([_I], ctypes.c_char_p),
+}
+
+
+def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
+    """Load the CUDA library (no GPU call is made).  Raises if it is absent."""
+    global _lib
+    with _lock:
+        if _lib is not None and path == LIB_PATH:
+            return _lib
+        if not os.path.exists(path):
+            raise RuntimeError(
+                "libar_gb300.so is not built (expected at %s); run "
+                "`python -c 'import __graft_entry__ as g; g.build()'`" % path)
+        lib = ctypes.CDLL(path)
+        for name, (args, res) in SIGNATURES.items():
+            fn = getattr(lib, name)
+            fn.argtypes, fn.restype = args, res
+        if path == LIB_PATH:
+            _lib = lib
+        return lib
+
+
+def _ptr(x) -> int:
+    if x is None:
+        return 0
+    if isinstance(x, int):
+        return x
+    return int(x.data_ptr())
+
+
+def _stream(s) -> int:
+    if s is None:
+        import torch
+        return int(torch.cuda.current_stream().cuda_stream)
+    if isinstance(s, int):
+        return s
+    return int(s.cuda_stream)
+
+
+def _ptr_array(bufs):
+    return (ctypes.c_void_p * len(bufs))(*[_ptr(b) for b in bufs])
+
+
+def _check(code: int, where: str) -> None:
+    if code != AR_OK:
+        raise ArError(code, where)
+
+
+def ar_strerror(code: int) -> str:
+    return load_library().ar_strerror(code).decode()
+
+
+def ar_create(R: int, N: int, dtype) -> int:
+    """Create a handle for R ranks of N elements; returns it as an integer."""
+    dt = DTYPES[dtype] if isinstance(dtype, str) else dtype
+    h = ctypes.c_void_p()
+    _check(load_library().ar_create(R, N, dt, ctypes.byref(h)), "ar_create")
+    return h.value
+
+
+def ar_destroy(h: int) -> None:
+    _check(load_library().ar_destroy(h), "ar_destroy")
+
+
+def ar_allreduce(h: int, ins, outs, algo=AR_ONE_SHOT, proto=AR_HB, stream=None) -> None:
+    algo = ALGOS[algo] if isinstance(algo, str) else algo
+    proto = PROTOS[proto] if isinstance(proto, str) else proto
+    _check(load_library().ar_allreduce(h, _ptr_array(ins), _ptr_array(outs), algo, proto,
+                                       _stream(stream)), "ar_allreduce")
+
+
+def ar_reduce_scatter(h: int, ins, outs, stream=None) -> None:
+    _check(load_library().ar_reduce_scatter(h, _ptr_array(ins), _ptr_array(outs), _stream(stream)),
+           "ar_reduce_scatter")
+
+
+def ar_all_gather(h: int, outs, stream=None) -> None:
+    _check(load_library().ar_all_gather(h, _ptr_array(outs), _stream(stream)), "ar_all_gather")
+
+
+def ar_ll_pack(h: int, src, pkts, n: int, flag: int, stream=None) -> None:
+    _check(load_library().ar_ll_pack(h, _ptr(src), _ptr(pkts), n, flag & 0xFFFFFFFF,
+                                     _stream(stream)), "ar_ll_pack")
+
+
+def ar_ll_unpack(h: int, pkts, dst, n: int, flag: int, stream=None) -> None:
+    _check(load_library().ar_ll_unpack(h, _ptr(pkts), _ptr(dst), n, flag & 0xFFFFFFFF,
+                                       _stream(stream)), "ar_ll_unpack")
+
+
+def ar_status(h: int, stream=None) -> int:
+    """Wait for the stream; return (and clear) the handle's device status."""
+    return load_library().ar_status(h, _stream(stream))
+
+
+def ar_set_timeout(h: int, ns: int) -> None:
+    _check(load_library().ar_set_timeout(h, ns), "ar_set_timeout")
+
+
+def ar_debug_drop_rank(h: int, rank: int) -> None:
+    _check(load_library().ar_debug_drop_rank(h, rank), "ar_debug_drop_rank")
+
+
+def ar_round(dtype, src, dst, n: int, stream=None) -> None:
+    dt = DTYPES[dtype] if isinstance(dtype, str) else dtype
+    _check(load_library().ar_round(dt, _ptr(src), _ptr(dst), n, _stream(stream)), "ar_round")
+
+
+def ar_get_info(h: int) -> dict:
+    info = ar_info()
+    _check(load_library().ar_get_info(h, ctypes.byref(info)), "ar_get_info")
+    return info.as_dict()
+
+
+class Handle:
+    """Owns one handle: ``with Handle(R, N, "bf16") as h: ar_allreduce(h.h, ...)``."""
+
+    def __init__(self, R: int, N: int, dtype):
+        self.R, self.N = R, N
+        self.dtype = dtype
+        self.h = ar_create(R, N, dtype)
+
+    def close(self) -> None:
+        if self.h:
+            ar_destroy(self.h)
+            self.h = 0
+
+    def __enter__(self):
+        return self
+
+    def __exit__(self, *exc):
+        self.close()
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass

@@ -1,0 +1,444 @@
+// The C ABI (include/ar.h): handle life cycle, argument checks and the choice
+// of kernel for each (algo, proto, alignment).  Nothing here allocates,
+// copies or synchronises on the hot path, so every call can be captured in a
+// CUDA graph.  The NCCL-style drop-in statement of the call follows
+// "【论文分享】MSCCL++：让 GPU 通信像 CUDA 一样可编程", section
+// "第一层：Collective API"; its guards (dtypes, SUM only) "SGLang 中的 MSCCL++
+// All-Reduce 基准测试与推理集成指南", section 4.3.
+#include <new>
+
+#include "ar_internal.h"
+
+using namespace ar;
+
+struct ar_handle {
+    int R;
+    size_t N;
+    int dtype;
+    size_t esz;
+    int device;
+    int num_sms;
+    void *dev_mem;
+    size_t dev_bytes;
+    Ctl ctl;
+    uint64_t *slots;        // LL scratch, NULL if the handle is not LL capable
+    uint64_t ppad;          // packets per slot
+    uint64_t shard;         // two-shot shard S, elements
+    int ll_cap[2][2];       // co-resident LL CTAs [vec][two_shot]
+    int one_shot_warps;     // warps per CTA of the one-shot HB kernel
+    int one_shot_cap;       // CTAs of the one-shot HB kernel per launch
+    int reg_cap;            // CTAs of the 256-thread kernels per launch
+    int tma_tile;
+    int tma_stages;
+};
+
+namespace {
+
+const uint64_t kDefaultTimeoutNs = 1000000000ull;
+
+bool valid_dtype(int d) { return d == AR_BF16 || d == AR_FP16 || d == AR_FP32; }
+
+uint64_t ceil_div(uint64_t a, uint64_t b) { return (a + b - 1) / b; }
+
+int clamp_grid(uint64_t want, int cap) {
+    if (want < 1)
+        want = 1;
+    if (want > (uint64_t)cap)
+        want = (uint64_t)cap;
+    return (int)want;
+}
+
+bool on_device(const ar_handle *h) {
+    int dev = -1;
+    return cudaGetDevice(&dev) == cudaSuccess && dev == h->device;
+}
+
+bool ranges_overlap(uintptr_t a, uintptr_t b, size_t len) { return a < b + len && b < a + len; }
+
+// Checks shared by the calls that take R output pointers and, optionally, R
+// input pointers.  Sets *vec16 / *vec8 (all pointers 16- / 8-byte aligned)
+// and *inplace (some in[r] == out[r]).
+int check_buffers(const ar_handle *h, const void *const in[], void *const out[], bool *vec16,
+                  bool *vec8, bool *inplace) {
+    if (!h || !out)
+        return AR_ERR_INVALID;
+    if (!on_device(h))
+        return AR_ERR_INVALID;
+    const int R = h->R;
+    const size_t len = h->N * h->esz;
+    uintptr_t all = 0;
+    for (int r = 0; r < R; ++r) {
+        if (!out[r] || (in && !in[r]))
+            return AR_ERR_INVALID;
+        const uintptr_t o = (uintptr_t)out[r];
+        const uintptr_t i = in ? (uintptr_t)in[r] : 0;
+        if ((o % h->esz) != 0 || (i % h->esz) != 0)
+            return AR_ERR_INVALID;
+        all |= o | i;
+    }
+    *vec16 = (all & 15u) == 0;
+    *vec8 = (all & 7u) == 0;
+    *inplace = false;
+    for (int a = 0; a < R; ++a) {
+        const uintptr_t oa = (uintptr_t)out[a];
+        for (int b = a + 1; b < R; ++b)
+            if (ranges_overlap(oa, (uintptr_t)out[b], len))
+                return AR_ERR_INVALID;            // outputs must be disjoint
+        if (!in)
+            continue;
+        for (int b = 0; b < R; ++b) {
+            const uintptr_t ib = (uintptr_t)in[b];
+            if (!ranges_overlap(oa, ib, len))
+                continue;
+            if (a == b && ib == oa)
+                *inplace = true;                  // same rank, exactly in place
+            else
+                return AR_ERR_INVALID;
+        }
+    }
+    return AR_OK;
+}
+
+void fill_ptrs(const ar_handle *h, const void *const in[], void *const out[], RankPtrs *p) {
+    for (int r = 0; r < AR_MAX_RANKS; ++r) {
+        p->in[r] = (in && r < h->R) ? in[r] : nullptr;
+        p->out[r] = r < h->R ? out[r] : nullptr;
+    }
+}
+
+HbArgs hb_args(const ar_handle *h, const void *const in[], void *const out[], bool inplace) {
+    HbArgs a;
+    fill_ptrs(h, in, out, &a.p);
+    a.n = h->N;
+    a.shard = h->shard;
+    a.R = h->R;
+    a.inplace = inplace ? 1 : 0;
+    return a;
+}
+
+int from_cuda(cudaError_t e) {
+    if (e == cudaSuccess)
+        return AR_OK;
+    (void)cudaGetLastError();   // clear a non-sticky launch error
+    return AR_ERR_CUDA;
+}
+
+// ---- the four all-reduce paths ---------------------------------------------
+
+int one_shot_hb(ar_handle *h, const void *const in[], void *const out[], bool vec, bool inplace,
+                cudaStream_t s) {
+    const HbArgs a = hb_args(h, in, out, inplace);
+    const uint64_t per_vec = 16 / h->esz;
+    const uint64_t units = vec ? h->N / per_vec : h->N;
+    const uint64_t per_blk = (uint64_t)(h->one_shot_warps / h->R) * 32;
+    const int grid = clamp_grid(ceil_div(units, per_blk), h->one_shot_cap);
+    return from_cuda(launch_one_shot_hb(a, h->dtype, vec, grid, 32 * h->one_shot_warps, s));
+}
+
+int two_shot_hb(ar_handle *h, const void *const in[], void *const out[], bool vec, bool inplace,
+                cudaStream_t s) {
+    const uint64_t body = (h->N * h->esz) / 16 * 16;
+    if (vec && body > 0) {
+        TmaArgs a;
+        fill_ptrs(h, in, out, &a.p);
+        a.n = h->N;
+        a.body_bytes = body;
+        a.shard_bytes = h->shard * h->esz;
+        a.tiles_per_shard = ceil_div(a.shard_bytes, (uint64_t)h->tma_tile);
+        a.R = h->R;
+        a.tile_bytes = h->tma_tile;
+        a.stages = h->tma_stages;
+        a.c = h->ctl;
+        const uint64_t items = ceil_div(body, (uint64_t)h->tma_tile) + (uint64_t)h->R;
+        const int grid = clamp_grid(items, h->num_sms);
+        return from_cuda(launch_two_shot_tma(a, h->dtype, grid, s));
+    }
+    // unaligned buffers: one thread per element reduces once, stores R times
+    const HbArgs a = hb_args(h, in, out, inplace);
+    const uint64_t units = vec ? h->N / (16 / h->esz) : h->N;
+    const int grid = clamp_grid(ceil_div(units, kRegThreads), h->reg_cap);
+    return from_cuda(launch_reduce(a, h->dtype, vec, false, grid, s));
+}
+
+int ll(ar_handle *h, const void *const in[], void *const out[], bool vec, bool two,
+       cudaStream_t s) {
+    if (!h->slots)
+        return AR_ERR_UNSUPPORTED;
+    LlArgs a;
+    fill_ptrs(h, in, out, &a.p);
+    a.n = h->N;
+    a.shard = h->shard;
+    a.slots = h->slots;
+    a.ppad = h->ppad;
+    a.R = h->R;
+    a.c = h->ctl;
+    const uint64_t nbytes = h->N * h->esz;
+    const uint64_t work = vec ? nbytes / 8 + 1 : (nbytes + 3) / 4;   // units per rank
+    const int cap = h->ll_cap[vec ? 1 : 0][two ? 1 : 0];
+    int gmax = cap / h->R;
+    if (gmax > kEpochWords / h->R)
+        gmax = kEpochWords / h->R;
+    if (gmax < 1)
+        return AR_ERR_UNSUPPORTED;                 // cannot keep R CTAs resident
+    a.G = clamp_grid(ceil_div(work, kLlThreads), gmax);
+    return from_cuda(launch_ll(a, h->dtype, vec, two, s));
+}
+
+}  // namespace
+
+// ---------------------------------------------------------------------------
+
+extern "C" {
+
+const char *ar_strerror(int code) {
+    switch (code) {
+    case AR_OK: return "AR_OK";
+    case AR_ERR_INVALID: return "AR_ERR_INVALID: invalid argument";
+    case AR_ERR_UNSUPPORTED: return "AR_ERR_UNSUPPORTED: request not supported";
+    case AR_ERR_CUDA: return "AR_ERR_CUDA: CUDA runtime error";
+    case AR_ERR_NOMEM: return "AR_ERR_NOMEM: device allocation failed";
+    case AR_ERR_TIMEOUT: return "AR_ERR_TIMEOUT: a device-side wait timed out";
+    case AR_ERR_FLAG_MISMATCH: return "AR_ERR_FLAG_MISMATCH: LL packet with an unexpected flag";
+    default: return "unknown ar status code";
+    }
+}
+
+int ar_create(int R, size_t N, int dtype, ar_handle_t *out) {
+    if (!out)
+        return AR_ERR_INVALID;
+    *out = nullptr;
+    if (R < 1 || R > AR_MAX_RANKS || N < 1 || !valid_dtype(dtype))
+        return AR_ERR_INVALID;
+    const size_t esz = elem_size(dtype);
+    if (N > ((size_t)1 << 40) / esz)
+        return AR_ERR_INVALID;
+
+    ar_handle *h = new (std::nothrow) ar_handle();
+    if (!h)
+        return AR_ERR_NOMEM;
+    h->R = R;
+    h->N = N;
+    h->dtype = dtype;
+    h->esz = esz;
+    if (cudaGetDevice(&h->device) != cudaSuccess ||
+        cudaDeviceGetAttribute(&h->num_sms, cudaDevAttrMultiProcessorCount, h->device) !=
+            cudaSuccess) {
+        delete h;
+        return AR_ERR_CUDA;
+    }
+
+    // two-shot shard: ceil(N / R) rounded up to a whole 16-byte vector
+    const uint64_t per_vec = 16 / esz;
+    h->shard = ceil_div(ceil_div(N, (uint64_t)R), per_vec) * per_vec;
+
+    // device memory: [status, abort | epoch words | LL slots]
+    const size_t ctl_bytes = 256;
+    const size_t epoch_bytes = sizeof(uint32_t) * kEpochWords;
+    const bool ll_capable = N * esz <= AR_LL_MAX_BYTES;
+    h->ppad = ll_capable ? ceil_div(ceil_div(N * esz, 4), 4) * 4 : 0;
+    const size_t slot_bytes = ll_capable ? (size_t)(R + 1) * h->ppad * sizeof(uint64_t) : 0;
+    h->dev_bytes = ctl_bytes + epoch_bytes + slot_bytes;
+    if (cudaMalloc(&h->dev_mem, h->dev_bytes) != cudaSuccess) {
+        (void)cudaGetLastError();
+        delete h;
+        return AR_ERR_NOMEM;
+    }
+    if (cudaMemset(h->dev_mem, 0, h->dev_bytes) != cudaSuccess ||
+        cudaDeviceSynchronize() != cudaSuccess) {
+        cudaFree(h->dev_mem);
+        delete h;
+        return AR_ERR_CUDA;
+    }
+    uint8_t *base = static_cast<uint8_t *>(h->dev_mem);
+    h->ctl.status = reinterpret_cast<int *>(base);
+    h->ctl.abort = reinterpret_cast<uint32_t *>(base + 4);
+    h->ctl.epoch = reinterpret_cast<uint32_t *>(base + ctl_bytes);
+    h->ctl.timeout_ns = kDefaultTimeoutNs;
+    h->ctl.drop_rank = -1;
+    h->slots = ll_capable ? reinterpret_cast<uint64_t *>(base + ctl_bytes + epoch_bytes) : nullptr;
+
+    // launch shapes
+    int err = 0;
+    for (int v = 0; v < 2; ++v)
+        for (int t = 0; t < 2; ++t) {
+            int per_sm = 0;
+            err |= ll_occupancy(dtype, v != 0, t != 0, &per_sm) != cudaSuccess;
+            h->ll_cap[v][t] = per_sm * h->num_sms;
+        }
+    h->one_shot_warps = R <= 8 ? R * ((8 + R - 1) / R) : R;
+    h->one_shot_cap = h->num_sms * (2048 / (32 * h->one_shot_warps));
+    h->reg_cap = h->num_sms * (2048 / kRegThreads);
+    int tile = (int)((64 * 1024 / R) / 16 * 16);
+    if (tile > 8192)
+        tile = 8192;
+    if (tile < 1024)
+        tile = 1024;
+    int stages = (int)((220 * 1024 - 2 * tile) / ((size_t)R * tile));
+    if (stages > kTmaMaxStages)
+        stages = kTmaMaxStages;
+    if (stages < 2)
+        stages = 2;
+    h->tma_tile = tile;
+    h->tma_stages = stages;
+    err |= tma_prepare(dtype) != cudaSuccess;
+    if (err) {
+        (void)cudaGetLastError();
+        cudaFree(h->dev_mem);
+        delete h;
+        return AR_ERR_CUDA;
+    }
+    *out = h;
+    return AR_OK;
+}
+
+int ar_destroy(ar_handle_t h) {
+    if (!h)
+        return AR_OK;
+    int rc = AR_OK;
+    if (cudaDeviceSynchronize() != cudaSuccess)
+        rc = AR_ERR_CUDA;
+    if (cudaFree(h->dev_mem) != cudaSuccess)
+        rc = AR_ERR_CUDA;
+    delete h;
+    return rc;
+}
+
+int ar_allreduce(ar_handle_t h, const void *const in[], void *const out[], int algo, int proto,
+                 cudaStream_t stream) {
+    if (!in)
+        return AR_ERR_INVALID;
+    bool vec16, vec8, inplace;
+    const int rc = check_buffers(h, in, out, &vec16, &vec8, &inplace);
+    if (rc != AR_OK)
+        return rc;
+    if (algo != AR_ONE_SHOT && algo != AR_TWO_SHOT)
+        return AR_ERR_INVALID;
+    if (proto == AR_HB)
+        return algo == AR_ONE_SHOT ? one_shot_hb(h, in, out, vec16, inplace, stream)
+                                   : two_shot_hb(h, in, out, vec16, inplace, stream);
+    if (proto == AR_LL)
+        return ll(h, in, out, vec8, algo == AR_TWO_SHOT, stream);
+    return AR_ERR_INVALID;
+}
+
+int ar_reduce_scatter(ar_handle_t h, const void *const in[], void *const out[],
+                      cudaStream_t stream) {
+    if (!in)
+        return AR_ERR_INVALID;
+    bool vec16, vec8, inplace;
+    const int rc = check_buffers(h, in, out, &vec16, &vec8, &inplace);
+    if (rc != AR_OK)
+        return rc;
+    const HbArgs a = hb_args(h, in, out, inplace);
+    const uint64_t units = vec16 ? h->N / (16 / h->esz) : h->N;
+    const int grid = clamp_grid(ceil_div(units, kRegThreads), h->reg_cap);
+    return from_cuda(launch_reduce(a, h->dtype, vec16, true, grid, stream));
+}
+
+int ar_all_gather(ar_handle_t h, void *const out[], cudaStream_t stream) {
+    bool vec16, vec8, inplace;
+    const int rc = check_buffers(h, nullptr, out, &vec16, &vec8, &inplace);
+    if (rc != AR_OK)
+        return rc;
+    const HbArgs a = hb_args(h, nullptr, out, false);
+    const uint64_t units = vec16 ? h->N / (16 / h->esz) : h->N;
+    const int grid = clamp_grid(ceil_div(units, kRegThreads), h->reg_cap);
+    return from_cuda(launch_all_gather(a, h->dtype, vec16, grid, stream));
+}
+
+int ar_ll_pack(ar_handle_t h, const void *src, uint64_t *pkts, size_t n, uint32_t flag,
+               cudaStream_t stream) {
+    if (!h || !src || !pkts || !on_device(h))
+        return AR_ERR_INVALID;
+    if (((uintptr_t)src % h->esz) != 0 || ((uintptr_t)pkts % 8) != 0)
+        return AR_ERR_INVALID;
+    if (n == 0)
+        return AR_OK;
+    PackArgs a = {};
+    a.src = src;
+    a.pkts = pkts;
+    a.n = n;
+    a.flag = flag;
+    a.status = h->ctl.status;
+    const bool vec = ((uintptr_t)src % 8) == 0 && ((uintptr_t)pkts % 16) == 0;
+    const int grid = clamp_grid(ceil_div(ceil_div(n * h->esz, 8), kRegThreads), h->reg_cap);
+    return from_cuda(launch_pack(a, h->dtype, vec, grid, stream));
+}
+
+int ar_ll_unpack(ar_handle_t h, const uint64_t *pkts, void *dst, size_t n, uint32_t flag,
+                 cudaStream_t stream) {
+    if (!h || !dst || !pkts || !on_device(h))
+        return AR_ERR_INVALID;
+    if (((uintptr_t)dst % h->esz) != 0 || ((uintptr_t)pkts % 8) != 0)
+        return AR_ERR_INVALID;
+    if (n == 0)
+        return AR_OK;
+    PackArgs a = {};
+    a.dst = dst;
+    a.cpkts = pkts;
+    a.n = n;
+    a.flag = flag;
+    a.status = h->ctl.status;
+    const bool vec = ((uintptr_t)dst % 8) == 0 && ((uintptr_t)pkts % 16) == 0;
+    const int grid = clamp_grid(ceil_div(ceil_div(n * h->esz, 8), kRegThreads), h->reg_cap);
+    return from_cuda(launch_unpack(a, h->dtype, vec, grid, stream));
+}
+
+int ar_status(ar_handle_t h, cudaStream_t stream) {
+    if (!h)
+        return AR_ERR_INVALID;
+    if (cudaStreamSynchronize(stream) != cudaSuccess)
+        return from_cuda(cudaErrorUnknown);
+    int code = 0;
+    if (cudaMemcpyAsync(&code, h->ctl.status, sizeof(int), cudaMemcpyDeviceToHost, stream) !=
+            cudaSuccess ||
+        cudaMemsetAsync(h->ctl.status, 0, sizeof(int), stream) != cudaSuccess ||
+        cudaStreamSynchronize(stream) != cudaSuccess)
+        return from_cuda(cudaErrorUnknown);
+    return code;
+}
+
+int ar_set_timeout(ar_handle_t h, uint64_t ns) {
+    if (!h)
+        return AR_ERR_INVALID;
+    h->ctl.timeout_ns = ns ? ns : kDefaultTimeoutNs;
+    return AR_OK;
+}
+
+int ar_debug_drop_rank(ar_handle_t h, int rank) {
+    if (!h || rank < -1 || rank >= h->R)
+        return AR_ERR_INVALID;
+    h->ctl.drop_rank = rank;
+    return AR_OK;
+}
+
+int ar_round(int dtype, const float *src, void *dst, size_t n, cudaStream_t stream) {
+    if (!valid_dtype(dtype) || !src || !dst)
+        return AR_ERR_INVALID;
+    if (((uintptr_t)src % 4) != 0 || ((uintptr_t)dst % elem_size(dtype)) != 0)
+        return AR_ERR_INVALID;
+    if (n == 0)
+        return AR_OK;
+    const int grid = clamp_grid(ceil_div(n, kRegThreads), 4096);
+    return from_cuda(launch_round(dtype, src, dst, n, grid, stream));
+}
+
+int ar_get_info(ar_handle_t h, ar_info *info) {
+    if (!h || !info)
+        return AR_ERR_INVALID;
+    info->R = h->R;
+    info->dtype = h->dtype;
+    info->N = h->N;
+    info->elem_size = h->esz;
+    info->ll_capable = h->slots != nullptr;
+    info->ll_packets_per_rank = (h->N * h->esz + 3) / 4;
+    info->scratch_bytes = h->dev_bytes;
+    info->num_sms = h->num_sms;
+    info->ll_ctas_per_rank_max = h->ll_cap[1][0] / h->R;
+    info->tma_tile_bytes = h->tma_tile;
+    info->tma_stages = h->tma_stages;
+    info->timeout_ns = h->ctl.timeout_ns;
+    return AR_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,282 @@
+// Register-path kernels: one-shot HB, the reduce-scatter step, a fused
+// two-shot (reduce once, store to every output) used where TMA cannot be
+// (unaligned buffers), the all-gather step, and the standalone rounding.
+//
+// Sources: the one-shot and the reduce-scatter + all-gather ("rsag")
+// all-reduce algorithms of "SGLang 中的 MSCCL++ All-Reduce 基准测试与推理集成指南",
+// section 4.4; HB = bulk transfer with little synchronisation ("【论文分享】
+// MSCCL++：让 GPU 通信像 CUDA 一样可编程", section "MemoryChannel", protocol
+// table).
+#include "ar_device.cuh"
+
+namespace ar {
+
+// Fold R ranks' 16-byte vectors at vector index u, ranks 0..R-1 in order.
+// Loads are issued eight ranks at a time so that they overlap.
+template <int DT, bool L1>
+__device__ __forceinline__ uint4 fold_vec(const void *const *in, int R, uint64_t u) {
+    VecAcc<DT> acc;
+#pragma unroll 1
+    for (int k0 = 0; k0 < R; k0 += 8) {
+        uint4 v[8];
+#pragma unroll
+        for (int j = 0; j < 8; ++j)
+            if (k0 + j < R) {
+                const uint4 *p = reinterpret_cast<const uint4 *>(in[k0 + j]) + u;
+                v[j] = L1 ? ld_v4_l1(p) : ld_v4_stream(p);
+            }
+#pragma unroll
+        for (int j = 0; j < 8; ++j)
+            if (k0 + j < R) {
+                if (k0 + j == 0)
+                    acc.init(v[j]);
+                else
+                    acc.add(v[j]);
+            }
+    }
+    return acc.result();
+}
+
+// Fold one element i.
+template <int DT>
+__device__ __forceinline__ uint32_t fold_elem(const void *const *in, int R, uint64_t i) {
+    ElemAcc<DT> acc;
+    acc.init(ld_elem<DT>(in[0], i));
+    for (int k = 1; k < R; ++k)
+        acc.add(ld_elem<DT>(in[k], i));
+    return acc.result();
+}
+
+// ---------------------------------------------------------------------------
+// One-shot HB.  Virtual rank r's output reads all R inputs: warp w of a CTA
+// computes out[w % R] for a run of 32 units (16-byte vectors, or elements
+// when some buffer is not 16-byte aligned), so the R warps that read the
+// same input lines run side by side and the lines come from HBM once, the
+// other R - 1 reads hitting L1/L2.  In place (in[r] == out[r]) is safe: a
+// CTA's units belong to it alone, and it finishes every read of its units
+// (barrier) before any store.
+// ---------------------------------------------------------------------------
+template <int DT, bool VEC>
+__global__ void __launch_bounds__(1024) k_one_shot_hb(const __grid_constant__ HbArgs a) {
+    constexpr int PV = VEC ? Elem<DT>::kPerVec : 1;
+    const int R = a.R;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int W = blockDim.x >> 5;
+    const int r = warp % R;
+    const int g = warp / R;
+    const int m = W / R;
+    const uint64_t units = a.n / PV;
+    const uint64_t per_blk = (uint64_t)m * 32;
+    const uint64_t nblk = (units + per_blk - 1) / per_blk;
+
+    for (uint64_t blk = blockIdx.x; blk < nblk; blk += gridDim.x) {
+        const uint64_t u = blk * per_blk + (uint64_t)g * 32 + lane;
+        const bool live = u < units && g < m;
+        if (VEC) {
+            uint4 res = make_uint4(0, 0, 0, 0);
+            if (live)
+                res = fold_vec<DT, true>(a.p.in, R, u);
+            if (a.inplace)
+                __syncthreads();
+            if (live)
+                st_v4(reinterpret_cast<uint4 *>(a.p.out[r]) + u, res);
+        } else {
+            uint32_t res = 0;
+            if (live)
+                res = fold_elem<DT>(a.p.in, R, u);
+            if (a.inplace)
+                __syncthreads();
+            if (live)
+                st_elem<DT>(a.p.out[r], u, res);
+        }
+    }
+
+    // Ragged tail (fewer than one vector of elements): the last CTA, one
+    // thread per (element, rank), all reads before any store.
+    if (VEC && blockIdx.x == gridDim.x - 1) {
+        const uint64_t first = units * PV;
+        const int tail = (int)(a.n - first);
+        const int t = threadIdx.x;
+        const bool live = t < tail * R;
+        uint32_t res = 0;
+        if (live)
+            res = fold_elem<DT>(a.p.in, R, first + t / R);
+        __syncthreads();
+        if (live)
+            st_elem<DT>(a.p.out[t % R], first + t / R, res);
+    }
+}
+
+// ---------------------------------------------------------------------------
+// Reduce: one thread per unit folds the R inputs once, then stores either to
+// the output of the unit's shard owner only (reduce-scatter step) or to all
+// R outputs (fused two-shot).  The thread reads everything before it writes
+// and no other thread touches its unit, so in place is safe.
+// ---------------------------------------------------------------------------
+template <int DT, bool VEC, bool SCATTER>
+__global__ void __launch_bounds__(kRegThreads) k_reduce(const __grid_constant__ HbArgs a) {
+    constexpr int PV = VEC ? Elem<DT>::kPerVec : 1;
+    const int R = a.R;
+    const uint64_t units = a.n / PV;
+    const uint64_t stride = (uint64_t)gridDim.x * blockDim.x;
+    for (uint64_t u = (uint64_t)blockIdx.x * blockDim.x + threadIdx.x; u < units; u += stride) {
+        const int owner = (int)((u * PV) / a.shard);
+        if (VEC) {
+            const uint4 res = fold_vec<DT, false>(a.p.in, R, u);
+            if (SCATTER) {
+                st_v4(reinterpret_cast<uint4 *>(a.p.out[owner]) + u, res);
+            } else {
+                for (int r = 0; r < R; ++r)
+                    st_v4(reinterpret_cast<uint4 *>(a.p.out[r]) + u, res);
+            }
+        } else {
+            const uint32_t res = fold_elem<DT>(a.p.in, R, u);
+            if (SCATTER) {
+                st_elem<DT>(a.p.out[owner], u, res);
+            } else {
+                for (int r = 0; r < R; ++r)
+                    st_elem<DT>(a.p.out[r], u, res);
+            }
+        }
+    }
+    if (VEC && blockIdx.x == 0) {
+        const uint64_t i = units * PV + threadIdx.x;
+        if (i < a.n) {
+            const uint32_t res = fold_elem<DT>(a.p.in, R, i);
+            const int owner = (int)(i / a.shard);
+            if (SCATTER) {
+                st_elem<DT>(a.p.out[owner], i, res);
+            } else {
+                for (int r = 0; r < R; ++r)
+                    st_elem<DT>(a.p.out[r], i, res);
+            }
+        }
+    }
+}
+
+// ---------------------------------------------------------------------------
+// All-gather: every unit of shard j is read once from out[j] and stored to
+// the R - 1 other outputs (a copy: bits unchanged).
+// ---------------------------------------------------------------------------
+template <int ESZ, bool VEC>
+__global__ void __launch_bounds__(kRegThreads) k_all_gather(const __grid_constant__ HbArgs a) {
+    constexpr int PV = VEC ? 16 / ESZ : 1;
+    const int R = a.R;
+    const uint64_t units = a.n / PV;
+    const uint64_t stride = (uint64_t)gridDim.x * blockDim.x;
+    for (uint64_t u = (uint64_t)blockIdx.x * blockDim.x + threadIdx.x; u < units; u += stride) {
+        const int owner = (int)((u * PV) / a.shard);
+        if (VEC) {
+            const uint4 v = ld_v4_stream(reinterpret_cast<const uint4 *>(a.p.out[owner]) + u);
+            for (int r = 0; r < R; ++r)
+                if (r != owner)
+                    st_v4(reinterpret_cast<uint4 *>(a.p.out[r]) + u, v);
+        } else if (ESZ == 2) {
+            const uint16_t v = reinterpret_cast<const uint16_t *>(a.p.out[owner])[u];
+            for (int r = 0; r < R; ++r)
+                if (r != owner)
+                    reinterpret_cast<uint16_t *>(a.p.out[r])[u] = v;
+        } else {
+            const uint32_t v = reinterpret_cast<const uint32_t *>(a.p.out[owner])[u];
+            for (int r = 0; r < R; ++r)
+                if (r != owner)
+                    reinterpret_cast<uint32_t *>(a.p.out[r])[u] = v;
+        }
+    }
+    if (VEC && blockIdx.x == 0) {
+        const uint64_t i = units * PV + threadIdx.x;
+        if (i < a.n) {
+            const int owner = (int)(i / a.shard);
+            for (int r = 0; r < R; ++r) {
+                if (r == owner)
+                    continue;
+                if (ESZ == 2)
+                    reinterpret_cast<uint16_t *>(a.p.out[r])[i] =
+                        reinterpret_cast<const uint16_t *>(a.p.out[owner])[i];
+                else
+                    reinterpret_cast<uint32_t *>(a.p.out[r])[i] =
+                        reinterpret_cast<const uint32_t *>(a.p.out[owner])[i];
+            }
+        }
+    }
+}
+
+// ---------------------------------------------------------------------------
+// The final rounding on its own (exposes narrow1 for exhaustive checks).
+// ---------------------------------------------------------------------------
+template <int DT>
+__global__ void __launch_bounds__(kRegThreads) k_round(const float *src, void *dst, uint64_t n) {
+    const uint64_t stride = (uint64_t)gridDim.x * blockDim.x;
+    for (uint64_t i = (uint64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += stride)
+        st_elem<DT>(dst, i, narrow1<DT>(src[i]));
+}
+
+// ---------------------------------------------------------------------------
+// Launchers.
+// ---------------------------------------------------------------------------
+template <int DT>
+static cudaError_t one_shot_dt(const HbArgs &a, bool vec, int grid, int block, cudaStream_t s) {
+    if (vec)
+        k_one_shot_hb<DT, true><<<grid, block, 0, s>>>(a);
+    else
+        k_one_shot_hb<DT, false><<<grid, block, 0, s>>>(a);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_one_shot_hb(const HbArgs &a, int dtype, bool vec, int grid, int block,
+                               cudaStream_t s) {
+    switch (dtype) {
+    case AR_BF16: return one_shot_dt<AR_BF16>(a, vec, grid, block, s);
+    case AR_FP16: return one_shot_dt<AR_FP16>(a, vec, grid, block, s);
+    default: return one_shot_dt<AR_FP32>(a, vec, grid, block, s);
+    }
+}
+
+template <int DT>
+static cudaError_t reduce_dt(const HbArgs &a, bool vec, bool scatter, int grid, cudaStream_t s) {
+    if (vec && scatter)
+        k_reduce<DT, true, true><<<grid, kRegThreads, 0, s>>>(a);
+    else if (vec)
+        k_reduce<DT, true, false><<<grid, kRegThreads, 0, s>>>(a);
+    else if (scatter)
+        k_reduce<DT, false, true><<<grid, kRegThreads, 0, s>>>(a);
+    else
+        k_reduce<DT, false, false><<<grid, kRegThreads, 0, s>>>(a);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_reduce(const HbArgs &a, int dtype, bool vec, bool scatter_only, int grid,
+                          cudaStream_t s) {
+    switch (dtype) {
+    case AR_BF16: return reduce_dt<AR_BF16>(a, vec, scatter_only, grid, s);
+    case AR_FP16: return reduce_dt<AR_FP16>(a, vec, scatter_only, grid, s);
+    default: return reduce_dt<AR_FP32>(a, vec, scatter_only, grid, s);
+    }
+}
+
+cudaError_t launch_all_gather(const HbArgs &a, int dtype, bool vec, int grid, cudaStream_t s) {
+    if (elem_size(dtype) == 2) {
+        if (vec)
+            k_all_gather<2, true><<<grid, kRegThreads, 0, s>>>(a);
+        else
+            k_all_gather<2, false><<<grid, kRegThreads, 0, s>>>(a);
+    } else {
+        if (vec)
+            k_all_gather<4, true><<<grid, kRegThreads, 0, s>>>(a);
+        else
+            k_all_gather<4, false><<<grid, kRegThreads, 0, s>>>(a);
+    }
+    return cudaGetLastError();
+}
+
+cudaError_t launch_round(int dtype, const float *src, void *dst, uint64_t n, int grid,
+                         cudaStream_t s) {
+    switch (dtype) {
+    case AR_BF16: k_round<AR_BF16><<<grid, kRegThreads, 0, s>>>(src, dst, n); break;
+    case AR_FP16: k_round<AR_FP16><<<grid, kRegThreads, 0, s>>>(src, dst, n); break;
+    default: k_round<AR_FP32><<<grid, kRegThreads, 0, s>>>(src, dst, n); break;
+    }
+    return cudaGetLastError();
+}
+
+}  // namespace ar

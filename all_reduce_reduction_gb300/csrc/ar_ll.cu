@@ -1,0 +1,356 @@
+// LL protocol kernels: one-shot and two-shot all-reduce through flag-tagged
+// 8-byte packets, and the standalone packet encode/decode.
+//
+// Sources: the LL protocol (small granularity, frequent synchronisation, for
+// decode, sampling and small messages) of the MemoryChannel in
+// "【论文分享】MSCCL++：让 GPU 通信像 CUDA 一样可编程", section "MemoryChannel",
+// protocol table; its one-sided put/signal/wait primitives ("microsoft/mscclpp"
+// project page, "How it works"); the one-shot packet and the reduce-scatter +
+// all-gather all-reduce algorithms of "SGLang 中的 MSCCL++ All-Reduce 基准测试与
+// 推理集成指南", section 4.4.
+//
+// Virtual peers.  The R ranks' kernels are emulated as one kernel over all
+// ranks' data: CTA b works for virtual rank r = b % R (CTA gi = b / R of its
+// G CTAs).  A rank "puts" its input into its own slot of the handle's
+// scratch as packets (payload + this call's flag in one 8-byte store); the
+// peers' CTAs poll those packets until the flag matches.  All peers share
+// one HBM, so one slot per sender serves every receiver.  There is no grid
+// barrier: producers and consumers meet only through packet flags.
+//
+// Forward progress.  Consumers wait for packets that other CTAs produce, so
+// all CTAs must be resident together: the launch is cooperative and its grid
+// never exceeds the occupancy-derived capacity.  Every CTA performs all of
+// its puts before any of its waits, and in the two-shot kernel all of its
+// reduce-scatter work before any all-gather wait, so every wait depends only
+// on work that resident CTAs do without waiting.  Waits are bounded anyway.
+//
+// In place (in[r] == out[r]) is safe: the CTA that writes out[r]'s unit u is
+// the CTA that read in[r]'s unit u into packets, earlier.
+#include "ar_device.cuh"
+
+namespace ar {
+
+// Payload word q (message bytes [4q, 4q + 4), zero past the end) of an
+// n-element buffer, element by element (any alignment of the buffer).
+template <int ESZ>
+__device__ __forceinline__ uint32_t load_payload(const void *base, uint64_t n, uint64_t q) {
+    if (ESZ == 4)
+        return reinterpret_cast<const uint32_t *>(base)[q];
+    const uint16_t *b = reinterpret_cast<const uint16_t *>(base);
+    const uint32_t lo = b[2 * q];
+    const uint32_t hi = (2 * q + 1 < n) ? (uint32_t)b[2 * q + 1] : 0u;
+    return lo | (hi << 16);
+}
+
+template <int ESZ>
+__device__ __forceinline__ void store_payload(void *base, uint64_t n, uint64_t q, uint32_t pl) {
+    if (ESZ == 4) {
+        reinterpret_cast<uint32_t *>(base)[q] = pl;
+        return;
+    }
+    uint16_t *b = reinterpret_cast<uint16_t *>(base);
+    b[2 * q] = (uint16_t)pl;
+    if (2 * q + 1 < n)
+        b[2 * q + 1] = (uint16_t)(pl >> 16);
+}
+
+__device__ __forceinline__ uint2 ld_v2(const void *p) {
+    uint2 v;
+    asm volatile("ld.global.L1::no_allocate.v2.u32 {%0, %1}, [%2];"
+                 : "=r"(v.x), "=r"(v.y) : "l"(p));
+    return v;
+}
+__device__ __forceinline__ void st_v2(void *p, uint2 v) {
+    asm volatile("st.global.v2.u32 [%0], {%1, %2};" :: "l"(p), "r"(v.x), "r"(v.y) : "memory");
+}
+
+// Fold the packet pair at `base` (packet offset inside a slot) of slots
+// 0..R-1, in rank order.  Loads of eight ranks are issued before any flag is
+// checked, so a ready message costs one round trip per eight ranks.
+template <int DT>
+__device__ __forceinline__ bool fold_pair(Poller &w, const uint64_t *base, uint64_t ppad, int R,
+                                          uint2 &out) {
+    WordAcc<DT> a0, a1;
+#pragma unroll 1
+    for (int k0 = 0; k0 < R; k0 += 8) {
+        uint64_t p0[8], p1[8];
+#pragma unroll
+        for (int j = 0; j < 8; ++j)
+            if (k0 + j < R)
+                ld_pkt2(base + (uint64_t)(k0 + j) * ppad, p0[j], p1[j]);
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            if (k0 + j < R) {
+                if (pkt_flag(p0[j]) != w.flag || pkt_flag(p1[j]) != w.flag) {
+                    if (!poll_pkt2(w, base + (uint64_t)(k0 + j) * ppad, p0[j], p1[j]))
+                        return false;
+                }
+                if (k0 + j == 0) {
+                    a0.init(pkt_payload(p0[j]));
+                    a1.init(pkt_payload(p1[j]));
+                } else {
+                    a0.add(pkt_payload(p0[j]));
+                    a1.add(pkt_payload(p1[j]));
+                }
+            }
+        }
+    }
+    out = make_uint2(a0.result(), a1.result());
+    return true;
+}
+
+// Same for a single packet.
+template <int DT>
+__device__ __forceinline__ bool fold_one(Poller &w, const uint64_t *base, uint64_t ppad, int R,
+                                         uint32_t &out) {
+    WordAcc<DT> acc;
+#pragma unroll 1
+    for (int k0 = 0; k0 < R; k0 += 8) {
+        uint64_t p[8];
+#pragma unroll
+        for (int j = 0; j < 8; ++j)
+            if (k0 + j < R)
+                p[j] = ld_pkt(base + (uint64_t)(k0 + j) * ppad);
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            if (k0 + j < R) {
+                if (pkt_flag(p[j]) != w.flag && !poll_pkt(w, base + (uint64_t)(k0 + j) * ppad, p[j]))
+                    return false;
+                if (k0 + j == 0)
+                    acc.init(pkt_payload(p[j]));
+                else
+                    acc.add(pkt_payload(p[j]));
+            }
+        }
+    }
+    out = acc.result();
+    return true;
+}
+
+// Units: with VEC every in/out buffer is 8-byte aligned and a unit is 8
+// message bytes = two packets; the last (< 8) bytes travel as single packets
+// handled by CTA gi == 0 of each rank.  Without VEC every packet is single.
+template <int DT, bool VEC, bool TWO>
+__global__ void __launch_bounds__(kLlThreads) k_ll(const __grid_constant__ LlArgs a) {
+    constexpr int ESZ = Elem<DT>::kSize;
+    const int R = a.R, G = a.G;
+    const int r = blockIdx.x % R, gi = blockIdx.x / R;
+    const uint64_t tid = threadIdx.x, T = blockDim.x;
+    const uint32_t flag = call_flag(a.c);
+    Poller w{&a.c, flag, 0};
+
+    const uint64_t nbytes = a.n * ESZ;
+    const uint64_t P = (nbytes + 3) / 4;                  // packets per rank
+    const uint64_t U = nbytes / 8;                        // packet pairs (VEC)
+    const uint64_t first1 = VEC ? 2 * U : 0;              // first single packet
+    // this thread's single packets (same set in every phase that uses them)
+    const uint64_t q0 = VEC ? (gi == 0 ? first1 + tid : P) : (uint64_t)gi * T + tid;
+    const uint64_t qstep = VEC ? T : (uint64_t)G * T;
+    const uint64_t ustart = (uint64_t)gi * T + tid, ustep = (uint64_t)G * T;
+
+    const uint64_t ppad = a.ppad;
+    uint64_t *const slot_r = a.slots + (uint64_t)r * ppad;
+    uint64_t *const res = a.slots + (uint64_t)R * ppad;   // two-shot results
+    bool ok = true;
+
+    // ---- put: rank r's input -> slot r (one 8-byte store per packet) -------
+    if (a.c.drop_rank != r) {
+        if constexpr (VEC) {
+            const uint2 *src = reinterpret_cast<const uint2 *>(a.p.in[r]);
+            for (uint64_t u = ustart; u < U; u += ustep) {
+                const uint2 v = ld_v2(src + u);
+                st_pkt2(slot_r + 2 * u, make_pkt(v.x, flag), make_pkt(v.y, flag));
+            }
+        }
+        for (uint64_t q = q0; q < P; q += qstep)
+            st_pkt(slot_r + q, make_pkt(load_payload<ESZ>(a.p.in[r], a.n, q), flag));
+    }
+
+    if (!TWO) {
+        // ---- one-shot: out[r] = fold of every slot -------------------------
+        if constexpr (VEC) {
+            uint2 *dst = reinterpret_cast<uint2 *>(a.p.out[r]);
+            for (uint64_t u = ustart; ok && u < U; u += ustep) {
+                uint2 y;
+                ok = fold_pair<DT>(w, a.slots + 2 * u, ppad, R, y);
+                if (ok)
+                    st_v2(dst + u, y);
+            }
+        }
+        for (uint64_t q = q0; ok && q < P; q += qstep) {
+            uint32_t y;
+            ok = fold_one<DT>(w, a.slots + q, ppad, R, y);
+            if (ok)
+                store_payload<ESZ>(a.p.out[r], a.n, q, y);
+        }
+    } else {
+        // ---- reduce-scatter: rank r folds shard r into result packets ------
+        const uint64_t shard_pk = a.shard * ESZ / 4;      // packets per shard
+        if constexpr (VEC) {
+            const uint64_t lo = (uint64_t)r * shard_pk / 2;
+            uint64_t hi = lo + shard_pk / 2;
+            if (hi > U)
+                hi = U;
+            for (uint64_t u = lo + ustart; ok && u < hi; u += ustep) {
+                uint2 y;
+                ok = fold_pair<DT>(w, a.slots + 2 * u, ppad, R, y);
+                if (ok)
+                    st_pkt2(res + 2 * u, make_pkt(y.x, flag), make_pkt(y.y, flag));
+            }
+            // single packets belong to the shard that holds them
+            if (gi == 0) {
+                for (uint64_t q = first1 + tid; ok && q < P; q += T) {
+                    int owner = (int)(q / shard_pk);
+                    if (owner > R - 1)
+                        owner = R - 1;
+                    if (owner != r)
+                        continue;
+                    uint32_t y;
+                    ok = fold_one<DT>(w, a.slots + q, ppad, R, y);
+                    if (ok)
+                        st_pkt(res + q, make_pkt(y, flag));
+                }
+            }
+        } else {
+            const uint64_t lo = (uint64_t)r * shard_pk;
+            uint64_t hi = lo + shard_pk;
+            if (hi > P)
+                hi = P;
+            for (uint64_t q = lo + ustart; ok && q < hi; q += ustep) {
+                uint32_t y;
+                ok = fold_one<DT>(w, a.slots + q, ppad, R, y);
+                if (ok)
+                    st_pkt(res + q, make_pkt(y, flag));
+            }
+        }
+        // ---- all-gather: out[r] <- result packets (same units as the put) --
+        if constexpr (VEC) {
+            uint2 *dst = reinterpret_cast<uint2 *>(a.p.out[r]);
+            for (uint64_t u = ustart; ok && u < U; u += ustep) {
+                uint64_t p0, p1;
+                ok = poll_pkt2(w, res + 2 * u, p0, p1);
+                if (ok)
+                    st_v2(dst + u, make_uint2(pkt_payload(p0), pkt_payload(p1)));
+            }
+        }
+        for (uint64_t q = q0; ok && q < P; q += qstep) {
+            uint64_t p;
+            ok = poll_pkt(w, res + q, p);
+            if (ok)
+                store_payload<ESZ>(a.p.out[r], a.n, q, pkt_payload(p));
+        }
+    }
+
+    publish_epoch(a.c, flag);
+}
+
+template <int DT, bool VEC, bool TWO> static const void *ll_kernel() {
+    return reinterpret_cast<const void *>(&k_ll<DT, VEC, TWO>);
+}
+
+static const void *ll_kernel_for(int dtype, bool vec, bool two) {
+#define AR_LL_PICK(DT)                                                                  \
+    return vec ? (two ? ll_kernel<DT, true, true>() : ll_kernel<DT, true, false>())     \
+               : (two ? ll_kernel<DT, false, true>() : ll_kernel<DT, false, false>());
+    switch (dtype) {
+    case AR_BF16: AR_LL_PICK(AR_BF16)
+    case AR_FP16: AR_LL_PICK(AR_FP16)
+    default: AR_LL_PICK(AR_FP32)
+    }
+#undef AR_LL_PICK
+}
+
+cudaError_t ll_occupancy(int dtype, bool vec, bool two_shot, int *blocks_per_sm) {
+    return cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks_per_sm,
+                                                         ll_kernel_for(dtype, vec, two_shot),
+                                                         kLlThreads, 0);
+}
+
+cudaError_t launch_ll(const LlArgs &a, int dtype, bool vec, bool two_shot, cudaStream_t s) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)(a.R * a.G));
+    cfg.blockDim = dim3(kLlThreads);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeCooperative;
+    attr[0].val.cooperative = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    void *args[] = {const_cast<LlArgs *>(&a)};
+    return cudaLaunchKernelExC(&cfg, ll_kernel_for(dtype, vec, two_shot), args);
+}
+
+// ---------------------------------------------------------------------------
+// Standalone encode / decode (ar_ll_pack, ar_ll_unpack).  With VEC the
+// message buffer is 8-byte aligned and the packets 16-byte aligned.
+// ---------------------------------------------------------------------------
+template <int ESZ, bool VEC>
+__global__ void __launch_bounds__(kRegThreads) k_pack(const __grid_constant__ PackArgs a) {
+    const uint64_t nbytes = a.n * ESZ, P = (nbytes + 3) / 4;
+    const uint64_t U = VEC ? nbytes / 8 : 0;
+    const uint64_t stride = (uint64_t)gridDim.x * blockDim.x;
+    const uint64_t t0 = (uint64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    for (uint64_t u = t0; VEC && u < U; u += stride) {
+        const uint2 v = ld_v2(reinterpret_cast<const uint2 *>(a.src) + u);
+        st_pkt2(a.pkts + 2 * u, make_pkt(v.x, a.flag), make_pkt(v.y, a.flag));
+    }
+    for (uint64_t q = 2 * U + t0; q < P; q += stride)
+        st_pkt(a.pkts + q, make_pkt(load_payload<ESZ>(a.src, a.n, q), a.flag));
+}
+
+template <int ESZ, bool VEC>
+__global__ void __launch_bounds__(kRegThreads) k_unpack(const __grid_constant__ PackArgs a) {
+    const uint64_t nbytes = a.n * ESZ, P = (nbytes + 3) / 4;
+    const uint64_t U = VEC ? nbytes / 8 : 0;
+    const uint64_t stride = (uint64_t)gridDim.x * blockDim.x;
+    const uint64_t t0 = (uint64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    bool bad = false;
+    for (uint64_t u = t0; VEC && u < U; u += stride) {
+        uint64_t p0, p1;
+        ld_pkt2(a.cpkts + 2 * u, p0, p1);
+        const bool g0 = pkt_flag(p0) == a.flag, g1 = pkt_flag(p1) == a.flag;
+        if (g0 && g1) {
+            st_v2(reinterpret_cast<uint2 *>(a.dst) + u, make_uint2(pkt_payload(p0), pkt_payload(p1)));
+        } else {
+            bad = true;
+            if (g0)
+                reinterpret_cast<uint32_t *>(a.dst)[2 * u] = pkt_payload(p0);
+            if (g1)
+                reinterpret_cast<uint32_t *>(a.dst)[2 * u + 1] = pkt_payload(p1);
+        }
+    }
+    for (uint64_t q = 2 * U + t0; q < P; q += stride) {
+        const uint64_t p = ld_pkt(a.cpkts + q);
+        if (pkt_flag(p) == a.flag)
+            store_payload<ESZ>(a.dst, a.n, q, pkt_payload(p));
+        else
+            bad = true;
+    }
+    if (bad)
+        record_error(a.status, AR_ERR_FLAG_MISMATCH);
+}
+
+cudaError_t launch_pack(const PackArgs &a, int dtype, bool vec, int grid, cudaStream_t s) {
+    if (elem_size(dtype) == 2) {
+        if (vec) k_pack<2, true><<<grid, kRegThreads, 0, s>>>(a);
+        else k_pack<2, false><<<grid, kRegThreads, 0, s>>>(a);
+    } else {
+        if (vec) k_pack<4, true><<<grid, kRegThreads, 0, s>>>(a);
+        else k_pack<4, false><<<grid, kRegThreads, 0, s>>>(a);
+    }
+    return cudaGetLastError();
+}
+
+cudaError_t launch_unpack(const PackArgs &a, int dtype, bool vec, int grid, cudaStream_t s) {
+    if (elem_size(dtype) == 2) {
+        if (vec) k_unpack<2, true><<<grid, kRegThreads, 0, s>>>(a);
+        else k_unpack<2, false><<<grid, kRegThreads, 0, s>>>(a);
+    } else {
+        if (vec) k_unpack<4, true><<<grid, kRegThreads, 0, s>>>(a);
+        else k_unpack<4, false><<<grid, kRegThreads, 0, s>>>(a);
+    }
+    return cudaGetLastError();
+}
+
+}  // namespace ar

@@ -1,0 +1,237 @@
+/*
+ * ar.h -- C ABI of a GB300 (sm_103a) sum all-reduce over R virtual ranks.
+ *
+ * The R ranks' buffers all live in one GPU's HBM ("virtual peers").  The
+ * library sums them element by element and writes the sum into every rank's
+ * output, with the schedules and protocols the MSCCL++ pages describe:
+ *
+ *   - the collective: a SUM all-reduce over the tensor-parallel ranks, called
+ *     after every attention and MLP output ("SGLang 中的 MSCCL++ All-Reduce
+ *     基准测试与推理集成指南", section 1), as a drop-in NCCL-style call
+ *     ("【论文分享】MSCCL++：让 GPU 通信像 CUDA 一样可编程", section
+ *     "第一层：Collective API");
+ *   - dtypes float32 / float16 / bfloat16 and the SUM operation only (SGLang
+ *     guide, section 4.3, run-time guard items 2 and 4);
+ *   - the one-shot packet algorithm and the reduce-scatter + all-gather
+ *     ("rsag") algorithm (SGLang guide, section 4.4);
+ *   - the LL (low latency: small granularity, frequent synchronisation) and
+ *     HB (high bandwidth: bulk transfer, little synchronisation) protocols of
+ *     the MemoryChannel (MSCCL++ summary, section "MemoryChannel", protocol
+ *     table);
+ *   - capture in a CUDA graph (SGLang guide, section 1, first selling point).
+ *
+ * Arithmetic: every element is widened to binary32, the ranks are folded
+ * left to right (rank 0 first, starting from rank 0's value) with one IEEE
+ * binary32 round-to-nearest-even add per rank, and the result is rounded once
+ * to the buffer dtype with round-to-nearest-even; no flush to zero.  Every
+ * schedule and protocol gives bit-identical results.
+ *
+ * Conventions for every function:
+ *   - The return value is an ar_status_code; AR_OK is 0.
+ *   - "Device pointer": memory the current CUDA device can read/write with
+ *     ordinary loads and stores (cudaMalloc, torch CUDA tensors, ...).  The
+ *     library does not check that a pointer is a device pointer.
+ *   - "Host array": a plain C array in host memory, read during the call only.
+ *   - Work is enqueued on `stream` and nothing waits for it, except in
+ *     ar_create, ar_destroy and ar_status.  No entry point used on the hot
+ *     path (ar_allreduce, ar_reduce_scatter, ar_all_gather, ar_ll_pack,
+ *     ar_ll_unpack, ar_round) allocates memory, copies between host and
+ *     device, or synchronises, so all of them can be captured in a CUDA graph.
+ *   - Calls on one handle must be ordered on the device (one stream, or
+ *     streams joined by events): the handle's scratch and its epoch words are
+ *     shared by all its calls.
+ *   - Call with the device that was current at ar_create current; otherwise
+ *     AR_ERR_INVALID.
+ *   - Errors detected on the host are returned immediately and nothing is
+ *     enqueued.  Errors detected on the device (a timed-out wait, a packet
+ *     with the wrong flag) are recorded in the handle's status word and
+ *     returned, then cleared, by ar_status.
+ */
+#ifndef AR_H
+#define AR_H
+
+#include <stddef.h>
+#include <stdint.h>
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Largest number of virtual ranks one handle serves. */
+#define AR_MAX_RANKS 32
+
+/* Largest message, in bytes per rank, the LL protocol accepts.  LL is the
+ * small-message protocol (MSCCL++ summary, "MemoryChannel" table: decode,
+ * sampling, small messages); its packets double the bytes moved, and larger
+ * messages belong to HB.  A handle whose N * sizeof(dtype) exceeds this
+ * gets AR_ERR_UNSUPPORTED for LL calls and allocates no LL scratch. */
+#define AR_LL_MAX_BYTES (64ull << 20)
+
+typedef struct ar_handle *ar_handle_t;
+
+/* Buffer element types (SGLang guide, section 4.3, guard item 2). */
+enum ar_dtype {
+    AR_BF16 = 0,
+    AR_FP16 = 1,
+    AR_FP32 = 2
+};
+
+/* Schedules (SGLang guide, section 4.4).
+ *   AR_ONE_SHOT: every virtual rank r reads all R inputs and writes its own
+ *                output out[r].
+ *   AR_TWO_SHOT: reduce-scatter then all-gather.  The elements are cut into
+ *                R shards (shard j: [j*S, min((j+1)*S, N)), S = ceil(N/R)
+ *                rounded up to a whole 16-byte vector); rank j reduces shard
+ *                j, then the reduced shard is copied to every output. */
+enum ar_algo {
+    AR_ONE_SHOT = 0,
+    AR_TWO_SHOT = 1
+};
+
+/* Protocols (MSCCL++ summary, section "MemoryChannel", protocol table).
+ *   AR_LL: inputs travel as 8-byte packets, 4 message bytes in the low half
+ *          and a 4-byte flag in the high half, written with one store; a
+ *          receiver polls each packet until its flag equals the call's flag,
+ *          so producers and consumers synchronise per packet inside one
+ *          kernel.  The flag comes from epoch words kept on the device, so
+ *          replays of a captured graph use a fresh flag every time.
+ *   AR_HB: bulk path.  Two-shot HB stages tiles through shared memory with
+ *          the Tensor Memory Accelerator (cp.async.bulk + mbarrier, no
+ *          multicast) when every buffer is 16-byte aligned. */
+enum ar_proto {
+    AR_LL = 0,
+    AR_HB = 1
+};
+
+enum ar_status_code {
+    AR_OK = 0,
+    AR_ERR_INVALID = 1,        /* bad argument (null, range, aliasing, device) */
+    AR_ERR_UNSUPPORTED = 2,    /* valid request this library does not serve   */
+    AR_ERR_CUDA = 3,           /* a CUDA runtime call failed                   */
+    AR_ERR_NOMEM = 4,          /* device allocation failed in ar_create        */
+    AR_ERR_TIMEOUT = 5,        /* device: a wait ran past the handle's timeout */
+    AR_ERR_FLAG_MISMATCH = 6   /* device: ar_ll_unpack met a packet whose flag
+                                  differs from the expected one               */
+};
+
+/* Description of a handle, filled by ar_get_info. */
+typedef struct ar_info {
+    int R;                     /* virtual ranks                                */
+    int dtype;                 /* enum ar_dtype                                */
+    size_t N;                  /* elements per rank                            */
+    size_t elem_size;          /* bytes per element                            */
+    int ll_capable;            /* 1 if N * elem_size <= AR_LL_MAX_BYTES        */
+    size_t ll_packets_per_rank;/* ceil(N * elem_size / 4)                      */
+    size_t scratch_bytes;      /* device bytes the handle owns                 */
+    int num_sms;               /* SMs of the handle's device                   */
+    int ll_ctas_per_rank_max;  /* co-resident CTAs per rank for LL kernels     */
+    int tma_tile_bytes;        /* per-rank tile of the two-shot TMA kernel     */
+    int tma_stages;            /* pipeline stages of the two-shot TMA kernel   */
+    uint64_t timeout_ns;       /* current device-side wait limit               */
+} ar_info;
+
+/* Create a handle for R virtual ranks of N elements of `dtype` each, on the
+ * current device.
+ *   R:     1 .. AR_MAX_RANKS.
+ *   N:     >= 1 elements per rank.
+ *   dtype: enum ar_dtype.
+ *   out:   receives the handle (host pointer, must not be NULL).
+ * Allocates the handle's device memory (status word, epoch words and, when
+ * N * elem_size <= AR_LL_MAX_BYTES, the LL packet scratch of (R + 1) slots of
+ * ceil(N * elem_size / 4) packets, rounded up to 4 packets), zeroes it and
+ * waits for that to finish.  Errors: AR_ERR_INVALID (R or N out of range,
+ * bad dtype, out == NULL), AR_ERR_NOMEM, AR_ERR_CUDA. */
+int ar_create(int R, size_t N, int dtype, ar_handle_t *out);
+
+/* Free the handle and its device memory.  Waits for the device first.
+ * NULL is accepted and ignored. */
+int ar_destroy(ar_handle_t h);
+
+/* Sum all-reduce: for every rank r and element i < N,
+ *   out[r][i] = round_dtype( in[0][i] + in[1][i] + ... + in[R-1][i] )
+ * with the binary32 left fold described at the top of this file.
+ *   in:    host array of R device pointers, N elements each.
+ *   out:   host array of R device pointers, N elements each.
+ *   algo:  enum ar_algo.   proto: enum ar_proto.
+ *   stream: the CUDA stream to enqueue on (0 = legacy default stream).
+ * Every pointer must be non-NULL and aligned to the element size; 16-byte
+ * alignment of all 2R pointers enables the vector paths, other alignments
+ * run an element-wise GPU path (same results).  Outputs must not overlap
+ * each other.  An input may overlap an output only as the same rank's
+ * buffer exactly (in[r] == out[r], in place); inputs may overlap each other.
+ * Errors: AR_ERR_INVALID (NULL handle or pointer, misaligned pointer,
+ * forbidden overlap, wrong device, bad algo/proto), AR_ERR_UNSUPPORTED (LL on
+ * a handle without LL scratch), AR_ERR_CUDA (launch failure).  Device-side
+ * errors (AR_ERR_TIMEOUT) are reported by ar_status. */
+int ar_allreduce(ar_handle_t h, const void *const in[], void *const out[],
+                 int algo, int proto, cudaStream_t stream);
+
+/* Reduce-scatter step of the two-shot schedule (HB): for every shard j,
+ *   out[j][i] = round_dtype(fold of in[0..R-1][i])  for i in shard j,
+ * and nothing else is written.  Shards as in enum ar_algo.  Arguments,
+ * alignment and aliasing rules as in ar_allreduce. */
+int ar_reduce_scatter(ar_handle_t h, const void *const in[], void *const out[],
+                      cudaStream_t stream);
+
+/* All-gather step of the two-shot schedule: for every shard j and rank
+ * r != j, copies out[j]'s shard j into out[r]'s shard j (bits unchanged).
+ *   out: host array of R device pointers, N elements each, not overlapping.
+ * ar_reduce_scatter followed by ar_all_gather on the same outputs equals
+ * ar_allreduce. */
+int ar_all_gather(ar_handle_t h, void *const out[], cudaStream_t stream);
+
+/* LL encode of one message of n elements of the handle's dtype.
+ *   src:  device pointer, n elements.
+ *   pkts: device pointer, ceil(n * elem_size / 4) 8-byte packets, 8-byte
+ *         aligned.  Packet p = ((uint64_t)flag << 32) | payload, payload =
+ *         message bytes [4p, 4p + 4) little-endian, zero past the end; so
+ *         two-byte elements 2p and 2p + 1 are its low and high halves and a
+ *         binary32 element p is its whole payload.
+ *   n:    0 is accepted and does nothing.
+ * Each packet is written with a single 8-byte store.  (Layout: the pages
+ * name the LL protocol but print no layout; this is the library's reading.)
+ * Errors: AR_ERR_INVALID (NULL, misaligned pointer). */
+int ar_ll_pack(ar_handle_t h, const void *src, uint64_t *pkts, size_t n,
+               uint32_t flag, cudaStream_t stream);
+
+/* LL decode: the inverse of ar_ll_pack.  A packet whose flag differs from
+ * `flag` leaves its bytes of dst unwritten and records AR_ERR_FLAG_MISMATCH
+ * in the handle's status word (read it with ar_status).  No waiting. */
+int ar_ll_unpack(ar_handle_t h, const uint64_t *pkts, void *dst, size_t n,
+                 uint32_t flag, cudaStream_t stream);
+
+/* Wait for `stream`, then return and clear the handle's device status word:
+ * AR_OK, AR_ERR_TIMEOUT or AR_ERR_FLAG_MISMATCH (the first error recorded
+ * since the last ar_status), or AR_ERR_CUDA if the stream reports a CUDA
+ * error. */
+int ar_status(ar_handle_t h, cudaStream_t stream);
+
+/* Limit, in nanoseconds, of every device-side wait (LL packet polls, TMA
+ * barrier waits) of later calls.  Default 1e9 (one second); 0 restores the
+ * default.  A wait past the limit records AR_ERR_TIMEOUT, makes the other
+ * waiters of the same call give up, and the kernel returns normally. */
+int ar_set_timeout(ar_handle_t h, uint64_t ns);
+
+/* Fault injection for tests: virtual rank `rank` (0..R-1) writes no LL
+ * packets in later LL calls, so its peers' polls time out (AR_ERR_TIMEOUT
+ * from ar_status) and the kernel returns.  -1 turns it off. */
+int ar_debug_drop_rank(ar_handle_t h, int rank);
+
+/* The final rounding step on its own: dst[i] = round_dtype(src[i]) for n
+ * binary32 values, with the same conversion the all-reduce kernels use
+ * (round to nearest even, no flush to zero).  src, dst: device pointers.
+ * Errors: AR_ERR_INVALID. */
+int ar_round(int dtype, const float *src, void *dst, size_t n, cudaStream_t stream);
+
+/* Fill *info (host pointer) with the handle's description. */
+int ar_get_info(ar_handle_t h, ar_info *info);
+
+/* Static string naming an ar_status_code. */
+const char *ar_strerror(int code);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* AR_H */

@@ -1,0 +1,255 @@
+"""GPU parity: every schedule and protocol against the CPU oracle, bit for bit.
+
+Inputs come from the seeded generator; the expected values from the oracle
+alone.  Outputs sit between canary zones that must stay untouched.
+"""
+import numpy as np
+import pytest
+import torch
+
+import all_reduce_reduction_gb300 as ar
+import oracle
+from all_reduce_reduction_gb300 import workload as wl
+from gpu_helpers import (ALL_PATHS, PATH_IDS, assert_bits_equal, check_guards, device_inputs,
+                         expected, guarded_outputs, need_gpu)
+
+pytestmark = pytest.mark.gpu
+
+DTYPES = ["bf16", "fp16", "fp32"]
+
+
+def run_case(R, n, dtype, algo, proto, dist="loguniform", config=40, offset=0, inplace=False):
+    need_gpu()
+    cpu = wl.make_inputs(config, R, n, dtype, dist)
+    want = expected(cpu, dtype)
+    ins = device_inputs(cpu, offset)
+    if inplace:
+        outs, bufs = ins, None
+    else:
+        bufs, outs = guarded_outputs(R, n, dtype, offset)
+    with ar.Handle(R, n, dtype) as h:
+        ar.ar_allreduce(h.h, ins, outs, algo, proto)
+        st = ar.ar_status(h.h)
+        assert st == ar.AR_OK, ar.ar_strerror(st)
+    for r in range(R):
+        assert_bits_equal(outs[r], want, dtype, "R=%d n=%d %s rank %d" % (R, n, dtype, r))
+    if bufs is not None:
+        check_guards(bufs, n, dtype, offset)
+
+
+def test_small_config_every_path():
+    """8 ranks x 512 bf16, uniform [-1, 1): the small workload."""
+    w = wl.SMALL
+    for algo, proto in ALL_PATHS:
+        run_case(w.R, w.n, w.dtype, algo, proto, dist=w.dist, config=w.config)
+
+
+@pytest.mark.parametrize("path", ALL_PATHS, ids=PATH_IDS)
+@pytest.mark.parametrize("dtype", DTYPES)
+@pytest.mark.parametrize("R", [1, 2, 3, 8, 16, 32])
+@pytest.mark.parametrize("n", [1, 3, 8, 9, 100, 4097, 70001])
+def test_parity_matrix(path, dtype, R, n):
+    run_case(R, n, dtype, *path)
+
+
+@pytest.mark.parametrize("path", ALL_PATHS, ids=PATH_IDS)
+@pytest.mark.parametrize("dtype", DTYPES)
+@pytest.mark.parametrize("R", [4, 16])
+def test_many_tiles_ragged_tail(path, dtype, R):
+    """Over a million elements: many TMA tiles / LL units, plus a ragged tail."""
+    run_case(R, (1 << 20) + 5, dtype, *path, dist="normal")
+
+
+@pytest.mark.parametrize("path", ALL_PATHS, ids=PATH_IDS)
+@pytest.mark.parametrize("dtype", DTYPES)
+@pytest.mark.parametrize("offset", [1, 2, 3])
+def test_misaligned_buffers(path, dtype, offset):
+    """Buffers off 16-byte alignment take the element-wise paths."""
+    if dtype == "fp32" and offset == 3:
+        offset = 1
+    run_case(5, 3001, dtype, *path, offset=offset)
+
+
+@pytest.mark.parametrize("path", ALL_PATHS, ids=PATH_IDS)
+@pytest.mark.parametrize("dtype", DTYPES)
+@pytest.mark.parametrize("n", [7, 4099, 300001])
+def test_in_place(path, dtype, n):
+    run_case(8, n, dtype, *path, inplace=True)
+
+
+@pytest.mark.parametrize("path", ALL_PATHS, ids=PATH_IDS)
+def test_in_place_misaligned(path):
+    run_case(3, 999, "bf16", *path, offset=1, inplace=True)
+
+
+@pytest.mark.parametrize("dtype", DTYPES)
+@pytest.mark.parametrize("R,n", [(4, 4097 * 3 + 3), (16, 1001), (5, 9), (32, 70001), (8, 1 << 20)])
+def test_reduce_scatter_then_all_gather(dtype, R, n):
+    need_gpu()
+    cpu = wl.make_inputs(41, R, n, dtype, "normal")
+    ins = device_inputs(cpu)
+    bufs, outs = guarded_outputs(R, n, dtype)
+    # oracle reduce-scatter on the same starting outputs (canary-filled)
+    start = [wl.bits(o.cpu()).copy() for o in outs]
+    want_rs = oracle.reduce_scatter([wl.bits(t) for t in cpu], wl.DTYPE_CODE[dtype], start)
+    with ar.Handle(R, n, dtype) as h:
+        ar.ar_reduce_scatter(h.h, ins, outs)
+        assert ar.ar_status(h.h) == ar.AR_OK
+        for r in range(R):
+            assert_bits_equal(outs[r], want_rs[r], dtype, "reduce-scatter rank %d" % r)
+        ar.ar_all_gather(h.h, outs)
+        assert ar.ar_status(h.h) == ar.AR_OK
+    want = expected(cpu, dtype)
+    for r in range(R):
+        assert_bits_equal(outs[r], want, dtype, "all-gather rank %d" % r)
+    check_guards(bufs, n, dtype)
+
+
+@pytest.mark.parametrize("dtype", DTYPES)
+@pytest.mark.parametrize("n", [1, 2, 3, 5, 64, 1001, 1 << 18])
+@pytest.mark.parametrize("offset", [0, 1])
+def test_ll_pack_unpack_vs_oracle(dtype, n, offset):
+    need_gpu()
+    x = wl.make_inputs(42, 1, n, dtype, "loguniform")[0]
+    flag = 0xC0FFEE00 + n
+    want = oracle.ll_pack(wl.bits(x), wl.DTYPE_CODE[dtype], flag)
+    src = device_inputs([x], offset)[0]
+    P = want.size
+    pk_buf = torch.zeros(P + 2, dtype=torch.int64, device="cuda")
+    pk = pk_buf[offset: offset + P]
+    with ar.Handle(1, n, dtype) as h:
+        ar.ar_ll_pack(h.h, src, pk, n, flag)
+        got = pk.cpu().numpy().view(np.uint64)
+        assert np.array_equal(got, want)
+        dst = torch.zeros(n + offset, dtype=x.dtype, device="cuda")[offset:]
+        ar.ar_ll_unpack(h.h, pk, dst, n, flag)
+        assert ar.ar_status(h.h) == ar.AR_OK
+        assert_bits_equal(dst, wl.bits(x), dtype, "unpack")
+        # a wrong flag: nothing written, mismatch reported
+        dst.zero_()
+        ar.ar_ll_unpack(h.h, pk, dst, n, flag + 1)
+        assert ar.ar_status(h.h) == ar.AR_ERR_FLAG_MISMATCH
+        assert int(dst.view(torch.int16 if dtype != "fp32" else torch.int32).abs().sum()) == 0
+        assert ar.ar_status(h.h) == ar.AR_OK        # cleared by the read
+
+
+@pytest.mark.parametrize("dtype", DTYPES)
+def test_ll_unpack_partial_mismatch(dtype):
+    need_gpu()
+    n = 37
+    x = wl.make_inputs(43, 1, n, dtype, "normal")[0]
+    pk = oracle.ll_pack(wl.bits(x), wl.DTYPE_CODE[dtype], 9)
+    pk[3] = (pk[3] & np.uint64(0xFFFFFFFF)) | (np.uint64(8) << np.uint64(32))
+    want = np.zeros(n, dtype=oracle.STORAGE[wl.DTYPE_CODE[dtype]])
+    want, bad = oracle.ll_unpack(pk, wl.DTYPE_CODE[dtype], n, 9, dst=want)
+    assert bad == 1
+    dpk = torch.from_numpy(pk.view(np.int64)).cuda()
+    dst = torch.zeros(n, dtype=x.dtype, device="cuda")
+    with ar.Handle(1, n, dtype) as h:
+        ar.ar_ll_unpack(h.h, dpk, dst, n, 9)
+        assert ar.ar_status(h.h) == ar.AR_ERR_FLAG_MISMATCH
+    assert_bits_equal(dst, want, dtype, "partial unpack")
+
+
+@pytest.mark.parametrize("path", ALL_PATHS, ids=PATH_IDS)
+def test_graph_replays_see_new_inputs(path):
+    """10 calls captured in one CUDA graph; the inputs change between replays.
+    A flag frozen at capture time would let LL receivers accept the previous
+    replay's packets; the device epoch must prevent that."""
+    need_gpu()
+    R, n, dtype = 8, 4096 + 3, "bf16"
+    algo, proto = path
+    ins = [torch.empty(n, dtype=torch.bfloat16, device="cuda") for _ in range(R)]
+    outs = [torch.empty_like(t) for t in ins]
+    h = ar.Handle(R, n, dtype)
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        for t in ins:
+            t.zero_()
+        ar.ar_allreduce(h.h, ins, outs, algo, proto, stream=s)   # warm up outside capture
+    s.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        for _ in range(10):
+            ar.ar_allreduce(h.h, ins, outs, algo, proto, stream=s)
+    for rep in range(4):
+        cpu = wl.make_inputs(50 + rep, R, n, dtype, "uniform")
+        for t, c in zip(ins, cpu):
+            t.copy_(c)
+        for o in outs:
+            o.fill_(float("nan"))
+        g.replay()
+        torch.cuda.synchronize()
+        assert ar.ar_status(h.h) == ar.AR_OK
+        want = expected(cpu, dtype)
+        for r in range(R):
+            assert_bits_equal(outs[r], want, dtype, "replay %d rank %d" % (rep, r))
+    h.close()
+
+
+@pytest.mark.parametrize("algo", [ar.AR_ONE_SHOT, ar.AR_TWO_SHOT], ids=["one_shot", "two_shot"])
+def test_ll_timeout_then_recovery(algo):
+    """A rank that never writes its packets: the peers' bounded polls give up,
+    AR_ERR_TIMEOUT is reported, and the next normal call is correct."""
+    need_gpu()
+    R, n, dtype = 4, 10000, "bf16"
+    cpu = wl.make_inputs(44, R, n, dtype, "uniform")
+    ins = device_inputs(cpu)
+    outs = [torch.empty_like(t) for t in ins]
+    with ar.Handle(R, n, dtype) as h:
+        ar.ar_set_timeout(h.h, 20_000_000)      # 20 ms
+        ar.ar_debug_drop_rank(h.h, 2)
+        ar.ar_allreduce(h.h, ins, outs, algo, ar.AR_LL)
+        assert ar.ar_status(h.h) == ar.AR_ERR_TIMEOUT
+        ar.ar_debug_drop_rank(h.h, -1)
+        ar.ar_allreduce(h.h, ins, outs, algo, ar.AR_LL)
+        assert ar.ar_status(h.h) == ar.AR_OK
+    want = expected(cpu, dtype)
+    for r in range(R):
+        assert_bits_equal(outs[r], want, dtype, "after recovery rank %d" % r)
+
+
+def test_ll_rejected_above_cap():
+    need_gpu()
+    n = ar.AR_LL_MAX_BYTES // 2 + 1
+    x = [torch.zeros(n, dtype=torch.bfloat16, device="cuda") for _ in range(2)]
+    with ar.Handle(2, n, "bf16") as h:
+        assert ar.ar_get_info(h.h)["ll_capable"] == 0
+        with pytest.raises(ar.ArError) as e:
+            ar.ar_allreduce(h.h, x, x, ar.AR_ONE_SHOT, ar.AR_LL)
+        assert e.value.code == ar.AR_ERR_UNSUPPORTED
+        ar.ar_allreduce(h.h, x, x, ar.AR_TWO_SHOT, ar.AR_HB)   # HB still serves it
+
+
+def test_invalid_aliasing_rejected():
+    need_gpu()
+    R, n = 3, 100
+    a = [torch.zeros(n, dtype=torch.bfloat16, device="cuda") for _ in range(R)]
+    big = torch.zeros(3 * n, dtype=torch.bfloat16, device="cuda")
+    with ar.Handle(R, n, "bf16") as h:
+        # two outputs overlapping
+        outs = [big[0:n], big[n // 2: n // 2 + n], big[2 * n:]]
+        with pytest.raises(ar.ArError):
+            ar.ar_allreduce(h.h, a, outs, ar.AR_ONE_SHOT, ar.AR_HB)
+        # rank 0's input is rank 1's output
+        with pytest.raises(ar.ArError):
+            ar.ar_allreduce(h.h, [a[0], a[1], a[2]], [a[1], big[:n], big[n:2 * n]],
+                            ar.AR_ONE_SHOT, ar.AR_HB)
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "fp16"])
+def test_round_exhaustive_vs_oracle(dtype):
+    """The kernels' rounding (cvt.rn) on all 2^32 binary32 patterns equals
+    the oracle's definition-based rounding."""
+    need_gpu()
+    chunk = 1 << 28
+    dst = torch.empty(chunk, dtype=wl.TORCH_DTYPE[dtype], device="cuda")
+    for start in range(0, 1 << 32, chunk):
+        pats = torch.arange(start, start + chunk, dtype=torch.int64, device="cuda")
+        src = (pats - (1 << 32) * (pats >= (1 << 31)).long()).to(torch.int32).view(torch.float32)
+        ar.ar_round(dtype, src, dst, chunk)
+        got = wl.bits(dst.cpu())
+        f = src.cpu().numpy()
+        want = oracle.round_f32(f, wl.DTYPE_CODE[dtype])
+        nan = np.isnan(f)
+        assert np.array_equal(got[~nan], want[~nan]), "chunk at %#x" % start
