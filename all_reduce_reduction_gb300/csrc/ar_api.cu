@@ -268,19 +268,22 @@ int ar_create(int R, size_t N, int dtype, ar_handle_t *out) {
     h->one_shot_warps = R <= 8 ? R * ((8 + R - 1) / R) : R;
     h->one_shot_cap = h->num_sms * (2048 / (32 * h->one_shot_warps));
     h->reg_cap = h->num_sms * (2048 / kRegThreads);
+    int smem_limit = 0;
+    err |= tma_prepare(dtype, &smem_limit) != cudaSuccess;
+    // per-rank tile: a 64 KiB stage over R ranks, 1..8 KiB; then as many
+    // stages (2..4) as the shared memory holds
     int tile = (int)((64 * 1024 / R) / 16 * 16);
     if (tile > 8192)
         tile = 8192;
     if (tile < 1024)
         tile = 1024;
-    int stages = (int)((220 * 1024 - 2 * tile) / ((size_t)R * tile));
-    if (stages > kTmaMaxStages)
-        stages = kTmaMaxStages;
-    if (stages < 2)
-        stages = 2;
+    int stages = kTmaMaxStages;
+    while (stages > 2 && tma_smem_bytes(R, tile, stages) > (size_t)smem_limit)
+        --stages;
+    while (tile > 1024 && tma_smem_bytes(R, tile, stages) > (size_t)smem_limit)
+        tile -= 1024;
     h->tma_tile = tile;
     h->tma_stages = stages;
-    err |= tma_prepare(dtype) != cudaSuccess;
     if (err) {
         (void)cudaGetLastError();
         cudaFree(h->dev_mem);

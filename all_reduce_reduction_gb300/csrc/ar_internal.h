@@ -100,7 +100,7 @@ cudaError_t launch_round(int dtype, const float *src, void *dst, uint64_t n, int
                          cudaStream_t s);
 
 // ar_tma.cu
-cudaError_t tma_prepare(int dtype);   // opt in to large dynamic shared memory
+cudaError_t tma_prepare(int dtype, int *max_dynamic_smem);   // opt in to large shared memory
 size_t tma_smem_bytes(int R, int tile_bytes, int stages);
 cudaError_t launch_two_shot_tma(const TmaArgs &a, int dtype, int grid, cudaStream_t s);
 

@@ -132,7 +132,7 @@ __device__ __forceinline__ bool item_range(const TmaArgs &a, uint64_t i, uint64_
 
 template <int DT>
 __global__ void __launch_bounds__(kTmaThreads, 1) k_two_shot_tma(const __grid_constant__ TmaArgs a) {
-    extern __shared__ __align__(1024) uint8_t smem[];
+    extern __shared__ __align__(128) uint8_t smem[];
     __shared__ int abort_flag;
     __shared__ uint64_t consumed_items;
 
@@ -264,27 +264,33 @@ size_t tma_smem_bytes(int R, int tile_bytes, int stages) {
     return (size_t)stages * R * tile_bytes + 2 * (size_t)tile_bytes + 2 * sizeof(uint64_t) * stages;
 }
 
-// Dynamic shared memory the kernel may opt in to (227 KB per CTA on sm_103a,
-// less what the kernel declares statically).
-static const int kTmaSmemLimit = 227 * 1024 - 64;
-
-template <int DT> static cudaError_t prepare_dt() {
+// Dynamic shared memory the kernel may opt in to: the device's per-block
+// opt-in maximum less what the kernel declares statically.
+template <int DT> static cudaError_t prepare_dt(int *limit) {
+    int dev = 0, optin = 0;
+    cudaFuncAttributes fa;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e == cudaSuccess)
+        e = cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
+    if (e == cudaSuccess)
+        e = cudaFuncGetAttributes(&fa, k_two_shot_tma<DT>);
+    if (e != cudaSuccess)
+        return e;
+    *limit = optin - (int)fa.sharedSizeBytes;
     return cudaFuncSetAttribute(k_two_shot_tma<DT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                kTmaSmemLimit);
+                                *limit);
 }
 
-cudaError_t tma_prepare(int dtype) {
+cudaError_t tma_prepare(int dtype, int *max_dynamic_smem) {
     switch (dtype) {
-    case AR_BF16: return prepare_dt<AR_BF16>();
-    case AR_FP16: return prepare_dt<AR_FP16>();
-    default: return prepare_dt<AR_FP32>();
+    case AR_BF16: return prepare_dt<AR_BF16>(max_dynamic_smem);
+    case AR_FP16: return prepare_dt<AR_FP16>(max_dynamic_smem);
+    default: return prepare_dt<AR_FP32>(max_dynamic_smem);
     }
 }
 
 cudaError_t launch_two_shot_tma(const TmaArgs &a, int dtype, int grid, cudaStream_t s) {
     const size_t smem = tma_smem_bytes(a.R, a.tile_bytes, a.stages);
-    if (smem > (size_t)kTmaSmemLimit)
-        return cudaErrorInvalidValue;
     switch (dtype) {
     case AR_BF16: k_two_shot_tma<AR_BF16><<<grid, kTmaThreads, smem, s>>>(a); break;
     case AR_FP16: k_two_shot_tma<AR_FP16><<<grid, kTmaThreads, smem, s>>>(a); break;
