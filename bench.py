@@ -1,0 +1,570 @@
+#!/usr/bin/env python3
+"""Benchmark of the virtual-rank sum all-reduce on GB300.
+
+Default workload: 8 virtual ranks, bf16, one-shot LL, message sizes
+N = 2^9 .. 2^18 elements per rank (1 KiB .. 512 KiB), uniform [-1, 1) inputs;
+10 all-reduce calls captured in one CUDA graph per size, 2 warm-up replays
+(the message-size sweep and graph timing of "SGLang 中的 MSCCL++ All-Reduce
+基准测试与推理集成指南", section 3.3).  One step = one replay of every size's
+graph.  L2 is flushed (a 256 MiB write) before every replay, outside the
+timed events.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload sweep|decode|prefill|edge]
+                    [--impl ours|reference]
+
+Prints one JSON line.  `value` is the whole job's throughput in GB/s on the
+minimal-bytes basis (every input byte read once, every output byte written
+once: 2 * R * N * elem_size per call), summed over all ranks; `sweep` gives
+µs/call per message size.  `--impl reference` times the CPU oracle on the
+host cores instead (the only other place this script runs it).  N > 1 runs N
+independent replicas, one per GPU (the path has no cross-GPU exchange).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = ("all-reduce µs/call and GB/s vs msg size (R=8 bf16, 1 GB300), "
+          "% of HBM roofline")
+FALLBACK_HBM_GBS = 6800.0
+L2_FLUSH_BYTES = 256 << 20
+
+
+# ---------------------------------------------------------------------------
+# workloads
+# ---------------------------------------------------------------------------
+def workload_cases(name: str, args=None):
+    """(workload description, list of cases).  A case is one all-reduce
+    configuration timed as a graph of `calls` calls."""
+    from all_reduce_reduction_gb300 import workload as wl
+    if name == "custom":
+        dist_name = "uniform" if args.n <= (1 << 18) else "normal"
+        w = wl.Workload(9, "custom_r%d_n%d_%s" % (args.R, args.n, args.dtype), args.R, args.n,
+                        args.dtype, dist_name)
+        big = 2 * w.R * w.n * wl.ELEM_SIZE[w.dtype] > (256 << 20)
+        cases = [dict(w=w, algo=args.algo, proto=args.proto, calls=args.calls, flush=not big)]
+        desc = "custom: R=%d, N=%d %s per rank, %s %s, %d calls per CUDA graph" % (
+            args.R, args.n, args.dtype, args.algo, args.proto, args.calls)
+    elif name == "sweep":
+        cases = [dict(w=w, algo="one_shot", proto="ll", calls=10, flush=True) for w in wl.LL_SWEEP]
+        desc = ("r8_bf16_ll_sweep: R=8 virtual ranks, bf16, N=2^9..2^18 elements per rank "
+                "(1 KiB..512 KiB), uniform[-1,1), one-shot LL, 10 calls per CUDA graph")
+    elif name == "decode":
+        cases = [dict(w=w, algo="one_shot", proto="hb", calls=10, flush=True) for w in wl.DECODE]
+        desc = ("r8_bf16_decode: R=8, bf16 [B, 8192] for B in 1,8,32,128,256, N(0,1), "
+                "one-shot HB, 10 calls per CUDA graph")
+    elif name == "prefill":
+        cases = [dict(w=wl.PREFILL, algo="two_shot", proto="hb", calls=1, flush=False)]
+        desc = ("r16_bf16_prefill: R=16, bf16 [8192, 8192] per rank (128 MiB), N(0,1), "
+                "two-shot HB with TMA staging")
+    elif name == "edge":
+        w = [x for x in wl.EDGE if x.R == 32 and x.dtype == "fp32"][0]
+        cases = [dict(w=w, algo="two_shot", proto="hb", calls=1, flush=False)]
+        desc = ("r32_fp32_edge: R=32, fp32, N=4097*4096+3 per rank, log-uniform |x| in "
+                "[1e-4,1e4), two-shot HB")
+    else:
+        raise SystemExit("unknown workload " + name)
+    return desc, cases
+
+
+def case_bytes(c) -> int:
+    w = c["w"]
+    from all_reduce_reduction_gb300 import workload as wl
+    return 2 * w.R * w.n * wl.ELEM_SIZE[w.dtype]
+
+
+# ---------------------------------------------------------------------------
+# distributed plumbing (host side only: a barrier and a max over ranks)
+# ---------------------------------------------------------------------------
+class Dist:
+    def __init__(self):
+        self.world = int(os.environ.get("WORLD_SIZE", "1"))
+        self.rank = int(os.environ.get("RANK", "0"))
+        self.local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+        self.pg = None
+        if self.world > 1:
+            import torch.distributed as dist
+            dist.init_process_group("gloo")
+            self.pg = dist
+
+    def barrier(self):
+        if self.pg:
+            self.pg.barrier()
+
+    def max(self, x: float) -> float:
+        if not self.pg:
+            return x
+        import torch
+        t = torch.tensor([x], dtype=torch.float64)
+        self.pg.all_reduce(t, op=self.pg.ReduceOp.MAX)
+        return float(t.item())
+
+    def sum(self, x: float) -> float:
+        if not self.pg:
+            return x
+        import torch
+        t = torch.tensor([x], dtype=torch.float64)
+        self.pg.all_reduce(t, op=self.pg.ReduceOp.SUM)
+        return float(t.item())
+
+    def close(self):
+        if self.pg:
+            self.pg.destroy_process_group()
+
+
+# ---------------------------------------------------------------------------
+# clocks during the timed region
+# ---------------------------------------------------------------------------
+REASONS = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+
+
+class ClockSampler:
+    def __init__(self, bus_id: str | None):
+        self.bus_id = bus_id
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        q = ("pci.bus_id,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             + ",".join("clocks_event_reasons." + r for r in REASONS))
+        try:
+            import tempfile
+            fd, self.path = tempfile.mkstemp(prefix="clocks_", suffix=".csv")
+            os.close(fd)
+            self.out = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "--query-gpu=" + q, "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=self.out, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self) -> dict | None:
+        if not self.proc:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.out.close()
+        with open(self.path) as f:
+            lines = f.readlines()
+        os.unlink(self.path)
+        return parse_clock_rows(lines, self.bus_id)
+
+
+def parse_clock_rows(lines, bus_id: str | None) -> dict | None:
+    """Summarise nvidia-smi CSV rows (pci.bus_id, clocks.sm, clocks.max.sm,
+    power.draw, reasons.active, then one Active/Not Active column per REASONS
+    entry) of the GPU whose bus id ends with `bus_id`."""
+    rows = []
+    for line in lines:
+        f = [x.strip() for x in line.split(",")]
+        if len(f) < 5 + len(REASONS):
+            continue
+        if bus_id and not f[0].lower().endswith(bus_id.lower()):
+            continue
+        rows.append(f)
+    if not rows:
+        return None
+    sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+    mx = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+    seen = sorted({REASONS[i] for r in rows for i in range(len(REASONS))
+                   if r[5 + i].lower().startswith("active")})
+    return {"sm_mhz": statistics.median(sm) if sm else None,
+            "sm_max_mhz": max(mx) if mx else None,
+            "reasons": seen, "samples": len(rows)}
+
+
+def clocks_rejected(c: dict | None) -> bool:
+    if not c:
+        return False
+    if set(c["reasons"]) & {"hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown"}:
+        return True
+    if c["sm_mhz"] and c["sm_max_mhz"] and not c["reasons"] and c["sm_mhz"] < 0.6 * c["sm_max_mhz"]:
+        return True
+    return False
+
+
+# ---------------------------------------------------------------------------
+# peaks and committed ncu traffic
+# ---------------------------------------------------------------------------
+def hbm_peak():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            return float(json.load(f)["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def kernel_source_digest() -> str:
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "all_reduce_reduction_gb300", "csrc")
+    for fn in sorted(os.listdir(csrc)):
+        if fn.endswith((".cu", ".cuh", ".h")):
+            h.update(open(os.path.join(csrc, fn), "rb").read())
+    return h.hexdigest()[:16]
+
+
+def committed_traffic(kernel_key: str):
+    """DRAM bytes per launch recorded by an ncu capture in profiles/, if the
+    kernels have not changed since (same source digest); else None."""
+    path = os.path.join(ROOT, "profiles", "traffic.txt")
+    if not os.path.exists(path):
+        return None
+    digest = kernel_source_digest()
+    for line in open(path):
+        f = line.split()
+        if len(f) >= 3 and f[0] == kernel_key and f[2] == digest:
+            return float(f[1])
+    return None
+
+
+# ---------------------------------------------------------------------------
+# our arm
+# ---------------------------------------------------------------------------
+class CaseRunner:
+    """Handle, device inputs/outputs and a captured graph for one case."""
+
+    def __init__(self, c, stream):
+        import torch
+        import all_reduce_reduction_gb300 as ar
+        from all_reduce_reduction_gb300 import workload as wl
+        self.c, self.w, self.s = c, c["w"], stream
+        w = self.w
+        self.cpu_inputs = w.inputs(threads=16)
+        self.ins = [t.cuda() for t in self.cpu_inputs]
+        self.outs = [torch.empty_like(t) for t in self.ins]
+        self.h = ar.Handle(w.R, w.n, w.dtype)
+        self.algo, self.proto = ar.ALGOS[c["algo"]], ar.PROTOS[c["proto"]]
+        self.bytes = case_bytes(c)
+        with torch.cuda.stream(stream):
+            ar.ar_allreduce(self.h.h, self.ins, self.outs, self.algo, self.proto, stream=stream)
+        stream.synchronize()
+        self.graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(self.graph, stream=stream):
+            for _ in range(c["calls"]):
+                ar.ar_allreduce(self.h.h, self.ins, self.outs, self.algo, self.proto, stream=stream)
+        for _ in range(2):
+            self.graph.replay()
+        torch.cuda.synchronize()
+        if ar.ar_status(self.h.h) != ar.AR_OK:
+            raise RuntimeError("device status after warm-up: " + ar.ar_strerror(ar.ar_status(self.h.h)))
+        self.pinned_in = [t.pin_memory() for t in self.cpu_inputs]
+        self.pinned_out = [torch.empty_like(t).pin_memory() for t in self.cpu_inputs]
+
+    def close(self):
+        self.h.close()
+
+
+def run_ours(args, dist: Dist):
+    import torch
+    import all_reduce_reduction_gb300 as ar
+    from all_reduce_reduction_gb300 import workload as wl
+
+    torch.cuda.set_device(dist.local_rank)
+    desc, cases = workload_cases(args.workload, args)
+    stream = torch.cuda.Stream()
+    runners = [CaseRunner(c, stream) for c in cases]
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device="cuda")
+
+    def one_step(events):
+        for i, r in enumerate(runners):
+            with torch.cuda.stream(stream):
+                if r.c["flush"]:
+                    flush.fill_(i & 0xFF)
+                e0 = torch.cuda.Event(enable_timing=True)
+                e1 = torch.cuda.Event(enable_timing=True)
+                e0.record(stream)
+                r.graph.replay()
+                e1.record(stream)
+            events.append((i, e0, e1))
+
+    def timed(K):
+        events = []
+        dist.barrier()
+        torch.cuda.synchronize()
+        for _ in range(K):
+            one_step(events)
+        torch.cuda.synchronize()
+        dist.barrier()
+        per_case = [0.0] * len(runners)
+        for i, e0, e1 in events:
+            per_case[i] += e0.elapsed_time(e1)
+        return per_case
+
+    for _ in range(args.warmup):
+        one_step([])
+    torch.cuda.synchronize()
+
+    props = torch.cuda.get_device_properties(dist.local_rank)
+    bus = None
+    if hasattr(props, "pci_bus_id"):
+        bus = "%02X:%02X.0" % (props.pci_bus_id, props.pci_device_id)
+    sampler = ClockSampler(bus)
+    sampler.start()
+    per_case = timed(args.steps)
+    clocks = sampler.stop()
+    remeasured = False
+    if clocks_rejected(clocks):
+        sampler = ClockSampler(bus)
+        sampler.start()
+        per_case = timed(args.steps)
+        clocks = sampler.stop()
+        remeasured = True
+
+    total_ms = sum(per_case)
+    for r in runners:
+        st = ar.ar_status(r.h.h, stream)
+        if st != ar.AR_OK:
+            raise RuntimeError("device status after the timed region: " + ar.ar_strerror(st))
+    calls = [r.c["calls"] for r in runners]
+    bytes_step = sum(r.bytes * k for r, k in zip(runners, calls))
+    ms_step = dist.max(total_ms / args.steps)
+    value = dist.sum(bytes_step) / (ms_step * 1e-3) / 1e9
+
+    # dominant kernel: the case with the largest share of the step
+    dom = max(range(len(runners)), key=lambda i: per_case[i])
+    dr = runners[dom]
+    launch_s = per_case[dom] * 1e-3 / (args.steps * dr.c["calls"])
+    peak, peak_kind = hbm_peak()
+    achieved = dr.bytes / launch_s / 1e9
+    kkey = "%s_%s_r%d_n%d_%s" % (dr.c["algo"], dr.c["proto"], dr.w.R, dr.w.n, dr.w.dtype)
+    roofline = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
+                "frac": round(achieved / peak, 4), "traffic": committed_traffic(kkey),
+                "kernel": kkey, "peak_source": peak_kind + " (MEASURED_PEAKS.json hbm_gbs)"
+                if peak_kind == "measured" else "fallback 6800 GB/s"}
+
+    sweep = {}
+    for i, r in enumerate(runners):
+        us = per_case[i] * 1e3 / (args.steps * r.c["calls"])
+        nb = r.w.n * wl.ELEM_SIZE[r.w.dtype]
+        sweep[str(r.w.n)] = {
+            "bytes_per_rank": nb, "us_per_call": round(us, 3),
+            "algbw_GBps": round(nb / us / 1e3, 2),
+            "busbw_GBps": round(nb / us / 1e3 * 2 * (r.w.R - 1) / r.w.R, 2),
+            "min_bytes_GBps": round(r.bytes / us / 1e3, 1),
+            "frac_of_hbm_peak": round(r.bytes / us / 1e3 / peak, 4),
+            "l2_resident": 2 * r.bytes <= 100 << 20,
+        }
+
+    # end to end: pinned host inputs -> device, the same graph, outputs -> host
+    e2e_steps = max(3, min(args.steps, 50))
+    e2e_ms = 0.0
+    h2d = sum(sum(t.numel() * t.element_size() for t in r.pinned_in) for r in runners)
+    d2h = sum(sum(t.numel() * t.element_size() for t in r.pinned_out) for r in runners)
+    dist.barrier()
+    torch.cuda.synchronize()
+    for _ in range(e2e_steps):
+        for r in runners:
+            with torch.cuda.stream(stream):
+                e0 = torch.cuda.Event(enable_timing=True)
+                e1 = torch.cuda.Event(enable_timing=True)
+                e0.record(stream)
+                for d, hsrc in zip(r.ins, r.pinned_in):
+                    d.copy_(hsrc, non_blocking=True)
+                r.graph.replay()
+                for hdst, o in zip(r.pinned_out, r.outs):
+                    hdst.copy_(o, non_blocking=True)
+                e1.record(stream)
+            e1.synchronize()
+            e2e_ms += e0.elapsed_time(e1)
+    e2e_ms = dist.max(e2e_ms / e2e_steps)
+    e2e_value = dist.sum(bytes_step) / (e2e_ms * 1e-3) / 1e9
+
+    variants = None
+    if args.workload == "sweep" and not args.no_variants:
+        variants = measure_variants(runners, stream, flush, max(20, args.steps // 10))
+
+    cpu = None
+    if dist.world == 1 and not args.no_cpu_baseline:
+        cpu = cpu_baseline(runners, seconds=args.cpu_seconds)
+
+    launches = args.steps * sum(calls)
+    line = {
+        "metric": METRIC, "value": round(value, 2), "unit": "GB/s",
+        "n_gpus": dist.world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(ms_step, 5), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": runners[0].w.dtype, "data": "synthetic",
+        "config": {"workload": desc, "R": runners[0].w.R,
+                   "sizes_elems_per_rank": [r.w.n for r in runners],
+                   "algo": cases[0]["algo"], "proto": cases[0]["proto"],
+                   "calls_per_graph": cases[0]["calls"],
+                   "l2": ("flushed (256 MiB write) before every graph replay, outside the timed events"
+                          if cases[0]["flush"] else "inputs larger than L2 (no flush)"),
+                   "bytes_basis": "minimal: 2*R*N*elem_size per call",
+                   "parallelism": "replicas" if dist.world > 1 else "single GPU"},
+        "roofline": roofline,
+        "cpu_baseline": cpu,
+        "e2e": {"value": round(e2e_value, 2), "unit": "GB/s", "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h,
+                "note": "pinned host inputs copied in, the step's graphs, all R outputs copied out"},
+        "gpu_launches": launches,
+        "clocks": clocks, "clocks_remeasured": remeasured,
+        "sweep": sweep,
+    }
+    if variants is not None:
+        line["variants_us_per_call"] = variants
+    for r in runners:
+        r.close()
+    return line
+
+
+def measure_variants(runners, stream, flush, K):
+    """µs/call of the other schedule/protocol pairs at the sweep's sizes
+    (informative; not part of `value`)."""
+    import torch
+    import all_reduce_reduction_gb300 as ar
+    out = {}
+    for algo, proto in (("one_shot", "hb"), ("two_shot", "hb"), ("two_shot", "ll")):
+        row = {}
+        for r in runners:
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=stream):
+                for _ in range(r.c["calls"]):
+                    ar.ar_allreduce(r.h.h, r.ins, r.outs, ar.ALGOS[algo], ar.PROTOS[proto],
+                                    stream=stream)
+            for _ in range(2):
+                g.replay()
+            tot = 0.0
+            for _ in range(K):
+                with torch.cuda.stream(stream):
+                    flush.fill_(1)
+                    e0 = torch.cuda.Event(enable_timing=True)
+                    e1 = torch.cuda.Event(enable_timing=True)
+                    e0.record(stream)
+                    g.replay()
+                    e1.record(stream)
+                e1.synchronize()
+                tot += e0.elapsed_time(e1)
+            row[str(r.w.n)] = round(tot * 1e3 / (K * r.c["calls"]), 3)
+        out["%s_%s" % (algo, proto)] = row
+    torch.cuda.synchronize()
+    return out
+
+
+def cpu_baseline(runners, seconds: float):
+    """The oracle, as it stands (one thread), on a bounded sample of the same
+    workload: the step's cases one call each, repeated for ~`seconds`."""
+    import oracle
+    from all_reduce_reduction_gb300 import workload as wl
+    lib = oracle.load()
+    sample = []
+    for r in runners:
+        ins = [wl.bits(t) for t in r.cpu_inputs]
+        if r.w.n > (1 << 22):           # large messages: a leading slice of every rank
+            ins = [a[: 1 << 22].copy() for a in ins]
+        sample.append(ins)
+    done_bytes, t0 = 0, time.perf_counter()
+    passes = 0
+    while True:
+        for ins in sample:
+            oracle.allreduce(ins, wl.DTYPE_CODE[runners[0].w.dtype], lib=lib)
+            done_bytes += 2 * len(ins) * ins[0].nbytes
+        passes += 1
+        if time.perf_counter() - t0 >= seconds:
+            break
+    dt = time.perf_counter() - t0
+    return {"value": round(done_bytes / dt / 1e9, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
+            "sample": "%d passes over the step's %d cases, one call each%s (%.1f s)" % (
+                passes, len(sample),
+                ", first 2^22 elements per rank" if any(r.w.n > (1 << 22) for r in runners) else "",
+                dt)}
+
+
+# ---------------------------------------------------------------------------
+# reference arm: the CPU oracle on the host cores
+# ---------------------------------------------------------------------------
+def run_reference(args, world: int):
+    from all_reduce_reduction_gb300 import workload as wl
+    import oracle
+    desc, cases = workload_cases(args.workload, args)
+    lib = oracle.load()
+    sample = []
+    for c in cases:
+        w = c["w"]
+        n = min(w.n, 1 << 20)
+        ins = [wl.bits(t) for t in wl.make_inputs(w.config, w.R, n, w.dtype, w.dist)]
+        sample.append(ins)
+    dt_code = wl.DTYPE_CODE[cases[0]["w"].dtype]
+
+    def step():
+        b = 0
+        for ins in sample:
+            oracle.allreduce(ins, dt_code, lib=lib)
+            b += 2 * len(ins) * ins[0].nbytes
+        return b
+
+    for _ in range(args.warmup):
+        step()
+    t0 = time.perf_counter()
+    done = 0
+    for _ in range(args.steps):
+        done += step()
+    dt = time.perf_counter() - t0
+    value = done / dt / 1e9
+    sample_desc = ("per step: each of the %d cases once (the GPU arm's step runs each %d times)%s"
+                   % (len(sample), cases[0]["calls"],
+                      "; at most 2^20 elements per rank" if any(c["w"].n > (1 << 20) for c in cases)
+                      else ""))
+    return {
+        "impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "GB/s",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(dt * 1e3 / args.steps, 4), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": cases[0]["w"].dtype, "data": "synthetic",
+        "config": {"workload": desc, "R": cases[0]["w"].R,
+                   "sizes_elems_per_rank": [c["w"].n for c in cases],
+                   "algo": cases[0]["algo"], "proto": cases[0]["proto"]},
+        "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
+                         "sample": sample_desc},
+        "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+
+
+def main():
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=1000)
+    p.add_argument("--warmup", type=int, default=10)
+    p.add_argument("--workload", default="sweep",
+                   choices=["sweep", "decode", "prefill", "edge", "custom"])
+    # --workload custom: one case (used for profiling single kernels)
+    p.add_argument("--R", type=int, default=8)
+    p.add_argument("--n", type=int, default=1 << 18)
+    p.add_argument("--dtype", default="bf16", choices=["bf16", "fp16", "fp32"])
+    p.add_argument("--algo", default="one_shot", choices=["one_shot", "two_shot"])
+    p.add_argument("--proto", default="ll", choices=["ll", "hb"])
+    p.add_argument("--calls", type=int, default=10)
+    p.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    p.add_argument("--cpu-seconds", type=float, default=10.0)
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--no-variants", action="store_true")
+    args = p.parse_args()
+    if args.warmup < 3:
+        raise SystemExit("--warmup must be >= 3")
+
+    if args.impl == "reference":
+        # rank 0 alone times the oracle; the other ranks exit without work
+        if int(os.environ.get("RANK", "0")) == 0:
+            print(json.dumps(run_reference(args, int(os.environ.get("WORLD_SIZE", "1")))),
+                  flush=True)
+        return
+    dist = Dist()
+    line = run_ours(args, dist)
+    if dist.rank == 0:
+        print(json.dumps(line), flush=True)
+    dist.close()
+
+
+if __name__ == "__main__":
+    main()

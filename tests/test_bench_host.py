@@ -1,0 +1,95 @@
+"""Host-side logic of bench.py, on the CPU: the max/sum over ranks with two
+gloo processes, the reference arm (alone and under torchrun), and the
+parsing of the clock samples."""
+import json
+import os
+import subprocess
+import sys
+
+import pytest
+import torch.multiprocessing as mp
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+sys.path.insert(0, ROOT)
+import bench  # noqa: E402
+
+
+def _worker(rank, world, port, q):
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port), RANK=str(rank),
+                      WORLD_SIZE=str(world), LOCAL_RANK=str(rank))
+    d = bench.Dist()
+    d.barrier()
+    q.put((rank, d.max(float(rank + 1) * 1.5), d.sum(10.0 * (rank + 1))))
+    d.close()
+
+
+def test_dist_max_and_sum_two_ranks():
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    port = 29500 + os.getpid() % 2000
+    procs = [ctx.Process(target=_worker, args=(r, 2, port, q)) for r in range(2)]
+    for p in procs:
+        p.start()
+    got = sorted(q.get(timeout=120) for _ in procs)
+    for p in procs:
+        p.join(timeout=60)
+        assert p.exitcode == 0
+    assert got == [(0, 3.0, 30.0), (1, 3.0, 30.0)]
+
+
+def _lines(out: str):
+    return [l for l in out.splitlines() if l.strip().startswith("{")]
+
+
+def test_reference_arm_line():
+    res = subprocess.run([sys.executable, "bench.py", "--impl", "reference", "--steps", "3",
+                          "--warmup", "3"], cwd=ROOT, capture_output=True, text=True, timeout=300)
+    assert res.returncode == 0, res.stderr
+    lines = _lines(res.stdout)
+    assert len(lines) == 1
+    d = json.loads(lines[0])
+    assert d["impl"] == "reference" and d["unit"] == "GB/s" and d["value"] > 0
+    assert d["cpu_baseline"]["kind"] == "oracle" and d["cpu_baseline"]["value"] == d["value"]
+    assert d["e2e"]["h2d_bytes_per_step"] == 0 and d["e2e"]["d2h_bytes_per_step"] == 0
+    assert d["higher_is_better"] is True and d["steps"] == 3 and d["warmup"] == 3
+
+
+def test_reference_arm_under_torchrun_prints_once():
+    port = 31000 + os.getpid() % 2000
+    res = subprocess.run([sys.executable, "-m", "torch.distributed.run", "--nnodes=1",
+                          "--nproc-per-node", "2", "--master-addr", "127.0.0.1",
+                          "--master-port", str(port), "bench.py", "--impl", "reference",
+                          "--gpus", "2", "--steps", "3", "--warmup", "3"],
+                         cwd=ROOT, capture_output=True, text=True, timeout=300)
+    assert res.returncode == 0, res.stderr[-2000:]
+    lines = _lines(res.stdout)
+    assert len(lines) == 1
+    assert json.loads(lines[0])["n_gpus"] == 2
+
+
+def test_warmup_below_three_is_refused():
+    res = subprocess.run([sys.executable, "bench.py", "--impl", "reference", "--warmup", "2"],
+                         cwd=ROOT, capture_output=True, text=True, timeout=120)
+    assert res.returncode != 0
+
+
+def test_clock_rows():
+    hdr = "00000000:1B:00.0, {sm}, 2070, 900.5, 0x0, {a}, Not Active, Not Active, {b}"
+    lines = [hdr.format(sm=s, a="Not Active", b="Not Active") for s in (1965, 1980, 1995)]
+    lines.append("00000000:2C:00.0, 300, 2070, 100, 0x0, Active, Not Active, Not Active, Not Active")
+    c = bench.parse_clock_rows(lines, "1B:00.0")
+    assert c == {"sm_mhz": 1980.0, "sm_max_mhz": 2070.0, "reasons": [], "samples": 3}
+    assert not bench.clocks_rejected(c)
+    lines.append(hdr.format(sm=1900, a="Active", b="Active"))
+    c = bench.parse_clock_rows(lines, "1B:00.0")
+    assert c["reasons"] == ["hw_slowdown", "sw_power_cap"] and bench.clocks_rejected(c)
+    low = [hdr.format(sm=900, a="Not Active", b="Not Active")] * 3
+    assert bench.clocks_rejected(bench.parse_clock_rows(low, None))
+    capped = [hdr.format(sm=1500, a="Not Active", b="Active")] * 3
+    assert not bench.clocks_rejected(bench.parse_clock_rows(capped, None))
+
+
+def test_traffic_lookup_needs_matching_digest(tmp_path, monkeypatch):
+    d = bench.kernel_source_digest()
+    assert len(d) == 16
+    assert bench.committed_traffic("no_such_kernel") is None
