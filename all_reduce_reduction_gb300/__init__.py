@@ -86,6 +86,7 @@ SIGNATURES = {
     "ar_round": ([_I, _VP, _VP, _SZ, _VP], _I),
     "ar_get_info": ([_VP, ctypes.POINTER(ar_info)], _I),
     "ar_strerror": ([_I], ctypes.c_char_p),
+    "ar_allreduce_ll_static": ([_I, _SZ, _I, _VPP, _VPP, _VP], _I),
 }
 
 
@@ -198,6 +199,20 @@ def ar_get_info(h: int) -> dict:
     info = ar_info()
     _check(load_library().ar_get_info(h, ctypes.byref(info)), "ar_get_info")
     return info.as_dict()
+
+
+def ar_allreduce_ll_static(R: int, N: int, dtype, ins, outs, stream=None) -> None:
+    """One-shot LL all-reduce with no handle and no allocation, for callers
+    that may not allocate device memory where they run it (see include/ar.h:
+    library-static scratch, at most AR_NOALLOC_SCRATCH_BYTES of packets;
+    the first call on a device must precede any stream capture; calls that
+    overlap on the GPU race)."""
+    dt = DTYPES[dtype] if isinstance(dtype, str) else dtype
+    _check(load_library().ar_allreduce_ll_static(R, N, dt, _ptr_array(ins), _ptr_array(outs),
+                                                 _stream(stream)), "ar_allreduce_ll_static")
+
+
+AR_NOALLOC_SCRATCH_BYTES = 8 << 20
 
 
 class Handle:

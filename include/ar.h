@@ -230,6 +230,40 @@ int ar_get_info(ar_handle_t h, ar_info *info);
 /* Static string naming an ar_status_code. */
 const char *ar_strerror(int code);
 
+/* Bytes of packet scratch compiled into the library for
+ * ar_allreduce_ll_static (every GPU that loads the library holds this much
+ * static device memory, plus 33 KiB of control words, until the process
+ * exits). */
+#define AR_NOALLOC_SCRATCH_BYTES (8u << 20)
+
+/* One-shot LL all-reduce that allocates nothing.  The pages have no
+ * counterpart of this call; it exists for callers that cannot allocate
+ * device memory where they run the collective: a plugin hook that an
+ * inference engine calls while capturing its stream into a CUDA graph (an
+ * allocation there is an illegal call during capture), or an engine that
+ * serves all device memory from its own pool and forbids side allocations.
+ * ar_create's scratch is unavailable to them; this call uses a fixed array
+ * of static device memory inside the library instead.
+ *   R, N, dtype: as in ar_create.   in, out, stream: as in ar_allreduce
+ *   (same alignment and aliasing rules).
+ * Computes exactly what ar_allreduce(h, in, out, AR_ONE_SHOT, AR_LL, stream)
+ * computes.  Limit: R * ceil(ceil(N * elem_size / 4) / 4) * 32 bytes of
+ * packets must fit in AR_NOALLOC_SCRATCH_BYTES (8 MiB: for example R = 8
+ * ranks of up to 512 KiB each); larger messages return AR_ERR_UNSUPPORTED
+ * and nothing is enqueued.  It calls no cudaMalloc/cudaFree and no
+ * allocating library routine.
+ * The first call on each device sets the array up (resolves its device
+ * address, zeroes its control words and waits for that): make that first
+ * call, with the device current, before any stream capture.
+ * All calls share the one array and it keeps the last call's contents, so
+ * calls whose kernels overlap on the GPU race: order them on one stream (or
+ * with events).  Device-side wait limits are fixed at one second and a
+ * timed-out wait is not reported (there is no handle to query).
+ * Errors: AR_ERR_INVALID (arguments), AR_ERR_UNSUPPORTED (too large),
+ * AR_ERR_CUDA. */
+int ar_allreduce_ll_static(int R, size_t N, int dtype, const void *const in[],
+                           void *const out[], cudaStream_t stream);
+
 #ifdef __cplusplus
 }
 #endif
