@@ -30,6 +30,7 @@ AR_ERR_CUDA = 3
 AR_ERR_NOMEM = 4
 AR_ERR_TIMEOUT = 5
 AR_ERR_FLAG_MISMATCH = 6
+AR_LL_AUTO, AR_LL_GLOBAL, AR_LL_CLUSTER = 0, 1, 2
 AR_MAX_RANKS = 32
 AR_LL_MAX_BYTES = 64 << 20
 
@@ -60,6 +61,11 @@ class ar_info(ctypes.Structure):
         ("tma_tile_bytes", ctypes.c_int),
         ("tma_stages", ctypes.c_int),
         ("timeout_ns", ctypes.c_uint64),
+        ("ll_transport", ctypes.c_int),
+        ("ll_cluster_ok", ctypes.c_int),
+        ("ll_cluster_units", ctypes.c_int),
+        ("ll_cluster_max", ctypes.c_int),
+        ("pdl", ctypes.c_int),
     ]
 
     def as_dict(self) -> dict:
@@ -83,6 +89,8 @@ SIGNATURES = {
     "ar_status": ([_VP, _VP], _I),
     "ar_set_timeout": ([_VP, _U64], _I),
     "ar_debug_drop_rank": ([_VP, _I], _I),
+    "ar_set_ll_transport": ([_VP, _I], _I),
+    "ar_set_pdl": ([_VP, _I], _I),
     "ar_round": ([_I, _VP, _VP, _SZ, _VP], _I),
     "ar_get_info": ([_VP, ctypes.POINTER(ar_info)], _I),
     "ar_strerror": ([_I], ctypes.c_char_p),
@@ -184,6 +192,14 @@ def ar_status(h: int, stream=None) -> int:
 
 def ar_set_timeout(h: int, ns: int) -> None:
     _check(load_library().ar_set_timeout(h, ns), "ar_set_timeout")
+
+
+def ar_set_pdl(h: int, enable: int) -> None:
+    _check(load_library().ar_set_pdl(h, enable), "ar_set_pdl")
+
+
+def ar_set_ll_transport(h: int, transport: int) -> None:
+    _check(load_library().ar_set_ll_transport(h, transport), "ar_set_ll_transport")
 
 
 def ar_debug_drop_rank(h: int, rank: int) -> None:

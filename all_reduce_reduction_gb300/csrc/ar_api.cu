@@ -30,6 +30,11 @@ struct ar_handle {
     int reg_cap;            // CTAs of the 256-thread kernels per launch
     int tma_tile;
     int tma_stages;
+    int pdl;                // launch with programmatic dependent launch
+    int ll_transport;       // enum ar_ll_transport
+    bool cluster_ok;        // the cluster LL kernel can run for this R
+    uint64_t cluster_uc;    // its 16-byte units per rank per chunk (largest)
+    int cluster_max;        // co-resident clusters at that chunk size
 };
 
 namespace {
@@ -132,7 +137,7 @@ int one_shot_hb(ar_handle *h, const void *const in[], void *const out[], bool ve
     const uint64_t units = vec ? h->N / per_vec : h->N;
     const uint64_t per_blk = (uint64_t)(h->one_shot_warps / h->R) * 32;
     const int grid = clamp_grid(ceil_div(units, per_blk), h->one_shot_cap);
-    return from_cuda(launch_one_shot_hb(a, h->dtype, vec, grid, 32 * h->one_shot_warps, s));
+    return from_cuda(launch_one_shot_hb(a, h->dtype, vec, grid, 32 * h->one_shot_warps, s, h->pdl));
 }
 
 int two_shot_hb(ar_handle *h, const void *const in[], void *const out[], bool vec, bool inplace,
@@ -151,19 +156,44 @@ int two_shot_hb(ar_handle *h, const void *const in[], void *const out[], bool ve
         a.c = h->ctl;
         const uint64_t items = ceil_div(body, (uint64_t)h->tma_tile) + (uint64_t)h->R;
         const int grid = clamp_grid(items, h->num_sms);
-        return from_cuda(launch_two_shot_tma(a, h->dtype, grid, s));
+        return from_cuda(launch_two_shot_tma(a, h->dtype, grid, s, h->pdl));
     }
     // unaligned buffers: one thread per element reduces once, stores R times
     const HbArgs a = hb_args(h, in, out, inplace);
     const uint64_t units = vec ? h->N / (16 / h->esz) : h->N;
     const int grid = clamp_grid(ceil_div(units, kRegThreads), h->reg_cap);
-    return from_cuda(launch_reduce(a, h->dtype, vec, false, grid, s));
+    return from_cuda(launch_reduce(a, h->dtype, vec, false, grid, s, h->pdl));
 }
 
-int ll(ar_handle *h, const void *const in[], void *const out[], bool vec, bool two,
+// One-shot LL through thread-block clusters (R peers per cluster exchange
+// packets in distributed shared memory).
+int ll_cluster(ar_handle *h, const void *const in[], void *const out[], cudaStream_t s) {
+    LlClusterArgs a;
+    fill_ptrs(h, in, out, &a.p);
+    a.n = h->N;
+    a.R = h->R;
+    a.c = h->ctl;
+    const uint64_t U = h->N * h->esz / 16;
+    a.units_per_chunk = U < h->cluster_uc ? (U > 0 ? U : 1) : h->cluster_uc;
+    const uint64_t nchunks = U > 0 ? ceil_div(U, a.units_per_chunk) : 1;
+    int cap = h->cluster_max;
+    if (cap > kEpochWords / h->R)
+        cap = kEpochWords / h->R;
+    return from_cuda(launch_ll_cluster(a, h->dtype, clamp_grid(nchunks, cap), s, h->pdl));
+}
+
+bool use_cluster(const ar_handle *h, bool vec16, bool two) {
+    return !two && vec16 && h->cluster_ok && h->ll_transport == AR_LL_CLUSTER;
+}
+
+// vec: every buffer 8-byte aligned (global-memory kernel's vector path);
+// vec16: 16-byte aligned (needed by the cluster kernel).
+int ll(ar_handle *h, const void *const in[], void *const out[], bool vec, bool vec16, bool two,
        cudaStream_t s) {
     if (!h->slots)
         return AR_ERR_UNSUPPORTED;
+    if (use_cluster(h, vec16, two))
+        return ll_cluster(h, in, out, s);
     LlArgs a;
     fill_ptrs(h, in, out, &a.p);
     a.n = h->N;
@@ -181,7 +211,7 @@ int ll(ar_handle *h, const void *const in[], void *const out[], bool vec, bool t
     if (gmax < 1)
         return AR_ERR_UNSUPPORTED;                 // cannot keep R CTAs resident
     a.G = clamp_grid(ceil_div(work, kLlThreads), gmax);
-    return from_cuda(launch_ll(a, h->dtype, vec, two, s));
+    return from_cuda(launch_ll(a, h->dtype, vec, two, s, h->pdl));
 }
 
 }  // namespace
@@ -284,6 +314,28 @@ int ar_create(int R, size_t N, int dtype, ar_handle_t *out) {
         tile -= 1024;
     h->tma_tile = tile;
     h->tma_stages = stages;
+
+    // cluster LL: one CTA per virtual rank in a cluster (portable up to 8,
+    // 16 with the non-portable size); receive buffers of ~64 KiB per CTA
+    h->pdl = 1;
+    h->ll_transport = AR_LL_AUTO;
+    h->cluster_ok = false;
+    if (ll_capable && R <= 16) {
+        uint64_t uc = ((uint64_t)kLlClusterTargetSmem / (8u * R) - 4) / 4;
+        if (uc > 1024)
+            uc = 1024;
+        LlClusterArgs probe = {};
+        probe.R = R;
+        probe.units_per_chunk = uc;
+        int clusters = 0;
+        if (ll_cluster_prepare(dtype, R) == cudaSuccess &&
+            ll_cluster_max_clusters(probe, dtype, &clusters) == cudaSuccess && clusters > 0) {
+            h->cluster_ok = true;
+            h->cluster_uc = uc;
+            h->cluster_max = clusters;
+        }
+        (void)cudaGetLastError();   // a refused cluster shape only disables the path
+    }
     if (err) {
         (void)cudaGetLastError();
         cudaFree(h->dev_mem);
@@ -320,7 +372,7 @@ int ar_allreduce(ar_handle_t h, const void *const in[], void *const out[], int a
         return algo == AR_ONE_SHOT ? one_shot_hb(h, in, out, vec16, inplace, stream)
                                    : two_shot_hb(h, in, out, vec16, inplace, stream);
     if (proto == AR_LL)
-        return ll(h, in, out, vec8, algo == AR_TWO_SHOT, stream);
+        return ll(h, in, out, vec8, vec16, algo == AR_TWO_SHOT, stream);
     return AR_ERR_INVALID;
 }
 
@@ -335,7 +387,7 @@ int ar_reduce_scatter(ar_handle_t h, const void *const in[], void *const out[],
     const HbArgs a = hb_args(h, in, out, inplace);
     const uint64_t units = vec16 ? h->N / (16 / h->esz) : h->N;
     const int grid = clamp_grid(ceil_div(units, kRegThreads), h->reg_cap);
-    return from_cuda(launch_reduce(a, h->dtype, vec16, true, grid, stream));
+    return from_cuda(launch_reduce(a, h->dtype, vec16, true, grid, stream, h->pdl));
 }
 
 int ar_all_gather(ar_handle_t h, void *const out[], cudaStream_t stream) {
@@ -346,7 +398,7 @@ int ar_all_gather(ar_handle_t h, void *const out[], cudaStream_t stream) {
     const HbArgs a = hb_args(h, nullptr, out, false);
     const uint64_t units = vec16 ? h->N / (16 / h->esz) : h->N;
     const int grid = clamp_grid(ceil_div(units, kRegThreads), h->reg_cap);
-    return from_cuda(launch_all_gather(a, h->dtype, vec16, grid, stream));
+    return from_cuda(launch_all_gather(a, h->dtype, vec16, grid, stream, h->pdl));
 }
 
 int ar_ll_pack(ar_handle_t h, const void *src, uint64_t *pkts, size_t n, uint32_t flag,
@@ -365,7 +417,7 @@ int ar_ll_pack(ar_handle_t h, const void *src, uint64_t *pkts, size_t n, uint32_
     a.status = h->ctl.status;
     const bool vec = ((uintptr_t)src % 8) == 0 && ((uintptr_t)pkts % 16) == 0;
     const int grid = clamp_grid(ceil_div(ceil_div(n * h->esz, 8), kRegThreads), h->reg_cap);
-    return from_cuda(launch_pack(a, h->dtype, vec, grid, stream));
+    return from_cuda(launch_pack(a, h->dtype, vec, grid, stream, h->pdl));
 }
 
 int ar_ll_unpack(ar_handle_t h, const uint64_t *pkts, void *dst, size_t n, uint32_t flag,
@@ -384,7 +436,7 @@ int ar_ll_unpack(ar_handle_t h, const uint64_t *pkts, void *dst, size_t n, uint3
     a.status = h->ctl.status;
     const bool vec = ((uintptr_t)dst % 8) == 0 && ((uintptr_t)pkts % 16) == 0;
     const int grid = clamp_grid(ceil_div(ceil_div(n * h->esz, 8), kRegThreads), h->reg_cap);
-    return from_cuda(launch_unpack(a, h->dtype, vec, grid, stream));
+    return from_cuda(launch_unpack(a, h->dtype, vec, grid, stream, h->pdl));
 }
 
 int ar_status(ar_handle_t h, cudaStream_t stream) {
@@ -405,6 +457,20 @@ int ar_set_timeout(ar_handle_t h, uint64_t ns) {
     if (!h)
         return AR_ERR_INVALID;
     h->ctl.timeout_ns = ns ? ns : kDefaultTimeoutNs;
+    return AR_OK;
+}
+
+int ar_set_pdl(ar_handle_t h, int enable) {
+    if (!h || (enable != 0 && enable != 1))
+        return AR_ERR_INVALID;
+    h->pdl = enable;
+    return AR_OK;
+}
+
+int ar_set_ll_transport(ar_handle_t h, int transport) {
+    if (!h || (transport != AR_LL_AUTO && transport != AR_LL_GLOBAL && transport != AR_LL_CLUSTER))
+        return AR_ERR_INVALID;
+    h->ll_transport = transport;
     return AR_OK;
 }
 
@@ -441,6 +507,11 @@ int ar_get_info(ar_handle_t h, ar_info *info) {
     info->tma_tile_bytes = h->tma_tile;
     info->tma_stages = h->tma_stages;
     info->timeout_ns = h->ctl.timeout_ns;
+    info->ll_transport = h->ll_transport;
+    info->pdl = h->pdl;
+    info->ll_cluster_ok = h->cluster_ok ? 1 : 0;
+    info->ll_cluster_units = h->cluster_ok ? (int)h->cluster_uc : 0;
+    info->ll_cluster_max = h->cluster_ok ? h->cluster_max : 0;
     return AR_OK;
 }
 

@@ -183,6 +183,30 @@ __device__ __forceinline__ void st_u32_relaxed(uint32_t *p, uint32_t a) {
     asm volatile("st.relaxed.gpu.global.u32 [%0], %1;" :: "l"(p), "r"(a) : "memory");
 }
 
+// Payload word q (message bytes [4q, 4q + 4), zero past the end) of an
+// n-element buffer, element by element (any alignment of the buffer).
+template <int ESZ>
+__device__ __forceinline__ uint32_t load_payload(const void *base, uint64_t n, uint64_t q) {
+    if (ESZ == 4)
+        return reinterpret_cast<const uint32_t *>(base)[q];
+    const uint16_t *b = reinterpret_cast<const uint16_t *>(base);
+    const uint32_t lo = b[2 * q];
+    const uint32_t hi = (2 * q + 1 < n) ? (uint32_t)b[2 * q + 1] : 0u;
+    return lo | (hi << 16);
+}
+
+template <int ESZ>
+__device__ __forceinline__ void store_payload(void *base, uint64_t n, uint64_t q, uint32_t pl) {
+    if (ESZ == 4) {
+        reinterpret_cast<uint32_t *>(base)[q] = pl;
+        return;
+    }
+    uint16_t *b = reinterpret_cast<uint16_t *>(base);
+    b[2 * q] = (uint16_t)pl;
+    if (2 * q + 1 < n)
+        b[2 * q + 1] = (uint16_t)(pl >> 16);
+}
+
 __device__ __forceinline__ uint64_t make_pkt(uint32_t payload, uint32_t flag) {
     return ((uint64_t)flag << 32) | (uint64_t)payload;
 }
@@ -193,6 +217,17 @@ __device__ __forceinline__ uint64_t globaltimer_ns() {
     uint64_t t;
     asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
     return t;
+}
+
+// ---------------------------------------------------------------------------
+// Programmatic dependent launch.  Every kernel starts with kernel_prologue():
+// it lets the next kernel of the stream begin launching, then waits until
+// the kernels it depends on have completed and their writes are visible.
+// Both instructions do nothing when the launch did not ask for it.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ void kernel_prologue() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    asm volatile("griddepcontrol.wait;" ::: "memory");
 }
 
 // ---------------------------------------------------------------------------

@@ -58,6 +58,7 @@ __device__ __forceinline__ uint32_t fold_elem(const void *const *in, int R, uint
 // ---------------------------------------------------------------------------
 template <int DT, bool VEC>
 __global__ void __launch_bounds__(1024) k_one_shot_hb(const __grid_constant__ HbArgs a) {
+    kernel_prologue();
     constexpr int PV = VEC ? Elem<DT>::kPerVec : 1;
     const int R = a.R;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -115,6 +116,7 @@ __global__ void __launch_bounds__(1024) k_one_shot_hb(const __grid_constant__ Hb
 // ---------------------------------------------------------------------------
 template <int DT, bool VEC, bool SCATTER>
 __global__ void __launch_bounds__(kRegThreads) k_reduce(const __grid_constant__ HbArgs a) {
+    kernel_prologue();
     constexpr int PV = VEC ? Elem<DT>::kPerVec : 1;
     const int R = a.R;
     const uint64_t units = a.n / PV;
@@ -160,6 +162,7 @@ __global__ void __launch_bounds__(kRegThreads) k_reduce(const __grid_constant__ 
 // ---------------------------------------------------------------------------
 template <int ESZ, bool VEC>
 __global__ void __launch_bounds__(kRegThreads) k_all_gather(const __grid_constant__ HbArgs a) {
+    kernel_prologue();
     constexpr int PV = VEC ? 16 / ESZ : 1;
     const int R = a.R;
     const uint64_t units = a.n / PV;
@@ -206,6 +209,7 @@ __global__ void __launch_bounds__(kRegThreads) k_all_gather(const __grid_constan
 // ---------------------------------------------------------------------------
 template <int DT>
 __global__ void __launch_bounds__(kRegThreads) k_round(const float *src, void *dst, uint64_t n) {
+    kernel_prologue();
     const uint64_t stride = (uint64_t)gridDim.x * blockDim.x;
     for (uint64_t i = (uint64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += stride)
         st_elem<DT>(dst, i, narrow1<DT>(src[i]));
@@ -215,68 +219,59 @@ __global__ void __launch_bounds__(kRegThreads) k_round(const float *src, void *d
 // Launchers.
 // ---------------------------------------------------------------------------
 template <int DT>
-static cudaError_t one_shot_dt(const HbArgs &a, bool vec, int grid, int block, cudaStream_t s) {
+static cudaError_t one_shot_dt(const HbArgs &a, bool vec, int grid, int block, cudaStream_t s,
+                               bool pdl) {
     if (vec)
-        k_one_shot_hb<DT, true><<<grid, block, 0, s>>>(a);
-    else
-        k_one_shot_hb<DT, false><<<grid, block, 0, s>>>(a);
-    return cudaGetLastError();
+        return launch_kernel(k_one_shot_hb<DT, true>, grid, block, 0, s, pdl, a);
+    return launch_kernel(k_one_shot_hb<DT, false>, grid, block, 0, s, pdl, a);
 }
 
 cudaError_t launch_one_shot_hb(const HbArgs &a, int dtype, bool vec, int grid, int block,
-                               cudaStream_t s) {
+                               cudaStream_t s, bool pdl) {
     switch (dtype) {
-    case AR_BF16: return one_shot_dt<AR_BF16>(a, vec, grid, block, s);
-    case AR_FP16: return one_shot_dt<AR_FP16>(a, vec, grid, block, s);
-    default: return one_shot_dt<AR_FP32>(a, vec, grid, block, s);
+    case AR_BF16: return one_shot_dt<AR_BF16>(a, vec, grid, block, s, pdl);
+    case AR_FP16: return one_shot_dt<AR_FP16>(a, vec, grid, block, s, pdl);
+    default: return one_shot_dt<AR_FP32>(a, vec, grid, block, s, pdl);
     }
 }
 
 template <int DT>
-static cudaError_t reduce_dt(const HbArgs &a, bool vec, bool scatter, int grid, cudaStream_t s) {
+static cudaError_t reduce_dt(const HbArgs &a, bool vec, bool scatter, int grid, cudaStream_t s,
+                             bool pdl) {
     if (vec && scatter)
-        k_reduce<DT, true, true><<<grid, kRegThreads, 0, s>>>(a);
-    else if (vec)
-        k_reduce<DT, true, false><<<grid, kRegThreads, 0, s>>>(a);
-    else if (scatter)
-        k_reduce<DT, false, true><<<grid, kRegThreads, 0, s>>>(a);
-    else
-        k_reduce<DT, false, false><<<grid, kRegThreads, 0, s>>>(a);
-    return cudaGetLastError();
+        return launch_kernel(k_reduce<DT, true, true>, grid, kRegThreads, 0, s, pdl, a);
+    if (vec)
+        return launch_kernel(k_reduce<DT, true, false>, grid, kRegThreads, 0, s, pdl, a);
+    if (scatter)
+        return launch_kernel(k_reduce<DT, false, true>, grid, kRegThreads, 0, s, pdl, a);
+    return launch_kernel(k_reduce<DT, false, false>, grid, kRegThreads, 0, s, pdl, a);
 }
 
 cudaError_t launch_reduce(const HbArgs &a, int dtype, bool vec, bool scatter_only, int grid,
-                          cudaStream_t s) {
+                          cudaStream_t s, bool pdl) {
     switch (dtype) {
-    case AR_BF16: return reduce_dt<AR_BF16>(a, vec, scatter_only, grid, s);
-    case AR_FP16: return reduce_dt<AR_FP16>(a, vec, scatter_only, grid, s);
-    default: return reduce_dt<AR_FP32>(a, vec, scatter_only, grid, s);
+    case AR_BF16: return reduce_dt<AR_BF16>(a, vec, scatter_only, grid, s, pdl);
+    case AR_FP16: return reduce_dt<AR_FP16>(a, vec, scatter_only, grid, s, pdl);
+    default: return reduce_dt<AR_FP32>(a, vec, scatter_only, grid, s, pdl);
     }
 }
 
-cudaError_t launch_all_gather(const HbArgs &a, int dtype, bool vec, int grid, cudaStream_t s) {
-    if (elem_size(dtype) == 2) {
-        if (vec)
-            k_all_gather<2, true><<<grid, kRegThreads, 0, s>>>(a);
-        else
-            k_all_gather<2, false><<<grid, kRegThreads, 0, s>>>(a);
-    } else {
-        if (vec)
-            k_all_gather<4, true><<<grid, kRegThreads, 0, s>>>(a);
-        else
-            k_all_gather<4, false><<<grid, kRegThreads, 0, s>>>(a);
-    }
-    return cudaGetLastError();
+cudaError_t launch_all_gather(const HbArgs &a, int dtype, bool vec, int grid, cudaStream_t s,
+                              bool pdl) {
+    if (elem_size(dtype) == 2)
+        return vec ? launch_kernel(k_all_gather<2, true>, grid, kRegThreads, 0, s, pdl, a)
+                   : launch_kernel(k_all_gather<2, false>, grid, kRegThreads, 0, s, pdl, a);
+    return vec ? launch_kernel(k_all_gather<4, true>, grid, kRegThreads, 0, s, pdl, a)
+               : launch_kernel(k_all_gather<4, false>, grid, kRegThreads, 0, s, pdl, a);
 }
 
 cudaError_t launch_round(int dtype, const float *src, void *dst, uint64_t n, int grid,
                          cudaStream_t s) {
     switch (dtype) {
-    case AR_BF16: k_round<AR_BF16><<<grid, kRegThreads, 0, s>>>(src, dst, n); break;
-    case AR_FP16: k_round<AR_FP16><<<grid, kRegThreads, 0, s>>>(src, dst, n); break;
-    default: k_round<AR_FP32><<<grid, kRegThreads, 0, s>>>(src, dst, n); break;
+    case AR_BF16: return launch_kernel(k_round<AR_BF16>, grid, kRegThreads, 0, s, false, src, dst, n);
+    case AR_FP16: return launch_kernel(k_round<AR_FP16>, grid, kRegThreads, 0, s, false, src, dst, n);
+    default: return launch_kernel(k_round<AR_FP32>, grid, kRegThreads, 0, s, false, src, dst, n);
     }
-    return cudaGetLastError();
 }
 
 }  // namespace ar

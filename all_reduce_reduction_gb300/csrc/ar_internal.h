@@ -27,6 +27,30 @@ constexpr int kTmaMaxStages = 4;
 
 inline size_t elem_size(int dtype) { return dtype == AR_FP32 ? 4 : 2; }
 
+// Launch kernel(args...) on stream s.  With `pdl` the launch allows
+// programmatic dependent launch: it may start while the previous kernel in
+// the stream drains, and every kernel of this library waits (griddepcontrol
+// .wait) before its first global-memory access, so only the launch latency
+// overlaps, never the data.
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_kernel(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                                 cudaStream_t s, bool pdl, Args &&...args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    cfg.numAttrs = 0;
+    if (pdl) {
+        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[0].val.programmaticStreamSerializationAllowed = 1;
+        cfg.numAttrs = 1;
+    }
+    cfg.attrs = attr;
+    return cudaLaunchKernelEx(&cfg, kernel, static_cast<Args &&>(args)...);
+}
+
 // The R ranks' buffers.  512 bytes for R = 32.
 struct RankPtrs {
     const void *in[AR_MAX_RANKS];
@@ -77,6 +101,18 @@ struct LlArgs {
     Ctl c;
 };
 
+// LL one-shot through thread-block clusters (distributed shared memory).
+struct LlClusterArgs {
+    RankPtrs p;
+    uint64_t n;               // elements per rank
+    uint64_t units_per_chunk; // 16-byte units per rank per chunk (Uc)
+    int R;                    // cluster size = virtual ranks
+    Ctl c;
+};
+// Receive-buffer budget per CTA of the cluster LL kernel.
+constexpr int kLlClusterMaxSmem = 96 * 1024;
+constexpr int kLlClusterTargetSmem = 64 * 1024;
+
 // Standalone packet encode/decode and rounding.
 struct PackArgs {
     const void *src;
@@ -92,22 +128,34 @@ struct PackArgs {
 
 // ar_hb.cu
 cudaError_t launch_one_shot_hb(const HbArgs &a, int dtype, bool vec, int grid, int block,
-                               cudaStream_t s);
+                               cudaStream_t s, bool pdl = false);
 cudaError_t launch_reduce(const HbArgs &a, int dtype, bool vec, bool scatter_only, int grid,
-                          cudaStream_t s);
-cudaError_t launch_all_gather(const HbArgs &a, int dtype, bool vec, int grid, cudaStream_t s);
+                          cudaStream_t s, bool pdl = false);
+cudaError_t launch_all_gather(const HbArgs &a, int dtype, bool vec, int grid, cudaStream_t s,
+                              bool pdl = false);
 cudaError_t launch_round(int dtype, const float *src, void *dst, uint64_t n, int grid,
                          cudaStream_t s);
 
 // ar_tma.cu
 cudaError_t tma_prepare(int dtype, int *max_dynamic_smem);   // opt in to large shared memory
 size_t tma_smem_bytes(int R, int tile_bytes, int stages);
-cudaError_t launch_two_shot_tma(const TmaArgs &a, int dtype, int grid, cudaStream_t s);
+cudaError_t launch_two_shot_tma(const TmaArgs &a, int dtype, int grid, cudaStream_t s,
+                                bool pdl = false);
 
 // ar_ll.cu
 cudaError_t ll_occupancy(int dtype, bool vec, bool two_shot, int *blocks_per_sm);
-cudaError_t launch_ll(const LlArgs &a, int dtype, bool vec, bool two_shot, cudaStream_t s);
-cudaError_t launch_pack(const PackArgs &a, int dtype, bool vec, int grid, cudaStream_t s);
-cudaError_t launch_unpack(const PackArgs &a, int dtype, bool vec, int grid, cudaStream_t s);
+cudaError_t launch_ll(const LlArgs &a, int dtype, bool vec, bool two_shot, cudaStream_t s,
+                      bool pdl = false);
+cudaError_t launch_pack(const PackArgs &a, int dtype, bool vec, int grid, cudaStream_t s,
+                        bool pdl = false);
+cudaError_t launch_unpack(const PackArgs &a, int dtype, bool vec, int grid, cudaStream_t s,
+                          bool pdl = false);
+
+// ar_ll_cluster.cu
+size_t ll_cluster_smem_bytes(int R, uint64_t units_per_chunk);
+cudaError_t ll_cluster_prepare(int dtype, int R);
+cudaError_t ll_cluster_max_clusters(const LlClusterArgs &a, int dtype, int *clusters);
+cudaError_t launch_ll_cluster(const LlClusterArgs &a, int dtype, int nclusters, cudaStream_t s,
+                              bool pdl = false);
 
 }  // namespace ar

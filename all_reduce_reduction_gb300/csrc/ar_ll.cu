@@ -30,30 +30,6 @@
 
 namespace ar {
 
-// Payload word q (message bytes [4q, 4q + 4), zero past the end) of an
-// n-element buffer, element by element (any alignment of the buffer).
-template <int ESZ>
-__device__ __forceinline__ uint32_t load_payload(const void *base, uint64_t n, uint64_t q) {
-    if (ESZ == 4)
-        return reinterpret_cast<const uint32_t *>(base)[q];
-    const uint16_t *b = reinterpret_cast<const uint16_t *>(base);
-    const uint32_t lo = b[2 * q];
-    const uint32_t hi = (2 * q + 1 < n) ? (uint32_t)b[2 * q + 1] : 0u;
-    return lo | (hi << 16);
-}
-
-template <int ESZ>
-__device__ __forceinline__ void store_payload(void *base, uint64_t n, uint64_t q, uint32_t pl) {
-    if (ESZ == 4) {
-        reinterpret_cast<uint32_t *>(base)[q] = pl;
-        return;
-    }
-    uint16_t *b = reinterpret_cast<uint16_t *>(base);
-    b[2 * q] = (uint16_t)pl;
-    if (2 * q + 1 < n)
-        b[2 * q + 1] = (uint16_t)(pl >> 16);
-}
-
 __device__ __forceinline__ uint2 ld_v2(const void *p) {
     uint2 v;
     asm volatile("ld.global.L1::no_allocate.v2.u32 {%0, %1}, [%2];"
@@ -136,6 +112,7 @@ __global__ void __launch_bounds__(kLlThreads) k_ll(const __grid_constant__ LlArg
     const int R = a.R, G = a.G;
     const int r = blockIdx.x % R, gi = blockIdx.x / R;
     const uint64_t tid = threadIdx.x, T = blockDim.x;
+    kernel_prologue();
     const uint32_t flag = call_flag(a.c);
     Poller w{&a.c, flag, 0};
 
@@ -156,10 +133,21 @@ __global__ void __launch_bounds__(kLlThreads) k_ll(const __grid_constant__ LlArg
     // ---- put: rank r's input -> slot r (one 8-byte store per packet) -------
     if (a.c.drop_rank != r) {
         if constexpr (VEC) {
+            // four units' loads are in flight before the first packet store
+            constexpr int kPut = 4;
             const uint2 *src = reinterpret_cast<const uint2 *>(a.p.in[r]);
-            for (uint64_t u = ustart; u < U; u += ustep) {
-                const uint2 v = ld_v2(src + u);
-                st_pkt2(slot_r + 2 * u, make_pkt(v.x, flag), make_pkt(v.y, flag));
+            for (uint64_t u0 = ustart; u0 < U; u0 += kPut * ustep) {
+                uint2 v[kPut];
+#pragma unroll
+                for (int j = 0; j < kPut; ++j)
+                    if (u0 + j * ustep < U)
+                        v[j] = ld_v2(src + u0 + j * ustep);
+#pragma unroll
+                for (int j = 0; j < kPut; ++j) {
+                    const uint64_t u = u0 + j * ustep;
+                    if (u < U)
+                        st_pkt2(slot_r + 2 * u, make_pkt(v[j].x, flag), make_pkt(v[j].y, flag));
+                }
             }
         }
         for (uint64_t q = q0; q < P; q += qstep)
@@ -266,17 +254,23 @@ cudaError_t ll_occupancy(int dtype, bool vec, bool two_shot, int *blocks_per_sm)
                                                          kLlThreads, 0);
 }
 
-cudaError_t launch_ll(const LlArgs &a, int dtype, bool vec, bool two_shot, cudaStream_t s) {
+cudaError_t launch_ll(const LlArgs &a, int dtype, bool vec, bool two_shot, cudaStream_t s,
+                      bool pdl) {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)(a.R * a.G));
     cfg.blockDim = dim3(kLlThreads);
     cfg.dynamicSmemBytes = 0;
     cfg.stream = s;
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeCooperative;
     attr[0].val.cooperative = 1;
-    cfg.attrs = attr;
     cfg.numAttrs = 1;
+    if (pdl) {
+        attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[1].val.programmaticStreamSerializationAllowed = 1;
+        cfg.numAttrs = 2;
+    }
+    cfg.attrs = attr;
     void *args[] = {const_cast<LlArgs *>(&a)};
     return cudaLaunchKernelExC(&cfg, ll_kernel_for(dtype, vec, two_shot), args);
 }
@@ -287,6 +281,7 @@ cudaError_t launch_ll(const LlArgs &a, int dtype, bool vec, bool two_shot, cudaS
 // ---------------------------------------------------------------------------
 template <int ESZ, bool VEC>
 __global__ void __launch_bounds__(kRegThreads) k_pack(const __grid_constant__ PackArgs a) {
+    kernel_prologue();
     const uint64_t nbytes = a.n * ESZ, P = (nbytes + 3) / 4;
     const uint64_t U = VEC ? nbytes / 8 : 0;
     const uint64_t stride = (uint64_t)gridDim.x * blockDim.x;
@@ -301,6 +296,7 @@ __global__ void __launch_bounds__(kRegThreads) k_pack(const __grid_constant__ Pa
 
 template <int ESZ, bool VEC>
 __global__ void __launch_bounds__(kRegThreads) k_unpack(const __grid_constant__ PackArgs a) {
+    kernel_prologue();
     const uint64_t nbytes = a.n * ESZ, P = (nbytes + 3) / 4;
     const uint64_t U = VEC ? nbytes / 8 : 0;
     const uint64_t stride = (uint64_t)gridDim.x * blockDim.x;
@@ -331,26 +327,22 @@ __global__ void __launch_bounds__(kRegThreads) k_unpack(const __grid_constant__ 
         record_error(a.status, AR_ERR_FLAG_MISMATCH);
 }
 
-cudaError_t launch_pack(const PackArgs &a, int dtype, bool vec, int grid, cudaStream_t s) {
-    if (elem_size(dtype) == 2) {
-        if (vec) k_pack<2, true><<<grid, kRegThreads, 0, s>>>(a);
-        else k_pack<2, false><<<grid, kRegThreads, 0, s>>>(a);
-    } else {
-        if (vec) k_pack<4, true><<<grid, kRegThreads, 0, s>>>(a);
-        else k_pack<4, false><<<grid, kRegThreads, 0, s>>>(a);
-    }
-    return cudaGetLastError();
+cudaError_t launch_pack(const PackArgs &a, int dtype, bool vec, int grid, cudaStream_t s,
+                        bool pdl) {
+    if (elem_size(dtype) == 2)
+        return vec ? launch_kernel(k_pack<2, true>, grid, kRegThreads, 0, s, pdl, a)
+                   : launch_kernel(k_pack<2, false>, grid, kRegThreads, 0, s, pdl, a);
+    return vec ? launch_kernel(k_pack<4, true>, grid, kRegThreads, 0, s, pdl, a)
+               : launch_kernel(k_pack<4, false>, grid, kRegThreads, 0, s, pdl, a);
 }
 
-cudaError_t launch_unpack(const PackArgs &a, int dtype, bool vec, int grid, cudaStream_t s) {
-    if (elem_size(dtype) == 2) {
-        if (vec) k_unpack<2, true><<<grid, kRegThreads, 0, s>>>(a);
-        else k_unpack<2, false><<<grid, kRegThreads, 0, s>>>(a);
-    } else {
-        if (vec) k_unpack<4, true><<<grid, kRegThreads, 0, s>>>(a);
-        else k_unpack<4, false><<<grid, kRegThreads, 0, s>>>(a);
-    }
-    return cudaGetLastError();
+cudaError_t launch_unpack(const PackArgs &a, int dtype, bool vec, int grid, cudaStream_t s,
+                          bool pdl) {
+    if (elem_size(dtype) == 2)
+        return vec ? launch_kernel(k_unpack<2, true>, grid, kRegThreads, 0, s, pdl, a)
+                   : launch_kernel(k_unpack<2, false>, grid, kRegThreads, 0, s, pdl, a);
+    return vec ? launch_kernel(k_unpack<4, true>, grid, kRegThreads, 0, s, pdl, a)
+               : launch_kernel(k_unpack<4, false>, grid, kRegThreads, 0, s, pdl, a);
 }
 
 }  // namespace ar

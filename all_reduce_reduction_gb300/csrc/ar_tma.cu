@@ -155,6 +155,7 @@ __global__ void __launch_bounds__(kTmaThreads, 1) k_two_shot_tma(const __grid_co
         fence_mbar_init();
     }
     __syncthreads();
+    kernel_prologue();
 
     uint64_t issued = 0;   // producer: items whose loads were issued
     if (warp == 0) {
@@ -289,14 +290,13 @@ cudaError_t tma_prepare(int dtype, int *max_dynamic_smem) {
     }
 }
 
-cudaError_t launch_two_shot_tma(const TmaArgs &a, int dtype, int grid, cudaStream_t s) {
+cudaError_t launch_two_shot_tma(const TmaArgs &a, int dtype, int grid, cudaStream_t s, bool pdl) {
     const size_t smem = tma_smem_bytes(a.R, a.tile_bytes, a.stages);
     switch (dtype) {
-    case AR_BF16: k_two_shot_tma<AR_BF16><<<grid, kTmaThreads, smem, s>>>(a); break;
-    case AR_FP16: k_two_shot_tma<AR_FP16><<<grid, kTmaThreads, smem, s>>>(a); break;
-    default: k_two_shot_tma<AR_FP32><<<grid, kTmaThreads, smem, s>>>(a); break;
+    case AR_BF16: return launch_kernel(k_two_shot_tma<AR_BF16>, grid, kTmaThreads, smem, s, pdl, a);
+    case AR_FP16: return launch_kernel(k_two_shot_tma<AR_FP16>, grid, kTmaThreads, smem, s, pdl, a);
+    default: return launch_kernel(k_two_shot_tma<AR_FP32>, grid, kTmaThreads, smem, s, pdl, a);
     }
-    return cudaGetLastError();
 }
 
 }  // namespace ar

@@ -36,6 +36,7 @@ sys.path.insert(0, ROOT)
 METRIC = ("all-reduce µs/call and GB/s vs msg size (R=8 bf16, 1 GB300), "
           "% of HBM roofline")
 FALLBACK_HBM_GBS = 6800.0
+TRANSPORTS = {"auto": 0, "global": 1, "cluster": 2}   # enum ar_ll_transport
 L2_FLUSH_BYTES = 256 << 20
 
 
@@ -245,6 +246,8 @@ class CaseRunner:
         self.ins = [t.cuda() for t in self.cpu_inputs]
         self.outs = [torch.empty_like(t) for t in self.ins]
         self.h = ar.Handle(w.R, w.n, w.dtype)
+        ar.ar_set_ll_transport(self.h.h, c.get("transport", ar.AR_LL_AUTO))
+        ar.ar_set_pdl(self.h.h, c.get("pdl", 1))
         self.algo, self.proto = ar.ALGOS[c["algo"]], ar.PROTOS[c["proto"]]
         self.bytes = case_bytes(c)
         with torch.cuda.stream(stream):
@@ -273,6 +276,9 @@ def run_ours(args, dist: Dist):
 
     torch.cuda.set_device(dist.local_rank)
     desc, cases = workload_cases(args.workload, args)
+    for c in cases:
+        c["transport"] = TRANSPORTS[args.ll_transport]
+        c["pdl"] = 0 if args.no_pdl else 1
     stream = torch.cuda.Stream()
     runners = [CaseRunner(c, stream) for c in cases]
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device="cuda")
@@ -339,6 +345,11 @@ def run_ours(args, dist: Dist):
     peak, peak_kind = hbm_peak()
     achieved = dr.bytes / launch_s / 1e9
     kkey = "%s_%s_r%d_n%d_%s" % (dr.c["algo"], dr.c["proto"], dr.w.R, dr.w.n, dr.w.dtype)
+    if dr.c["proto"] == "ll" and dr.c["algo"] == "one_shot":
+        info = ar.ar_get_info(dr.h.h)
+        tr = dr.c.get("transport", ar.AR_LL_AUTO)
+        cluster = bool(info["ll_cluster_ok"]) and tr == ar.AR_LL_CLUSTER
+        kkey = kkey.replace("_ll_", "_ll_cluster_" if cluster else "_ll_global_")
     roofline = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                 "frac": round(achieved / peak, 4), "traffic": committed_traffic(kkey),
                 "kernel": kkey, "peak_source": peak_kind + " (MEASURED_PEAKS.json hbm_gbs)"
@@ -398,7 +409,9 @@ def run_ours(args, dist: Dist):
         "config": {"workload": desc, "R": runners[0].w.R,
                    "sizes_elems_per_rank": [r.w.n for r in runners],
                    "algo": cases[0]["algo"], "proto": cases[0]["proto"],
+                   "ll_transport": args.ll_transport if cases[0]["proto"] == "ll" else None,
                    "calls_per_graph": cases[0]["calls"],
+                   "programmatic_dependent_launch": not args.no_pdl,
                    "l2": ("flushed (256 MiB write) before every graph replay, outside the timed events"
                           if cases[0]["flush"] else "inputs larger than L2 (no flush)"),
                    "bytes_basis": "minimal: 2*R*N*elem_size per call",
@@ -425,9 +438,12 @@ def measure_variants(runners, stream, flush, K):
     import torch
     import all_reduce_reduction_gb300 as ar
     out = {}
-    for algo, proto in (("one_shot", "hb"), ("two_shot", "hb"), ("two_shot", "ll")):
+    for algo, proto, tr in (("one_shot", "hb", ar.AR_LL_AUTO), ("two_shot", "hb", ar.AR_LL_AUTO),
+                            ("two_shot", "ll", ar.AR_LL_AUTO),
+                            ("one_shot", "ll", ar.AR_LL_GLOBAL), ("one_shot", "ll", ar.AR_LL_CLUSTER)):
         row = {}
         for r in runners:
+            ar.ar_set_ll_transport(r.h.h, tr)
             g = torch.cuda.CUDAGraph()
             with torch.cuda.graph(g, stream=stream):
                 for _ in range(r.c["calls"]):
@@ -447,7 +463,11 @@ def measure_variants(runners, stream, flush, K):
                 e1.synchronize()
                 tot += e0.elapsed_time(e1)
             row[str(r.w.n)] = round(tot * 1e3 / (K * r.c["calls"]), 3)
-        out["%s_%s" % (algo, proto)] = row
+            ar.ar_set_ll_transport(r.h.h, r.c.get("transport", ar.AR_LL_AUTO))
+        key = "%s_%s" % (algo, proto)
+        if proto == "ll" and algo == "one_shot":
+            key += "_" + {ar.AR_LL_GLOBAL: "global", ar.AR_LL_CLUSTER: "cluster"}[tr]
+        out[key] = row
     torch.cuda.synchronize()
     return out
 
@@ -545,6 +565,9 @@ def main():
     p.add_argument("--algo", default="one_shot", choices=["one_shot", "two_shot"])
     p.add_argument("--proto", default="ll", choices=["ll", "hb"])
     p.add_argument("--calls", type=int, default=10)
+    p.add_argument("--ll-transport", default="auto", choices=["auto", "global", "cluster"])
+    p.add_argument("--no-pdl", action="store_true",
+                   help="launch without programmatic dependent launch")
     p.add_argument("--impl", default="ours", choices=["ours", "reference"])
     p.add_argument("--cpu-seconds", type=float, default=10.0)
     p.add_argument("--no-cpu-baseline", action="store_true")

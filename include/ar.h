@@ -104,6 +104,24 @@ enum ar_proto {
     AR_HB = 1
 };
 
+/* How one-shot LL packets travel between virtual peers.
+ *   AR_LL_GLOBAL:  through per-sender slots in the handle's scratch (HBM/L2),
+ *                  the layout real peers over NVLink would use; one
+ *                  cooperative kernel for all ranks.
+ *   AR_LL_CLUSTER: the R peers of a chunk form one thread-block cluster and
+ *                  store their packets straight into each other's shared
+ *                  memory (distributed shared memory), each receiver polling
+ *                  its own; used where it applies (one-shot, R <= 16, every
+ *                  buffer 16-byte aligned), AR_LL_GLOBAL elsewhere.
+ *   AR_LL_AUTO:    AR_LL_GLOBAL (default; on GB300 the global-memory
+ *                  exchange measured faster at every message size).
+ * All three give identical results. */
+enum ar_ll_transport {
+    AR_LL_AUTO = 0,
+    AR_LL_GLOBAL = 1,
+    AR_LL_CLUSTER = 2
+};
+
 enum ar_status_code {
     AR_OK = 0,
     AR_ERR_INVALID = 1,        /* bad argument (null, range, aliasing, device) */
@@ -129,6 +147,11 @@ typedef struct ar_info {
     int tma_tile_bytes;        /* per-rank tile of the two-shot TMA kernel     */
     int tma_stages;            /* pipeline stages of the two-shot TMA kernel   */
     uint64_t timeout_ns;       /* current device-side wait limit               */
+    int ll_transport;          /* enum ar_ll_transport in force                */
+    int ll_cluster_ok;         /* 1 if the cluster LL kernel can run           */
+    int ll_cluster_units;      /* its 16-byte units per rank per chunk         */
+    int ll_cluster_max;        /* its co-resident clusters                     */
+    int pdl;                   /* 1 if launches use programmatic dependent launch */
 } ar_info;
 
 /* Create a handle for R virtual ranks of N elements of `dtype` each, on the
@@ -212,6 +235,22 @@ int ar_status(ar_handle_t h, cudaStream_t stream);
  * default.  A wait past the limit records AR_ERR_TIMEOUT, makes the other
  * waiters of the same call give up, and the kernel returns normally. */
 int ar_set_timeout(ar_handle_t h, uint64_t ns);
+
+/* Programmatic dependent launch for the handle's later calls (1 = on, the
+ * default; 0 = off).  On, a call's kernel may begin launching while the
+ * previous kernel of the stream is still draining; it waits for that
+ * kernel's completion before its first global-memory access, so results
+ * are unchanged and only launch latency is hidden -- the per-call overhead
+ * that dominates the small messages the LL protocol serves (SGLang guide,
+ * section 1: latency enters every generated token).  Errors: AR_ERR_INVALID. */
+int ar_set_pdl(ar_handle_t h, int enable);
+
+/* Choose how later one-shot LL calls move packets (enum ar_ll_transport).
+ * The MemoryChannel lets GPU threads write a peer's memory directly
+ * (MSCCL++ summary, section "MemoryChannel"); for virtual peers on one GPU
+ * that memory can be HBM or a cluster peer's shared memory.
+ * Errors: AR_ERR_INVALID. */
+int ar_set_ll_transport(ar_handle_t h, int transport);
 
 /* Fault injection for tests: virtual rank `rank` (0..R-1) writes no LL
  * packets in later LL calls, so its peers' polls time out (AR_ERR_TIMEOUT

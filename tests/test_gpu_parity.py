@@ -18,7 +18,8 @@ pytestmark = pytest.mark.gpu
 DTYPES = ["bf16", "fp16", "fp32"]
 
 
-def run_case(R, n, dtype, algo, proto, dist="loguniform", config=40, offset=0, inplace=False):
+def run_case(R, n, dtype, algo, proto, dist="loguniform", config=40, offset=0, inplace=False,
+             transport=None):
     need_gpu()
     cpu = wl.make_inputs(config, R, n, dtype, dist)
     want = expected(cpu, dtype)
@@ -28,6 +29,8 @@ def run_case(R, n, dtype, algo, proto, dist="loguniform", config=40, offset=0, i
     else:
         bufs, outs = guarded_outputs(R, n, dtype, offset)
     with ar.Handle(R, n, dtype) as h:
+        if transport is not None:
+            ar.ar_set_ll_transport(h.h, transport)
         ar.ar_allreduce(h.h, ins, outs, algo, proto)
         st = ar.ar_status(h.h)
         assert st == ar.AR_OK, ar.ar_strerror(st)
@@ -50,6 +53,34 @@ def test_small_config_every_path():
 @pytest.mark.parametrize("n", [1, 3, 8, 9, 100, 4097, 70001])
 def test_parity_matrix(path, dtype, R, n):
     run_case(R, n, dtype, *path)
+
+
+TRANSPORTS = [ar.AR_LL_GLOBAL, ar.AR_LL_CLUSTER]
+TRANSPORT_IDS = ["global", "cluster"]
+
+
+@pytest.mark.parametrize("transport", TRANSPORTS, ids=TRANSPORT_IDS)
+@pytest.mark.parametrize("dtype", DTYPES)
+@pytest.mark.parametrize("R", [1, 2, 3, 5, 8, 12, 16])
+@pytest.mark.parametrize("n", [1, 7, 8, 9, 100, 4097, 70001, (1 << 20) + 3])
+def test_ll_one_shot_transports(transport, dtype, R, n):
+    """One-shot LL through HBM slots and through cluster shared memory."""
+    run_case(R, n, dtype, ar.AR_ONE_SHOT, ar.AR_LL, transport=transport)
+
+
+def test_cluster_transport_available_up_to_eight_ranks():
+    need_gpu()
+    for R in (1, 2, 3, 4, 5, 6, 7, 8):
+        with ar.Handle(R, 4096, "bf16") as h:
+            info = ar.ar_get_info(h.h)
+            assert info["ll_cluster_ok"] == 1 and info["ll_cluster_max"] > 0, (R, info)
+
+
+@pytest.mark.parametrize("transport", TRANSPORTS, ids=TRANSPORT_IDS)
+@pytest.mark.parametrize("offset", [0, 1])
+def test_ll_transports_in_place(transport, offset):
+    run_case(8, 70001, "bf16", ar.AR_ONE_SHOT, ar.AR_LL, transport=transport, offset=offset,
+             inplace=True)
 
 
 @pytest.mark.parametrize("path", ALL_PATHS, ids=PATH_IDS)
@@ -151,8 +182,9 @@ def test_ll_unpack_partial_mismatch(dtype):
     assert_bits_equal(dst, want, dtype, "partial unpack")
 
 
+@pytest.mark.parametrize("transport", TRANSPORTS, ids=TRANSPORT_IDS)
 @pytest.mark.parametrize("path", ALL_PATHS, ids=PATH_IDS)
-def test_graph_replays_see_new_inputs(path):
+def test_graph_replays_see_new_inputs(path, transport):
     """10 calls captured in one CUDA graph; the inputs change between replays.
     A flag frozen at capture time would let LL receivers accept the previous
     replay's packets; the device epoch must prevent that."""
@@ -162,6 +194,7 @@ def test_graph_replays_see_new_inputs(path):
     ins = [torch.empty(n, dtype=torch.bfloat16, device="cuda") for _ in range(R)]
     outs = [torch.empty_like(t) for t in ins]
     h = ar.Handle(R, n, dtype)
+    ar.ar_set_ll_transport(h.h, transport)
     s = torch.cuda.Stream()
     with torch.cuda.stream(s):
         for t in ins:
@@ -187,8 +220,11 @@ def test_graph_replays_see_new_inputs(path):
     h.close()
 
 
-@pytest.mark.parametrize("algo", [ar.AR_ONE_SHOT, ar.AR_TWO_SHOT], ids=["one_shot", "two_shot"])
-def test_ll_timeout_then_recovery(algo):
+@pytest.mark.parametrize("algo,transport", [(ar.AR_ONE_SHOT, ar.AR_LL_GLOBAL),
+                                             (ar.AR_ONE_SHOT, ar.AR_LL_CLUSTER),
+                                             (ar.AR_TWO_SHOT, ar.AR_LL_GLOBAL)],
+                         ids=["one_shot_global", "one_shot_cluster", "two_shot"])
+def test_ll_timeout_then_recovery(algo, transport):
     """A rank that never writes its packets: the peers' bounded polls give up,
     AR_ERR_TIMEOUT is reported, and the next normal call is correct."""
     need_gpu()
@@ -197,6 +233,7 @@ def test_ll_timeout_then_recovery(algo):
     ins = device_inputs(cpu)
     outs = [torch.empty_like(t) for t in ins]
     with ar.Handle(R, n, dtype) as h:
+        ar.ar_set_ll_transport(h.h, transport)
         ar.ar_set_timeout(h.h, 20_000_000)      # 20 ms
         ar.ar_debug_drop_rank(h.h, 2)
         ar.ar_allreduce(h.h, ins, outs, algo, ar.AR_LL)
@@ -253,3 +290,66 @@ def test_round_exhaustive_vs_oracle(dtype):
         want = oracle.round_f32(f, wl.DTYPE_CODE[dtype])
         nan = np.isnan(f)
         assert np.array_equal(got[~nan], want[~nan]), "chunk at %#x" % start
+
+
+@pytest.mark.parametrize("pdl", [1, 0], ids=["pdl", "no_pdl"])
+@pytest.mark.parametrize("captured", [False, True], ids=["eager", "graph"])
+def test_chained_calls_wait_for_their_inputs(pdl, captured):
+    """Each call reads the previous call's outputs.  With programmatic
+    dependent launch a kernel may start before the previous one ends; it
+    must still see that kernel's results (it waits before reading)."""
+    need_gpu()
+    R, n, dtype = 8, 70001, "bf16"
+    cpu = wl.make_inputs(45, R, n, dtype, "uniform")
+    bufs = [device_inputs(cpu)] + [[torch.empty(n, dtype=torch.bfloat16, device="cuda")
+                                    for _ in range(R)] for _ in range(len(ALL_PATHS))]
+    for b in bufs[1:]:
+        for t in b:
+            t.fill_(float("nan"))
+    h = ar.Handle(R, n, dtype)
+    ar.ar_set_pdl(h.h, pdl)
+    s = torch.cuda.Stream()
+
+    def chain():
+        for i, (algo, proto) in enumerate(ALL_PATHS):
+            ar.ar_allreduce(h.h, bufs[i], bufs[i + 1], algo, proto, stream=s)
+
+    with torch.cuda.stream(s):
+        if captured:
+            chain()                          # warm-up outside capture
+            s.synchronize()
+            for b in bufs[1:]:
+                for t in b:
+                    t.fill_(float("nan"))
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=s):
+                chain()
+            g.replay()
+        else:
+            chain()
+    torch.cuda.synchronize()
+    assert ar.ar_status(h.h) == ar.AR_OK
+    h.close()
+    want = [wl.bits(t) for t in cpu]
+    for i in range(len(ALL_PATHS)):
+        want = [oracle.allreduce(want, wl.DTYPE_CODE[dtype])[0]] * R
+        for r in range(R):
+            assert_bits_equal(bufs[i + 1][r], want[0], dtype, "step %d rank %d" % (i, r))
+
+
+@pytest.mark.parametrize("path", ALL_PATHS, ids=PATH_IDS)
+@pytest.mark.parametrize("n", [9, 4097, (1 << 20) + 5])
+def test_parity_without_pdl(path, n):
+    need_gpu()
+    R, dtype = 8, "fp16"
+    cpu = wl.make_inputs(46, R, n, dtype, "normal")
+    ins = device_inputs(cpu)
+    outs = [torch.empty_like(t) for t in ins]
+    with ar.Handle(R, n, dtype) as h:
+        ar.ar_set_pdl(h.h, 0)
+        assert ar.ar_get_info(h.h)["pdl"] == 0
+        ar.ar_allreduce(h.h, ins, outs, *path)
+        assert ar.ar_status(h.h) == ar.AR_OK
+    want = expected(cpu, dtype)
+    for r in range(R):
+        assert_bits_equal(outs[r], want, dtype, "rank %d" % r)

@@ -27,11 +27,12 @@ def oracle_single_output(cpu_inputs, dtype):
     return out
 
 
-def run_graph(w, algo, proto, cpu, calls=10, warm=2):
+def run_graph(w, algo, proto, cpu, calls=10, warm=2, transport=ar.AR_LL_AUTO):
     ins = [t.cuda() for t in cpu]
     outs = [torch.full_like(t, float("nan")) for t in ins]
     s = torch.cuda.Stream()
     with ar.Handle(w.R, w.n, w.dtype) as h:
+        ar.ar_set_ll_transport(h.h, transport)
         with torch.cuda.stream(s):
             ar.ar_allreduce(h.h, ins, outs, algo, proto, stream=s)
         s.synchronize()
@@ -46,14 +47,17 @@ def run_graph(w, algo, proto, cpu, calls=10, warm=2):
     return outs
 
 
+@pytest.mark.parametrize("transport", [ar.AR_LL_AUTO, ar.AR_LL_GLOBAL], ids=["auto", "global"])
 @pytest.mark.parametrize("path", ALL_PATHS, ids=PATH_IDS)
-def test_ll_sweep_sizes(path):
+def test_ll_sweep_sizes(path, transport):
     """R=8 bf16, N = 2^9..2^18, uniform [-1, 1), 10 calls per graph."""
     need_gpu()
+    if transport != ar.AR_LL_AUTO and path[1] != ar.AR_LL:
+        pytest.skip("transport applies to LL only")
     for w in wl.LL_SWEEP:
         cpu = w.inputs()
         want = oracle_single_output(cpu, w.dtype)
-        outs = run_graph(w, *path, cpu)
+        outs = run_graph(w, *path, cpu, transport=transport)
         for r in range(w.R):
             assert_bits_equal(outs[r], want, w.dtype, "%s rank %d" % (w.name, r))
 
