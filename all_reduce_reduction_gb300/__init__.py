@@ -21,8 +21,8 @@ LIB_PATH = os.path.join(HERE, "libar_gb300.so")
 
 # enum ar_dtype / ar_algo / ar_proto / ar_status_code (include/ar.h)
 AR_BF16, AR_FP16, AR_FP32 = 0, 1, 2
-AR_ONE_SHOT, AR_TWO_SHOT = 0, 1
-AR_LL, AR_HB = 0, 1
+AR_ONE_SHOT, AR_TWO_SHOT, AR_ALGO_AUTO = 0, 1, 2
+AR_LL, AR_HB, AR_PROTO_AUTO = 0, 1, 2
 AR_OK = 0
 AR_ERR_INVALID = 1
 AR_ERR_UNSUPPORTED = 2
@@ -35,8 +35,8 @@ AR_MAX_RANKS = 32
 AR_LL_MAX_BYTES = 64 << 20
 
 DTYPES = {"bf16": AR_BF16, "fp16": AR_FP16, "fp32": AR_FP32}
-ALGOS = {"one_shot": AR_ONE_SHOT, "two_shot": AR_TWO_SHOT}
-PROTOS = {"ll": AR_LL, "hb": AR_HB}
+ALGOS = {"one_shot": AR_ONE_SHOT, "two_shot": AR_TWO_SHOT, "auto": AR_ALGO_AUTO}
+PROTOS = {"ll": AR_LL, "hb": AR_HB, "auto": AR_PROTO_AUTO}
 
 
 class ArError(RuntimeError):
@@ -82,6 +82,10 @@ SIGNATURES = {
     "ar_create": ([_I, _SZ, _I, ctypes.POINTER(_VP)], _I),
     "ar_destroy": ([_VP], _I),
     "ar_allreduce": ([_VP, _VPP, _VPP, _I, _I, _VP], _I),
+    "ar_allreduce_n": ([_VP, _VPP, _VPP, _SZ, _I, _I, _VP], _I),
+    "ar_tune": ([_VP, _VP], _I),
+    "ar_get_tuning": ([_VP, _SZ, ctypes.POINTER(_I), ctypes.POINTER(_I),
+                       ctypes.POINTER(ctypes.c_float)], _I),
     "ar_reduce_scatter": ([_VP, _VPP, _VPP, _VP], _I),
     "ar_all_gather": ([_VP, _VPP, _VP], _I),
     "ar_ll_pack": ([_VP, _VP, _VP, _SZ, _U32, _VP], _I),
@@ -164,6 +168,27 @@ def ar_allreduce(h: int, ins, outs, algo=AR_ONE_SHOT, proto=AR_HB, stream=None) 
     proto = PROTOS[proto] if isinstance(proto, str) else proto
     _check(load_library().ar_allreduce(h, _ptr_array(ins), _ptr_array(outs), algo, proto,
                                        _stream(stream)), "ar_allreduce")
+
+
+def ar_allreduce_n(h: int, ins, outs, n: int, algo=AR_ALGO_AUTO, proto=AR_PROTO_AUTO,
+                   stream=None) -> None:
+    algo = ALGOS[algo] if isinstance(algo, str) else algo
+    proto = PROTOS[proto] if isinstance(proto, str) else proto
+    _check(load_library().ar_allreduce_n(h, _ptr_array(ins), _ptr_array(outs), n, algo, proto,
+                                         _stream(stream)), "ar_allreduce_n")
+
+
+def ar_tune(h: int, stream=None) -> None:
+    _check(load_library().ar_tune(h, _stream(stream)), "ar_tune")
+
+
+def ar_get_tuning(h: int, nbytes: int):
+    """(algo, proto, [µs one-shot LL, one-shot HB, two-shot LL, two-shot HB])."""
+    a, p = ctypes.c_int(), ctypes.c_int()
+    us = (ctypes.c_float * 4)()
+    _check(load_library().ar_get_tuning(h, nbytes, ctypes.byref(a), ctypes.byref(p), us),
+           "ar_get_tuning")
+    return a.value, p.value, list(us)
 
 
 def ar_reduce_scatter(h: int, ins, outs, stream=None) -> None:

@@ -11,6 +11,14 @@
 
 using namespace ar;
 
+// AUTO lookup: messages are bucketed by bytes per rank, rounded up to a power
+// of two and clamped to [512 B, 256 MiB] (SGLang guide, section 4.4).
+constexpr int kMinBucketLog2 = 9;
+constexpr int kMaxBucketLog2 = 28;
+constexpr int kBuckets = kMaxBucketLog2 - kMinBucketLog2 + 1;
+// ar_tune times 15 sizes, 2^9 .. 2^23 bytes per rank (the page's [2^9, 2^24)).
+constexpr int kTuneMaxLog2 = 23;
+
 struct ar_handle {
     int R;
     size_t N;
@@ -30,6 +38,10 @@ struct ar_handle {
     int reg_cap;            // CTAs of the 256-thread kernels per launch
     int tma_tile;
     int tma_stages;
+    // AUTO choice per message-size bucket (bucket b: messages of at most
+    // 2^(9+b) bytes per rank), timed by ar_tune; us[algo][proto], 0 = untimed
+    float tuned_us[kBuckets][2][2];
+    int tuned_max;          // largest tuned bucket, -1 before ar_tune
     int pdl;                // launch with programmatic dependent launch
     int ll_transport;       // enum ar_ll_transport
     bool cluster_ok;        // the cluster LL kernel can run for this R
@@ -63,14 +75,14 @@ bool ranges_overlap(uintptr_t a, uintptr_t b, size_t len) { return a < b + len &
 // Checks shared by the calls that take R output pointers and, optionally, R
 // input pointers.  Sets *vec16 / *vec8 (all pointers 16- / 8-byte aligned)
 // and *inplace (some in[r] == out[r]).
-int check_buffers(const ar_handle *h, const void *const in[], void *const out[], bool *vec16,
-                  bool *vec8, bool *inplace) {
+int check_buffers(const ar_handle *h, const void *const in[], void *const out[], uint64_t n,
+                  bool *vec16, bool *vec8, bool *inplace) {
     if (!h || !out)
         return AR_ERR_INVALID;
     if (!on_device(h))
         return AR_ERR_INVALID;
     const int R = h->R;
-    const size_t len = h->N * h->esz;
+    const size_t len = n * h->esz;
     uintptr_t all = 0;
     for (int r = 0; r < R; ++r) {
         if (!out[r] || (in && !in[r]))
@@ -111,13 +123,30 @@ void fill_ptrs(const ar_handle *h, const void *const in[], void *const out[], Ra
     }
 }
 
-HbArgs hb_args(const ar_handle *h, const void *const in[], void *const out[], bool inplace) {
+// One call: its buffers, its message length n (<= the handle's N) and what
+// the checks found.
+struct Call {
+    const void *const *in;
+    void *const *out;
+    uint64_t n;
+    uint64_t shard;         // two-shot shard of n elements
+    bool vec16, vec8, inplace;
+    cudaStream_t s;
+};
+
+// ceil(n / R) rounded up to a whole 16-byte vector
+uint64_t shard_of(uint64_t n, int R, size_t esz) {
+    const uint64_t per_vec = 16 / esz;
+    return ceil_div(ceil_div(n, (uint64_t)R), per_vec) * per_vec;
+}
+
+HbArgs hb_args(const ar_handle *h, const Call &c) {
     HbArgs a;
-    fill_ptrs(h, in, out, &a.p);
-    a.n = h->N;
-    a.shard = h->shard;
+    fill_ptrs(h, c.in, c.out, &a.p);
+    a.n = c.n;
+    a.shard = c.shard;
     a.R = h->R;
-    a.inplace = inplace ? 1 : 0;
+    a.inplace = c.inplace ? 1 : 0;
     return a;
 }
 
@@ -130,25 +159,23 @@ int from_cuda(cudaError_t e) {
 
 // ---- the four all-reduce paths ---------------------------------------------
 
-int one_shot_hb(ar_handle *h, const void *const in[], void *const out[], bool vec, bool inplace,
-                cudaStream_t s) {
-    const HbArgs a = hb_args(h, in, out, inplace);
-    const uint64_t per_vec = 16 / h->esz;
-    const uint64_t units = vec ? h->N / per_vec : h->N;
+int one_shot_hb(ar_handle *h, const Call &c) {
+    const HbArgs a = hb_args(h, c);
+    const uint64_t units = c.vec16 ? c.n / (16 / h->esz) : c.n;
     const uint64_t per_blk = (uint64_t)(h->one_shot_warps / h->R) * 32;
     const int grid = clamp_grid(ceil_div(units, per_blk), h->one_shot_cap);
-    return from_cuda(launch_one_shot_hb(a, h->dtype, vec, grid, 32 * h->one_shot_warps, s, h->pdl));
+    return from_cuda(
+        launch_one_shot_hb(a, h->dtype, c.vec16, grid, 32 * h->one_shot_warps, c.s, h->pdl));
 }
 
-int two_shot_hb(ar_handle *h, const void *const in[], void *const out[], bool vec, bool inplace,
-                cudaStream_t s) {
-    const uint64_t body = (h->N * h->esz) / 16 * 16;
-    if (vec && body > 0) {
+int two_shot_hb(ar_handle *h, const Call &c) {
+    const uint64_t body = (c.n * h->esz) / 16 * 16;
+    if (c.vec16 && body > 0) {
         TmaArgs a;
-        fill_ptrs(h, in, out, &a.p);
-        a.n = h->N;
+        fill_ptrs(h, c.in, c.out, &a.p);
+        a.n = c.n;
         a.body_bytes = body;
-        a.shard_bytes = h->shard * h->esz;
+        a.shard_bytes = c.shard * h->esz;
         a.tiles_per_shard = ceil_div(a.shard_bytes, (uint64_t)h->tma_tile);
         a.R = h->R;
         a.tile_bytes = h->tma_tile;
@@ -156,62 +183,111 @@ int two_shot_hb(ar_handle *h, const void *const in[], void *const out[], bool ve
         a.c = h->ctl;
         const uint64_t items = ceil_div(body, (uint64_t)h->tma_tile) + (uint64_t)h->R;
         const int grid = clamp_grid(items, h->num_sms);
-        return from_cuda(launch_two_shot_tma(a, h->dtype, grid, s, h->pdl));
+        return from_cuda(launch_two_shot_tma(a, h->dtype, grid, c.s, h->pdl));
     }
     // unaligned buffers: one thread per element reduces once, stores R times
-    const HbArgs a = hb_args(h, in, out, inplace);
-    const uint64_t units = vec ? h->N / (16 / h->esz) : h->N;
+    const HbArgs a = hb_args(h, c);
+    const uint64_t units = c.vec16 ? c.n / (16 / h->esz) : c.n;
     const int grid = clamp_grid(ceil_div(units, kRegThreads), h->reg_cap);
-    return from_cuda(launch_reduce(a, h->dtype, vec, false, grid, s, h->pdl));
+    return from_cuda(launch_reduce(a, h->dtype, c.vec16, false, grid, c.s, h->pdl));
 }
 
 // One-shot LL through thread-block clusters (R peers per cluster exchange
 // packets in distributed shared memory).
-int ll_cluster(ar_handle *h, const void *const in[], void *const out[], cudaStream_t s) {
+int ll_cluster(ar_handle *h, const Call &c) {
     LlClusterArgs a;
-    fill_ptrs(h, in, out, &a.p);
-    a.n = h->N;
+    fill_ptrs(h, c.in, c.out, &a.p);
+    a.n = c.n;
     a.R = h->R;
     a.c = h->ctl;
-    const uint64_t U = h->N * h->esz / 16;
+    const uint64_t U = c.n * h->esz / 16;
     a.units_per_chunk = U < h->cluster_uc ? (U > 0 ? U : 1) : h->cluster_uc;
     const uint64_t nchunks = U > 0 ? ceil_div(U, a.units_per_chunk) : 1;
     int cap = h->cluster_max;
     if (cap > kEpochWords / h->R)
         cap = kEpochWords / h->R;
-    return from_cuda(launch_ll_cluster(a, h->dtype, clamp_grid(nchunks, cap), s, h->pdl));
+    return from_cuda(launch_ll_cluster(a, h->dtype, clamp_grid(nchunks, cap), c.s, h->pdl));
 }
 
-bool use_cluster(const ar_handle *h, bool vec16, bool two) {
-    return !two && vec16 && h->cluster_ok && h->ll_transport == AR_LL_CLUSTER;
-}
-
-// vec: every buffer 8-byte aligned (global-memory kernel's vector path);
-// vec16: 16-byte aligned (needed by the cluster kernel).
-int ll(ar_handle *h, const void *const in[], void *const out[], bool vec, bool vec16, bool two,
-       cudaStream_t s) {
+// LL: the global-memory kernel's vector path needs 8-byte alignment, the
+// cluster kernel 16-byte alignment.
+int ll(ar_handle *h, const Call &c, bool two) {
     if (!h->slots)
         return AR_ERR_UNSUPPORTED;
-    if (use_cluster(h, vec16, two))
-        return ll_cluster(h, in, out, s);
+    if (!two && c.vec16 && h->cluster_ok && h->ll_transport == AR_LL_CLUSTER)
+        return ll_cluster(h, c);
     LlArgs a;
-    fill_ptrs(h, in, out, &a.p);
-    a.n = h->N;
-    a.shard = h->shard;
+    fill_ptrs(h, c.in, c.out, &a.p);
+    a.n = c.n;
+    a.shard = c.shard;
     a.slots = h->slots;
     a.ppad = h->ppad;
     a.R = h->R;
     a.c = h->ctl;
-    const uint64_t nbytes = h->N * h->esz;
-    const uint64_t work = vec ? nbytes / 8 + 1 : (nbytes + 3) / 4;   // units per rank
-    const int cap = h->ll_cap[vec ? 1 : 0][two ? 1 : 0];
+    const uint64_t nbytes = c.n * h->esz;
+    const uint64_t work = c.vec8 ? nbytes / 8 + 1 : (nbytes + 3) / 4;   // units per rank
+    const int cap = h->ll_cap[c.vec8 ? 1 : 0][two ? 1 : 0];
     int gmax = cap / h->R;
     if (gmax > kEpochWords / h->R)
         gmax = kEpochWords / h->R;
     if (gmax < 1)
         return AR_ERR_UNSUPPORTED;                 // cannot keep R CTAs resident
     a.G = clamp_grid(ceil_div(work, kLlThreads), gmax);
-    return from_cuda(launch_ll(a, h->dtype, vec, two, s, h->pdl));
+    return from_cuda(launch_ll(a, h->dtype, c.vec8, two, c.s, h->pdl));
+}
+
+int run_path(ar_handle *h, const Call &c, int algo, int proto) {
+    if (proto == AR_HB)
+        return algo == AR_ONE_SHOT ? one_shot_hb(h, c) : two_shot_hb(h, c);
+    return ll(h, c, algo == AR_TWO_SHOT);
+}
+
+// ---- AUTO -------------------------------------------------------------------
+
+int bucket_of(uint64_t bytes) {
+    int b = kMinBucketLog2;
+    while (b < kMaxBucketLog2 && ((uint64_t)1 << b) < bytes)
+        ++b;
+    return b - kMinBucketLog2;
+}
+
+// Resolve AR_ALGO_AUTO / AR_PROTO_AUTO for a message of `bytes` per rank:
+// the fastest tuned (algo, proto) allowed by the fixed half of the request,
+// or, before ar_tune, a fixed rule from GB300 measurements (one-shot HB up to
+// 256 KiB per rank, two-shot HB above; with LL forced, one-shot up to 2 MiB).
+void resolve(const ar_handle *h, uint64_t bytes, int *algo, int *proto) {
+    const bool ll_ok = h->slots != nullptr;
+    if (h->tuned_max >= 0) {
+        int b = bucket_of(bytes);
+        if (b > h->tuned_max)
+            b = h->tuned_max;
+        float best = 0.f;
+        int ba = -1, bp = -1;
+        for (int a = 0; a < 2; ++a)
+            for (int p = 0; p < 2; ++p) {
+                if ((*algo != AR_ALGO_AUTO && *algo != a) || (*proto != AR_PROTO_AUTO && *proto != p))
+                    continue;
+                if (p == AR_LL && !ll_ok)
+                    continue;
+                const float us = h->tuned_us[b][a][p];
+                if (us > 0.f && (ba < 0 || us < best)) {
+                    best = us;
+                    ba = a;
+                    bp = p;
+                }
+            }
+        if (ba >= 0) {
+            *algo = ba;
+            *proto = bp;
+            return;
+        }
+    }
+    if (*proto == AR_PROTO_AUTO)
+        *proto = AR_HB;
+    if (*algo == AR_ALGO_AUTO) {
+        const uint64_t limit = *proto == AR_LL ? (2u << 20) : (256u << 10);
+        *algo = bytes <= limit ? AR_ONE_SHOT : AR_TWO_SHOT;
+    }
 }
 
 }  // namespace
@@ -317,6 +393,11 @@ int ar_create(int R, size_t N, int dtype, ar_handle_t *out) {
 
     // cluster LL: one CTA per virtual rank in a cluster (portable up to 8,
     // 16 with the non-portable size); receive buffers of ~64 KiB per CTA
+    h->tuned_max = -1;
+    for (int b = 0; b < kBuckets; ++b)
+        for (int a = 0; a < 2; ++a)
+            for (int p = 0; p < 2; ++p)
+                h->tuned_us[b][a][p] = 0.f;
     h->pdl = 1;
     h->ll_transport = AR_LL_AUTO;
     h->cluster_ok = false;
@@ -358,47 +439,196 @@ int ar_destroy(ar_handle_t h) {
     return rc;
 }
 
-int ar_allreduce(ar_handle_t h, const void *const in[], void *const out[], int algo, int proto,
-                 cudaStream_t stream) {
-    if (!in)
+int ar_allreduce_n(ar_handle_t h, const void *const in[], void *const out[], size_t n, int algo,
+                   int proto, cudaStream_t stream) {
+    if (!in || !h || n < 1 || n > h->N)
         return AR_ERR_INVALID;
-    bool vec16, vec8, inplace;
-    const int rc = check_buffers(h, in, out, &vec16, &vec8, &inplace);
+    if (algo != AR_ONE_SHOT && algo != AR_TWO_SHOT && algo != AR_ALGO_AUTO)
+        return AR_ERR_INVALID;
+    if (proto != AR_LL && proto != AR_HB && proto != AR_PROTO_AUTO)
+        return AR_ERR_INVALID;
+    Call c;
+    const int rc = check_buffers(h, in, out, n, &c.vec16, &c.vec8, &c.inplace);
     if (rc != AR_OK)
         return rc;
-    if (algo != AR_ONE_SHOT && algo != AR_TWO_SHOT)
+    c.in = in;
+    c.out = out;
+    c.n = n;
+    c.shard = shard_of(n, h->R, h->esz);
+    c.s = stream;
+    if (algo == AR_ALGO_AUTO || proto == AR_PROTO_AUTO)
+        resolve(h, n * h->esz, &algo, &proto);
+    return run_path(h, c, algo, proto);
+}
+
+int ar_allreduce(ar_handle_t h, const void *const in[], void *const out[], int algo, int proto,
+                 cudaStream_t stream) {
+    if (!h)
         return AR_ERR_INVALID;
-    if (proto == AR_HB)
-        return algo == AR_ONE_SHOT ? one_shot_hb(h, in, out, vec16, inplace, stream)
-                                   : two_shot_hb(h, in, out, vec16, inplace, stream);
-    if (proto == AR_LL)
-        return ll(h, in, out, vec8, vec16, algo == AR_TWO_SHOT, stream);
-    return AR_ERR_INVALID;
+    return ar_allreduce_n(h, in, out, h->N, algo, proto, stream);
 }
 
 int ar_reduce_scatter(ar_handle_t h, const void *const in[], void *const out[],
                       cudaStream_t stream) {
-    if (!in)
+    if (!in || !h)
         return AR_ERR_INVALID;
-    bool vec16, vec8, inplace;
-    const int rc = check_buffers(h, in, out, &vec16, &vec8, &inplace);
+    Call c;
+    const int rc = check_buffers(h, in, out, h->N, &c.vec16, &c.vec8, &c.inplace);
     if (rc != AR_OK)
         return rc;
-    const HbArgs a = hb_args(h, in, out, inplace);
-    const uint64_t units = vec16 ? h->N / (16 / h->esz) : h->N;
+    c.in = in;
+    c.out = out;
+    c.n = h->N;
+    c.shard = h->shard;
+    c.s = stream;
+    const HbArgs a = hb_args(h, c);
+    const uint64_t units = c.vec16 ? h->N / (16 / h->esz) : h->N;
     const int grid = clamp_grid(ceil_div(units, kRegThreads), h->reg_cap);
-    return from_cuda(launch_reduce(a, h->dtype, vec16, true, grid, stream, h->pdl));
+    return from_cuda(launch_reduce(a, h->dtype, c.vec16, true, grid, stream, h->pdl));
 }
 
 int ar_all_gather(ar_handle_t h, void *const out[], cudaStream_t stream) {
-    bool vec16, vec8, inplace;
-    const int rc = check_buffers(h, nullptr, out, &vec16, &vec8, &inplace);
+    if (!h)
+        return AR_ERR_INVALID;
+    Call c;
+    const int rc = check_buffers(h, nullptr, out, h->N, &c.vec16, &c.vec8, &c.inplace);
     if (rc != AR_OK)
         return rc;
-    const HbArgs a = hb_args(h, nullptr, out, false);
-    const uint64_t units = vec16 ? h->N / (16 / h->esz) : h->N;
+    c.in = nullptr;
+    c.out = out;
+    c.n = h->N;
+    c.shard = h->shard;
+    c.s = stream;
+    const HbArgs a = hb_args(h, c);
+    const uint64_t units = c.vec16 ? h->N / (16 / h->esz) : h->N;
     const int grid = clamp_grid(ceil_div(units, kRegThreads), h->reg_cap);
-    return from_cuda(launch_all_gather(a, h->dtype, vec16, grid, stream, h->pdl));
+    return from_cuda(launch_all_gather(a, h->dtype, c.vec16, grid, stream, h->pdl));
+}
+
+int ar_tune(ar_handle_t h, cudaStream_t stream) {
+    if (!h || !on_device(h))
+        return AR_ERR_INVALID;
+    const size_t esz = h->esz;
+    uint64_t max_bytes = (uint64_t)1 << kTuneMaxLog2;
+    if (max_bytes > h->N * esz)
+        max_bytes = h->N * esz;
+    const uint64_t nmax = max_bytes / esz > 0 ? max_bytes / esz : 1;
+    const size_t buf_bytes = (nmax * esz + 255) / 256 * 256;
+    void *mem = nullptr;
+    if (cudaStreamSynchronize(stream) != cudaSuccess)
+        return from_cuda(cudaErrorUnknown);
+    if (cudaMalloc(&mem, buf_bytes * 2 * h->R) != cudaSuccess) {
+        (void)cudaGetLastError();
+        return AR_ERR_NOMEM;
+    }
+    const void *ins[AR_MAX_RANKS];
+    void *outs[AR_MAX_RANKS];
+    for (int r = 0; r < h->R; ++r) {
+        ins[r] = static_cast<uint8_t *>(mem) + buf_bytes * r;
+        outs[r] = static_cast<uint8_t *>(mem) + buf_bytes * (h->R + r);
+    }
+    cudaStream_t ts = nullptr;
+    cudaEvent_t e0 = nullptr, e1 = nullptr;
+    int rc = AR_OK;
+    if (cudaMemset(mem, 0, buf_bytes * 2 * h->R) != cudaSuccess ||
+        cudaStreamCreateWithFlags(&ts, cudaStreamNonBlocking) != cudaSuccess ||
+        cudaEventCreate(&e0) != cudaSuccess || cudaEventCreate(&e1) != cudaSuccess)
+        rc = AR_ERR_CUDA;
+    int last = -1;
+    // every power of two from 512 B to max_bytes per rank (at least one size)
+    for (int lg = kMinBucketLog2; rc == AR_OK && lg <= kTuneMaxLog2; ++lg) {
+        const uint64_t bytes = (uint64_t)1 << lg;
+        if (bytes > max_bytes && lg > kMinBucketLog2)
+            break;
+        const uint64_t n = bytes <= max_bytes ? bytes / esz : nmax;
+        const int b = lg - kMinBucketLog2;
+        Call c;
+        c.in = ins;
+        c.out = outs;
+        c.n = n > 0 ? n : 1;
+        c.shard = shard_of(c.n, h->R, esz);
+        c.vec16 = c.vec8 = true;
+        c.inplace = false;
+        c.s = ts;
+        for (int a = 0; a < 2 && rc == AR_OK; ++a)
+            for (int p = 0; p < 2 && rc == AR_OK; ++p) {
+                h->tuned_us[b][a][p] = 0.f;
+                if (p == AR_LL && !h->slots)
+                    continue;
+                // 10 calls per graph, 5 warm-up replays, 20 timed replays
+                cudaGraph_t g = nullptr;
+                cudaGraphExec_t ge = nullptr;
+                if (run_path(h, c, a, p) != AR_OK ||
+                    cudaStreamBeginCapture(ts, cudaStreamCaptureModeThreadLocal) != cudaSuccess) {
+                    rc = AR_ERR_CUDA;
+                    break;
+                }
+                int crc = AR_OK;
+                for (int k = 0; k < 10 && crc == AR_OK; ++k)
+                    crc = run_path(h, c, a, p);
+                if (cudaStreamEndCapture(ts, &g) != cudaSuccess || crc != AR_OK ||
+                    cudaGraphInstantiate(&ge, g, 0) != cudaSuccess) {
+                    if (g)
+                        cudaGraphDestroy(g);
+                    rc = AR_ERR_CUDA;
+                    break;
+                }
+                float ms = 0.f;
+                bool okc = true;
+                for (int k = 0; k < 5 && okc; ++k)
+                    okc = cudaGraphLaunch(ge, ts) == cudaSuccess;
+                okc = okc && cudaEventRecord(e0, ts) == cudaSuccess;
+                for (int k = 0; k < 20 && okc; ++k)
+                    okc = cudaGraphLaunch(ge, ts) == cudaSuccess;
+                okc = okc && cudaEventRecord(e1, ts) == cudaSuccess &&
+                      cudaEventSynchronize(e1) == cudaSuccess &&
+                      cudaEventElapsedTime(&ms, e0, e1) == cudaSuccess;
+                cudaGraphExecDestroy(ge);
+                cudaGraphDestroy(g);
+                if (!okc) {
+                    rc = AR_ERR_CUDA;
+                    break;
+                }
+                h->tuned_us[b][a][p] = ms * 1000.f / 200.f;
+            }
+        if (rc == AR_OK)
+            last = b;
+    }
+    if (ts) {
+        cudaStreamSynchronize(ts);
+        cudaStreamDestroy(ts);
+    }
+    if (e0)
+        cudaEventDestroy(e0);
+    if (e1)
+        cudaEventDestroy(e1);
+    cudaFree(mem);
+    if (rc != AR_OK) {
+        (void)cudaGetLastError();
+        h->tuned_max = -1;
+        return rc;
+    }
+    h->tuned_max = last;
+    // a timed-out wait during tuning would show in the status word
+    const int st = ar_status(h, stream);
+    return st;
+}
+
+int ar_get_tuning(ar_handle_t h, size_t bytes, int *algo, int *proto, float us[4]) {
+    if (!h || !algo || !proto)
+        return AR_ERR_INVALID;
+    int a = AR_ALGO_AUTO, p = AR_PROTO_AUTO;
+    resolve(h, bytes, &a, &p);
+    *algo = a;
+    *proto = p;
+    if (us) {
+        int b = bucket_of(bytes);
+        if (h->tuned_max >= 0 && b > h->tuned_max)
+            b = h->tuned_max;
+        for (int k = 0; k < 4; ++k)
+            us[k] = h->tuned_max >= 0 ? h->tuned_us[b][k / 2][k % 2] : 0.f;
+    }
+    return AR_OK;
 }
 
 int ar_ll_pack(ar_handle_t h, const void *src, uint64_t *pkts, size_t n, uint32_t flag,

@@ -562,8 +562,8 @@ def main():
     p.add_argument("--R", type=int, default=8)
     p.add_argument("--n", type=int, default=1 << 18)
     p.add_argument("--dtype", default="bf16", choices=["bf16", "fp16", "fp32"])
-    p.add_argument("--algo", default="one_shot", choices=["one_shot", "two_shot"])
-    p.add_argument("--proto", default="ll", choices=["ll", "hb"])
+    p.add_argument("--algo", default="one_shot", choices=["one_shot", "two_shot", "auto"])
+    p.add_argument("--proto", default="ll", choices=["ll", "hb", "auto"])
     p.add_argument("--calls", type=int, default=10)
     p.add_argument("--ll-transport", default="auto", choices=["auto", "global", "cluster"])
     p.add_argument("--no-pdl", action="store_true",

@@ -86,7 +86,8 @@ enum ar_dtype {
  *                j, then the reduced shard is copied to every output. */
 enum ar_algo {
     AR_ONE_SHOT = 0,
-    AR_TWO_SHOT = 1
+    AR_TWO_SHOT = 1,
+    AR_ALGO_AUTO = 2           /* chosen per message size, see ar_tune */
 };
 
 /* Protocols (MSCCL++ summary, section "MemoryChannel", protocol table).
@@ -101,7 +102,8 @@ enum ar_algo {
  *          multicast) when every buffer is 16-byte aligned. */
 enum ar_proto {
     AR_LL = 0,
-    AR_HB = 1
+    AR_HB = 1,
+    AR_PROTO_AUTO = 2          /* chosen per message size, see ar_tune */
 };
 
 /* How one-shot LL packets travel between virtual peers.
@@ -189,6 +191,35 @@ int ar_destroy(ar_handle_t h);
  * errors (AR_ERR_TIMEOUT) are reported by ar_status. */
 int ar_allreduce(ar_handle_t h, const void *const in[], void *const out[],
                  int algo, int proto, cudaStream_t stream);
+
+/* ar_allreduce on the first n elements of every buffer, 1 <= n <= N (the
+ * handle's N is the largest message it serves; n has its own shards, S =
+ * ceil(n/R) rounded up to a 16-byte vector).  Buffers need n elements.
+ * With AR_ALGO_AUTO and/or AR_PROTO_AUTO the library picks the half left
+ * open, per message size: the tuned fastest choice after ar_tune, else a
+ * fixed rule from GB300 measurements (HB; one-shot up to 256 KiB per rank,
+ * two-shot above; with AR_LL forced, one-shot up to 2 MiB).
+ * Errors: as ar_allreduce; AR_ERR_INVALID also for n == 0 or n > N. */
+int ar_allreduce_n(ar_handle_t h, const void *const in[], void *const out[], size_t n,
+                   int algo, int proto, cudaStream_t stream);
+
+/* Autotune AUTO for this handle (SGLang guide, section 4.4: every
+ * (algorithm, configuration) is timed inside a CUDA graph at 15
+ * power-of-two message sizes in [2^9, 2^24) bytes, and later calls map their
+ * size, rounded up to a power of two and clamped to [512 B, 256 MiB], to the
+ * fastest).  Here: each (algo, proto) pair is timed at every power of two
+ * from 512 B to min(8 MiB, N * elem_size) bytes per rank as a graph of 10
+ * calls, 5 warm-up replays then 20 timed replays; sizes above the largest
+ * tuned one use its choice.  Not a hot-path call: it waits for `stream`,
+ * allocates and frees 2 * R temporary buffers, creates a private stream and
+ * synchronises.  Returns AR_OK or the first error (including a device-side
+ * one, as ar_status would). */
+int ar_tune(ar_handle_t h, cudaStream_t stream);
+
+/* The AUTO choice for a message of `bytes` per rank (*algo, *proto) and,
+ * if `us` is not NULL, the tuned µs per call of the four pairs in the order
+ * one-shot LL, one-shot HB, two-shot LL, two-shot HB (0 = not timed). */
+int ar_get_tuning(ar_handle_t h, size_t bytes, int *algo, int *proto, float us[4]);
 
 /* Reduce-scatter step of the two-shot schedule (HB): for every shard j,
  *   out[j][i] = round_dtype(fold of in[0..R-1][i])  for i in shard j,
