@@ -60,9 +60,9 @@ def workload_cases(name: str, args=None):
         desc = ("r8_bf16_ll_sweep: R=8 virtual ranks, bf16, N=2^9..2^18 elements per rank "
                 "(1 KiB..512 KiB), uniform[-1,1), one-shot LL, 10 calls per CUDA graph")
     elif name == "decode":
-        cases = [dict(w=w, algo="one_shot", proto="hb", calls=10, flush=True) for w in wl.DECODE]
+        cases = [dict(w=w, algo="auto", proto="auto", calls=10, flush=True) for w in wl.DECODE]
         desc = ("r8_bf16_decode: R=8, bf16 [B, 8192] for B in 1,8,32,128,256, N(0,1), "
-                "one-shot HB, 10 calls per CUDA graph")
+                "AUTO (tuned) schedule and protocol, 10 calls per CUDA graph")
     elif name == "prefill":
         cases = [dict(w=wl.PREFILL, algo="two_shot", proto="hb", calls=1, flush=False)]
         desc = ("r16_bf16_prefill: R=16, bf16 [8192, 8192] per rank (128 MiB), N(0,1), "
@@ -249,6 +249,11 @@ class CaseRunner:
         ar.ar_set_ll_transport(self.h.h, c.get("transport", ar.AR_LL_AUTO))
         ar.ar_set_pdl(self.h.h, c.get("pdl", 1))
         self.algo, self.proto = ar.ALGOS[c["algo"]], ar.PROTOS[c["proto"]]
+        self.choice = None
+        if c["algo"] == "auto" or c["proto"] == "auto":
+            ar.ar_tune(self.h.h, stream)
+            a, p, _ = ar.ar_get_tuning(self.h.h, w.n * wl.ELEM_SIZE[w.dtype])
+            self.choice = "%s_%s" % ({0: "one_shot", 1: "two_shot"}[a], {0: "ll", 1: "hb"}[p])
         self.bytes = case_bytes(c)
         with torch.cuda.stream(stream):
             ar.ar_allreduce(self.h.h, self.ins, self.outs, self.algo, self.proto, stream=stream)
@@ -367,6 +372,8 @@ def run_ours(args, dist: Dist):
             "frac_of_hbm_peak": round(r.bytes / us / 1e3 / peak, 4),
             "l2_resident": 2 * r.bytes <= 100 << 20,
         }
+        if r.choice:
+            sweep[str(r.w.n)]["auto_choice"] = r.choice
 
     # end to end: pinned host inputs -> device, the same graph, outputs -> host
     e2e_steps = max(3, min(args.steps, 50))
@@ -393,7 +400,7 @@ def run_ours(args, dist: Dist):
     e2e_value = dist.sum(bytes_step) / (e2e_ms * 1e-3) / 1e9
 
     variants = None
-    if args.workload == "sweep" and not args.no_variants:
+    if args.workload in ("sweep", "decode") and not args.no_variants:
         variants = measure_variants(runners, stream, flush, max(20, args.steps // 10))
 
     cpu = None
@@ -440,9 +447,12 @@ def measure_variants(runners, stream, flush, K):
     out = {}
     for algo, proto, tr in (("one_shot", "hb", ar.AR_LL_AUTO), ("two_shot", "hb", ar.AR_LL_AUTO),
                             ("two_shot", "ll", ar.AR_LL_AUTO),
-                            ("one_shot", "ll", ar.AR_LL_GLOBAL), ("one_shot", "ll", ar.AR_LL_CLUSTER)):
+                            ("one_shot", "ll", ar.AR_LL_GLOBAL), ("one_shot", "ll", ar.AR_LL_CLUSTER),
+                            ("auto", "auto", ar.AR_LL_AUTO)):
         row = {}
         for r in runners:
+            if algo == "auto" and r.choice is None:
+                ar.ar_tune(r.h.h, stream)
             ar.ar_set_ll_transport(r.h.h, tr)
             g = torch.cuda.CUDAGraph()
             with torch.cuda.graph(g, stream=stream):
@@ -464,7 +474,7 @@ def measure_variants(runners, stream, flush, K):
                 tot += e0.elapsed_time(e1)
             row[str(r.w.n)] = round(tot * 1e3 / (K * r.c["calls"]), 3)
             ar.ar_set_ll_transport(r.h.h, r.c.get("transport", ar.AR_LL_AUTO))
-        key = "%s_%s" % (algo, proto)
+        key = "%s_%s" % (algo, proto) if algo != "auto" else "auto_tuned"
         if proto == "ll" and algo == "one_shot":
             key += "_" + {ar.AR_LL_GLOBAL: "global", ar.AR_LL_CLUSTER: "cluster"}[tr]
         out[key] = row
