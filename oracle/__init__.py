@@ -73,6 +73,9 @@ def _bind(lib: ctypes.CDLL) -> ctypes.CDLL:
     lib.oracle_ll_packets.argtypes, lib.oracle_ll_packets.restype = [i32, sz], sz
     lib.oracle_ll_pack.argtypes, lib.oracle_ll_pack.restype = [i32, vp, sz, u32, vp], i32
     lib.oracle_ll_unpack.argtypes, lib.oracle_ll_unpack.restype = [i32, vp, sz, u32, vp], sz
+    ip = ctypes.POINTER(ctypes.c_int)
+    lib.oracle_plan_run.argtypes = [i32, sz, i32, i32, i32, ip, ip, ip, ip, ip, ip, vpp, vpp]
+    lib.oracle_plan_run.restype = i32
     lib.oracle_round_f32.argtypes, lib.oracle_round_f32.restype = [i32, vp, sz, vp], None
     lib.oracle_widen.argtypes, lib.oracle_widen.restype = [i32, vp, sz, vp], None
     return lib
@@ -156,3 +159,25 @@ def widen(bits: np.ndarray, dtype: int, lib=None) -> np.ndarray:
     out = np.empty(bits.size, dtype=np.float32)
     lib.oracle_widen(dtype, _ptr(bits), bits.size, _ptr(out))
     return out
+
+
+def plan_run(steps, ins, outs, dtype: int, nchunks: int, lib=None):
+    """Run a plan sequentially (see oracle_plan_run).  `steps` is a list of
+    dicts with keys kind ('copy'|'reduce'), dst, srcs (buffer ids: b < R is
+    in[b], R <= b < 2R is out[b - R]), cbeg, cend.  Modifies ins/outs in
+    place and returns outs."""
+    lib = lib or load()
+    R = len(ins)
+    n = len(steps)
+    arr = lambda vals: (ctypes.c_int * max(1, len(vals)))(*vals)
+    src = []
+    for st in steps:
+        src += list(st["srcs"]) + [0] * (32 - len(st["srcs"]))
+    rc = lib.oracle_plan_run(
+        R, ins[0].size, dtype, nchunks, n,
+        arr([0 if st["kind"] == "copy" else 1 for st in steps]), arr([st["dst"] for st in steps]),
+        arr([len(st["srcs"]) for st in steps]), arr(src), arr([st["cbeg"] for st in steps]),
+        arr([st["cend"] for st in steps]), _ptr_array(ins), _ptr_array(outs))
+    if rc != 0:
+        raise ValueError("oracle_plan_run rejected the plan")
+    return outs

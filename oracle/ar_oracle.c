@@ -236,8 +236,10 @@ static void store_narrowed(int dtype, void *buf, size_t i, float y)
  * The all-reduce.
  * ------------------------------------------------------------------------- */
 
-/* One element of the sum: widen, fold ranks 0..R-1 left to right in binary32
- * starting from rank 0's value, round once to the dtype (returned widened). */
+/* One element of the sum: widen, fold buffers 0..R-1 left to right in
+ * binary32 starting from buffer 0's value (the caller rounds once to the
+ * dtype).  Used by the all-reduce (the R ranks' inputs) and by plan reduce
+ * steps (the step's sources in their listed order). */
 static float fold_element(int R, int dtype, const void *const *in, size_t i)
 {
     float acc = load_widened(dtype, in[0], i);
@@ -301,6 +303,74 @@ int oracle_reduce_scatter(int R, size_t N, int dtype, const void *const *in, voi
         oracle_shard_bounds(R, N, dtype, j, &lo, &hi);
         for (i = lo; i < hi; ++i)
             store_narrowed(dtype, out[j], i, fold_element(R, dtype, in, i));
+    }
+    return 0;
+}
+
+/* ---------------------------------------------------------------------------
+ * Plans: sequences of reduce / copy steps over chunks of the rank buffers.
+ *
+ * "【论文分享】MSCCL++：让 GPU 通信像 CUDA 一样可编程", section
+ * "第二层：DSL API": an algorithm is written as channel put / wait / reduce
+ * steps; the compiler finds the data dependencies and inserts the
+ * synchronisation, and the runtime interprets the plan.  The meaning of a
+ * plan is therefore its steps executed one after another in the order
+ * written; that sequential execution is what this function does (a
+ * correctly synchronised parallel execution must give the same bits).
+ *
+ * A plan cuts every buffer into `nchunks` chunks: chunk c holds elements
+ * [c*C, min((c+1)*C, N)), C = ceil(N / nchunks) rounded up to a whole
+ * 16-byte vector.  Step k is described by the integers
+ *   kind[k]   0 = copy, 1 = reduce
+ *   dst[k]    buffer id of the destination
+ *   nsrc[k]   number of sources (1 for a copy)
+ *   src[k*32 + i], i < nsrc[k]: buffer ids of the sources, folded in order
+ *   cbeg[k], cend[k]: the chunk range [cbeg, cend)
+ * where buffer id b < R names in[b] and R <= b < 2R names out[b - R].
+ * A reduce widens every source element to binary32, folds them left to
+ * right, and rounds once to the dtype (the all-reduce fold above); a copy
+ * moves the bits.  Returns 0, or -1 on a bad step.
+ * ------------------------------------------------------------------------- */
+int oracle_plan_run(int R, size_t N, int dtype, int nchunks, int nsteps, const int *kind,
+                    const int *dst, const int *nsrc, const int *src, const int *cbeg,
+                    const int *cend, void *const *in, void *const *out)
+{
+    size_t per_vec, C;
+    int k;
+    if (R < 1 || nchunks < 1 || oracle_elem_size(dtype) == 0)
+        return -1;
+    per_vec = 16 / oracle_elem_size(dtype);
+    C = (N + (size_t)nchunks - 1) / (size_t)nchunks;
+    C = (C + per_vec - 1) / per_vec * per_vec;
+    for (k = 0; k < nsteps; ++k) {
+        void *d;
+        const void *srcs[32];
+        int i, c;
+        if (dst[k] < 0 || dst[k] >= 2 * R || nsrc[k] < 1 || nsrc[k] > 32 ||
+            (kind[k] == 0 && nsrc[k] != 1) || cbeg[k] < 0 || cend[k] > nchunks)
+            return -1;
+        d = dst[k] < R ? (void *)in[dst[k]] : out[dst[k] - R];
+        for (i = 0; i < nsrc[k]; ++i) {
+            int b = src[k * 32 + i];
+            if (b < 0 || b >= 2 * R)
+                return -1;
+            srcs[i] = b < R ? in[b] : out[b - R];
+        }
+        for (c = cbeg[k]; c < cend[k]; ++c) {
+            size_t lo = (size_t)c * C, hi = lo + C, e;
+            if (lo > N)
+                lo = N;
+            if (hi > N)
+                hi = N;
+            for (e = lo; e < hi; ++e) {
+                if (kind[k] == 0) {
+                    size_t s = oracle_elem_size(dtype);
+                    memmove((unsigned char *)d + e * s, (const unsigned char *)srcs[0] + e * s, s);
+                } else {
+                    store_narrowed(dtype, d, e, fold_element(nsrc[k], dtype, srcs, e));
+                }
+            }
+        }
     }
     return 0;
 }
