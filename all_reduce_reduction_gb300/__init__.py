@@ -72,6 +72,24 @@ class ar_info(ctypes.Structure):
         return {name: getattr(self, name) for name, _ in self._fields_}
 
 
+AR_OP_COPY, AR_OP_REDUCE = 0, 1
+AR_BUF_IN, AR_BUF_OUT = 0, 1
+
+
+class ar_op(ctypes.Structure):
+    _fields_ = [
+        ("kind", ctypes.c_int),
+        ("rank", ctypes.c_int),
+        ("dst_buf", ctypes.c_int),
+        ("dst_rank", ctypes.c_int),
+        ("src_buf", ctypes.c_int),
+        ("nsrc", ctypes.c_int),
+        ("src_rank", ctypes.c_int * AR_MAX_RANKS),
+        ("chunk_begin", ctypes.c_int),
+        ("chunk_end", ctypes.c_int),
+    ]
+
+
 _lock = threading.Lock()
 _lib = None
 
@@ -99,6 +117,11 @@ SIGNATURES = {
     "ar_get_info": ([_VP, ctypes.POINTER(ar_info)], _I),
     "ar_strerror": ([_I], ctypes.c_char_p),
     "ar_allreduce_ll_static": ([_I, _SZ, _I, _VPP, _VPP, _VP], _I),
+    "ar_plan_compile": ([_VP, ctypes.POINTER(ar_op), _I, _I, _I, ctypes.POINTER(_VP)], _I),
+    "ar_plan_builtin": ([_VP, _I, _I, _I, ctypes.POINTER(_VP)], _I),
+    "ar_plan_execute": ([_VP, _VPP, _VPP, _VP], _I),
+    "ar_plan_stats": ([_VP, ctypes.POINTER(_I), ctypes.POINTER(_I), ctypes.POINTER(_I)], _I),
+    "ar_plan_destroy": ([_VP], _I),
 }
 
 
@@ -254,6 +277,55 @@ def ar_allreduce_ll_static(R: int, N: int, dtype, ins, outs, stream=None) -> Non
 
 
 AR_NOALLOC_SCRATCH_BYTES = 8 << 20
+
+
+def make_op(kind, rank, dst, srcs, chunk_begin, chunk_end) -> ar_op:
+    """One plan step.  dst = (buf, rank); srcs = [(buf, rank), ...] (all of
+    one buffer kind)."""
+    o = ar_op()
+    o.kind = kind
+    o.rank = rank
+    o.dst_buf, o.dst_rank = dst
+    o.src_buf = srcs[0][0]
+    o.nsrc = len(srcs)
+    for i, (b, r) in enumerate(srcs):
+        if b != o.src_buf:
+            raise ValueError("the sources of one step share a buffer kind")
+        o.src_rank[i] = r
+    o.chunk_begin, o.chunk_end = chunk_begin, chunk_end
+    return o
+
+
+def ar_plan_compile(h: int, ops, nchunks: int, ctas_per_rank: int = 1) -> int:
+    arr = (ar_op * len(ops))(*ops)
+    p = ctypes.c_void_p()
+    _check(load_library().ar_plan_compile(h, arr, len(ops), nchunks, ctas_per_rank,
+                                          ctypes.byref(p)), "ar_plan_compile")
+    return p.value
+
+
+def ar_plan_builtin(h: int, algo, chunks_per_rank: int = 4, ctas_per_rank: int = 4) -> int:
+    algo = ALGOS[algo] if isinstance(algo, str) else algo
+    p = ctypes.c_void_p()
+    _check(load_library().ar_plan_builtin(h, algo, chunks_per_rank, ctas_per_rank,
+                                          ctypes.byref(p)), "ar_plan_builtin")
+    return p.value
+
+
+def ar_plan_execute(p: int, ins, outs, stream=None) -> None:
+    _check(load_library().ar_plan_execute(p, _ptr_array(ins), _ptr_array(outs), _stream(stream)),
+           "ar_plan_execute")
+
+
+def ar_plan_stats(p: int):
+    t, w, s = ctypes.c_int(), ctypes.c_int(), ctypes.c_int()
+    _check(load_library().ar_plan_stats(p, ctypes.byref(t), ctypes.byref(w), ctypes.byref(s)),
+           "ar_plan_stats")
+    return t.value, w.value, s.value
+
+
+def ar_plan_destroy(p: int) -> None:
+    _check(load_library().ar_plan_destroy(p), "ar_plan_destroy")
 
 
 class Handle:

@@ -292,6 +292,10 @@ void resolve(const ar_handle *h, uint64_t bytes, int *algo, int *proto) {
 
 }  // namespace
 
+namespace ar {
+Ctl handle_ctl(ar_handle_t h) { return h->ctl; }
+}  // namespace ar
+
 // ---------------------------------------------------------------------------
 
 extern "C" {

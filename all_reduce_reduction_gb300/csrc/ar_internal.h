@@ -126,6 +126,9 @@ struct PackArgs {
 
 // ---- launchers (return the launch's cudaError_t) ----------------------------
 
+// ar_api.cu: a handle's device control words (status, abort, epoch, limit)
+Ctl handle_ctl(ar_handle_t h);
+
 // ar_hb.cu
 cudaError_t launch_one_shot_hb(const HbArgs &a, int dtype, bool vec, int grid, int block,
                                cudaStream_t s, bool pdl = false);

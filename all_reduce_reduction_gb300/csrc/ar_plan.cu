@@ -1,0 +1,501 @@
+// Plans: an algorithm written as copy / reduce steps over chunks of the rank
+// buffers, compiled on the host into one instruction stream per CTA (with the
+// synchronisation the data dependencies need), and interpreted on the device
+// by one cooperative kernel.
+//
+// Source: "【论文分享】MSCCL++：让 GPU 通信像 CUDA 一样可编程", section
+// "第二层：DSL API": an algorithm author writes channel put / wait / reduce
+// steps; the DSL compiler analyses the data dependencies, inserts the
+// synchronisation and produces an execution plan that the runtime
+// interprets.  Here a step is a copy (a put into a peer's buffer: every
+// virtual peer's buffer is in this GPU's memory) or a reduce; the waits and
+// signals are what the compiler inserts.
+//
+// Compilation.
+//   * Buffers are cut into nchunks chunks (16-byte aligned boundaries).  Step
+//     k over chunks [b, e) becomes tasks (k, c), c in [b, e).  Task (k, c)
+//     runs on CTA rank_k * G + c % G: each virtual rank owns G CTAs.
+//   * Program order is the order of the steps.  For every (buffer, chunk)
+//     region the compiler tracks the last writer and the readers since; a
+//     task depends on the last writer of every region it reads or writes
+//     (read-after-write, write-after-write) and on the readers since that
+//     write of every region it writes (write-after-read).
+//   * A dependency inside one CTA needs nothing beyond program order (the
+//     CTA syncs its threads between tasks).  One across CTAs gets a
+//     semaphore: the producer task signals it once per run, the consumer
+//     waits for it.  Every wait targets a task earlier in program order, and
+//     all CTAs are resident at once (cooperative launch), so every wait ends.
+//
+// Runs.  Semaphores count completed producer tasks over all runs; run m
+// (read from per-CTA epoch words like the LL flag) waits for the value
+// m + 1, compared modulo 2^32.  A run whose wait timed out leaves the counts
+// out of step: such a plan reports AR_ERR_TIMEOUT and must be rebuilt.
+#include <algorithm>
+#include <map>
+#include <new>
+#include <vector>
+
+#include "ar_device.cuh"
+
+namespace ar {
+
+enum : int { kInstrWait = 0, kInstrTask = 1, kInstrSignal = 2 };
+
+struct PlanStep {            // device copy of one step
+    int kind;                // AR_OP_COPY / AR_OP_REDUCE
+    int dst;                 // buffer id: < R in[], else out[id - R]
+    int nsrc;
+    int src[AR_MAX_RANKS];
+};
+
+struct PlanArgs {
+    RankPtrs p;
+    uint64_t n;
+    uint64_t chunk;          // elements per chunk (multiple of a 16-byte vector)
+    const PlanStep *steps;
+    const int4 *instr;       // {kind, a, b, 0}: wait(sem a) / task(step a, chunk b) / signal(sem a)
+    const int *start;        // instr[start[b] .. start[b + 1]) belong to CTA b
+    uint32_t *sems;
+    uint32_t *epoch;         // one word per CTA: completed runs
+    int R;
+    int vec;                 // every buffer 16-byte aligned
+    Ctl c;
+};
+
+__device__ __forceinline__ const void *buf_ptr(const PlanArgs &a, int id) {
+    return id < a.R ? a.p.in[id] : a.p.out[id - a.R];
+}
+
+template <int DT>
+__device__ void run_task(const PlanArgs &a, const PlanStep &st, uint64_t chunk) {
+    constexpr int PV = Elem<DT>::kPerVec;
+    const uint64_t lo = chunk * a.chunk;
+    uint64_t hi = lo + a.chunk;
+    if (hi > a.n)
+        hi = a.n;
+    if (lo >= hi)
+        return;
+    void *dst = const_cast<void *>(buf_ptr(a, st.dst));
+    uint64_t vhi = lo;                                   // [lo, vhi): whole vectors
+    if (a.vec) {
+        vhi = lo + (hi - lo) / PV * PV;
+        for (uint64_t u = lo / PV + threadIdx.x; u < vhi / PV; u += blockDim.x) {
+            if (st.kind == AR_OP_COPY) {
+                st_v4(reinterpret_cast<uint4 *>(dst) + u,
+                      ld_v4_stream(reinterpret_cast<const uint4 *>(buf_ptr(a, st.src[0])) + u));
+            } else {
+                VecAcc<DT> acc;
+                acc.init(ld_v4_stream(reinterpret_cast<const uint4 *>(buf_ptr(a, st.src[0])) + u));
+                for (int k = 1; k < st.nsrc; ++k)
+                    acc.add(ld_v4_stream(reinterpret_cast<const uint4 *>(buf_ptr(a, st.src[k])) + u));
+                st_v4(reinterpret_cast<uint4 *>(dst) + u, acc.result());
+            }
+        }
+    }
+    for (uint64_t e = vhi + threadIdx.x; e < hi; e += blockDim.x) {
+        if (st.kind == AR_OP_COPY) {
+            st_elem<DT>(dst, e, ld_elem<DT>(buf_ptr(a, st.src[0]), e));
+        } else {
+            ElemAcc<DT> acc;
+            acc.init(ld_elem<DT>(buf_ptr(a, st.src[0]), e));
+            for (int k = 1; k < st.nsrc; ++k)
+                acc.add(ld_elem<DT>(buf_ptr(a, st.src[k]), e));
+            st_elem<DT>(dst, e, acc.result());
+        }
+    }
+}
+
+template <int DT>
+__global__ void __launch_bounds__(kRegThreads) k_plan(const __grid_constant__ PlanArgs a) {
+    __shared__ int give_up;
+    kernel_prologue();
+    const uint32_t run = ld_u32_relaxed(a.epoch + blockIdx.x);
+    const uint32_t target = run + 1u;                    // what a producer's semaphore reaches
+    if (threadIdx.x == 0)
+        give_up = 0;
+    __syncthreads();
+    const int i0 = a.start[blockIdx.x], i1 = a.start[blockIdx.x + 1];
+    for (int i = i0; i < i1; ++i) {
+        const int4 in = a.instr[i];
+        if (in.x == kInstrWait) {
+            if (threadIdx.x == 0 && !give_up) {
+                // bounded acquire-poll of the producer's semaphore
+                const uint32_t *sem = a.sems + in.y;
+                uint64_t deadline = 0;
+                uint32_t tries = 0;
+                for (;;) {
+                    uint32_t v;
+                    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(sem) : "memory");
+                    if ((int32_t)(v - target) >= 0)
+                        break;
+                    if (++tries > 8)
+                        __nanosleep(64);
+                    if ((tries & 15u) == 15u) {
+                        if (ld_u32_relaxed(a.c.abort) == target) {
+                            give_up = 1;
+                            break;
+                        }
+                        const uint64_t now = globaltimer_ns();
+                        if (deadline == 0) {
+                            deadline = now + a.c.timeout_ns;
+                        } else if (now > deadline) {
+                            record_error(a.c.status, AR_ERR_TIMEOUT);
+                            st_u32_relaxed(a.c.abort, target);
+                            give_up = 1;
+                            break;
+                        }
+                    }
+                }
+            }
+            __syncthreads();
+        } else if (in.x == kInstrTask) {
+            if (!give_up)
+                run_task<DT>(a, a.steps[in.y], (uint64_t)in.z);
+            __syncthreads();
+        } else {
+            // every thread's writes of the task are done (barrier above);
+            // make them visible GPU-wide, then count the task complete
+            if (threadIdx.x == 0 && !give_up) {
+                __threadfence();
+                asm volatile("red.release.gpu.global.add.u32 [%0], 1;" :: "l"(a.sems + in.y) : "memory");
+            }
+        }
+    }
+    __syncthreads();
+    if (threadIdx.x == 0)
+        st_u32_relaxed(a.epoch + blockIdx.x, target);
+}
+
+template <int DT> static const void *plan_kernel() {
+    return reinterpret_cast<const void *>(&k_plan<DT>);
+}
+
+static const void *plan_kernel_for(int dtype) {
+    switch (dtype) {
+    case AR_BF16: return plan_kernel<AR_BF16>();
+    case AR_FP16: return plan_kernel<AR_FP16>();
+    default: return plan_kernel<AR_FP32>();
+    }
+}
+
+}  // namespace ar
+
+using namespace ar;
+
+// ---------------------------------------------------------------------------
+// Host side: the compiler and the C ABI.
+// ---------------------------------------------------------------------------
+
+struct ar_plan {
+    int R, dtype, G, nchunks, device;
+    uint64_t N, chunk;
+    size_t esz;
+    int ntasks, nwaits, nsignals;
+    void *dev;               // one allocation: steps | instr | start | sems | epoch
+    PlanStep *steps;
+    int4 *instr;
+    int *start;
+    uint32_t *sems;
+    uint32_t *epoch;
+    Ctl ctl;                 // the handle's status / abort words and timeout
+};
+
+namespace {
+
+struct Task {
+    int step, chunk, cta;
+    std::vector<int> deps;   // producer tasks in other CTAs
+    bool signals = false;
+    int sem = -1;
+};
+
+uint64_t ceil_div_u(uint64_t a, uint64_t b) { return (a + b - 1) / b; }
+
+}  // namespace
+
+extern "C" int ar_plan_compile(ar_handle_t h, const ar_op *ops, int nops, int nchunks,
+                               int ctas_per_rank, ar_plan_t *out) {
+    ar_info info;
+    if (!out)
+        return AR_ERR_INVALID;
+    *out = nullptr;
+    if (!h || !ops || nops < 1 || nchunks < 1 || ctas_per_rank < 1 ||
+        ar_get_info(h, &info) != AR_OK)
+        return AR_ERR_INVALID;
+    const int R = info.R;
+    for (int k = 0; k < nops; ++k) {
+        const ar_op &o = ops[k];
+        if ((o.kind != AR_OP_COPY && o.kind != AR_OP_REDUCE) || o.rank < 0 || o.rank >= R ||
+            o.dst_buf < 0 || o.dst_buf > 1 || o.dst_rank < 0 || o.dst_rank >= R ||
+            o.src_buf < 0 || o.src_buf > 1 || o.nsrc < 1 || o.nsrc > R ||
+            (o.kind == AR_OP_COPY && o.nsrc != 1) || o.chunk_begin < 0 ||
+            o.chunk_end > nchunks || o.chunk_begin > o.chunk_end)
+            return AR_ERR_INVALID;
+        for (int i = 0; i < o.nsrc; ++i)
+            if (o.src_rank[i] < 0 || o.src_rank[i] >= R)
+                return AR_ERR_INVALID;
+    }
+    const int G = ctas_per_rank;
+    const int ctas = R * G;
+    int per_sm = 0, dev = 0, sms = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, plan_kernel_for(info.dtype),
+                                                      kRegThreads, 0) != cudaSuccess) {
+        (void)cudaGetLastError();
+        return AR_ERR_CUDA;
+    }
+    if (ctas > per_sm * sms || ctas > kEpochWords)
+        return AR_ERR_UNSUPPORTED;                       // not all CTAs can be resident
+
+    // tasks in program order, with their dependencies
+    std::vector<Task> tasks;
+    std::map<std::pair<int, int>, int> last_writer;            // (buffer id, chunk) -> task
+    std::map<std::pair<int, int>, std::vector<int>> readers;   // since that write
+    std::vector<PlanStep> steps(nops);
+    for (int k = 0; k < nops; ++k) {
+        const ar_op &o = ops[k];
+        PlanStep &st = steps[k];
+        st.kind = o.kind;
+        st.dst = o.dst_buf * R + o.dst_rank;
+        st.nsrc = o.nsrc;
+        for (int i = 0; i < AR_MAX_RANKS; ++i)
+            st.src[i] = i < o.nsrc ? o.src_buf * R + o.src_rank[i] : 0;
+        for (int c = o.chunk_begin; c < o.chunk_end; ++c) {
+            Task t;
+            t.step = k;
+            t.chunk = c;
+            t.cta = o.rank * G + c % G;
+            const int id = (int)tasks.size();
+            std::vector<int> deps;
+            for (int i = 0; i < o.nsrc; ++i) {
+                auto w = last_writer.find({st.src[i], c});
+                if (w != last_writer.end())
+                    deps.push_back(w->second);
+            }
+            const std::pair<int, int> dkey{st.dst, c};
+            auto w = last_writer.find(dkey);
+            if (w != last_writer.end())
+                deps.push_back(w->second);
+            for (int rd : readers[dkey])
+                deps.push_back(rd);
+            std::sort(deps.begin(), deps.end());
+            deps.erase(std::unique(deps.begin(), deps.end()), deps.end());
+            for (int d : deps)
+                if (tasks[d].cta != t.cta && d != id) {
+                    t.deps.push_back(d);
+                    tasks[d].signals = true;
+                }
+            for (int i = 0; i < o.nsrc; ++i)
+                if (st.src[i] != st.dst)
+                    readers[{st.src[i], c}].push_back(id);
+            last_writer[dkey] = id;
+            readers[dkey].clear();
+            tasks.push_back(t);
+        }
+    }
+    int nsems = 0, nwaits = 0;
+    for (auto &t : tasks)
+        if (t.signals)
+            t.sem = nsems++;
+    // one instruction stream per CTA, in program order
+    std::vector<std::vector<int4>> prog(ctas);
+    for (size_t id = 0; id < tasks.size(); ++id) {
+        const Task &t = tasks[id];
+        for (int d : t.deps) {
+            prog[t.cta].push_back(make_int4(kInstrWait, tasks[d].sem, 0, 0));
+            ++nwaits;
+        }
+        prog[t.cta].push_back(make_int4(kInstrTask, t.step, t.chunk, 0));
+        if (t.signals)
+            prog[t.cta].push_back(make_int4(kInstrSignal, t.sem, 0, 0));
+    }
+    std::vector<int> start(ctas + 1, 0);
+    std::vector<int4> flat;
+    for (int b = 0; b < ctas; ++b) {
+        start[b] = (int)flat.size();
+        flat.insert(flat.end(), prog[b].begin(), prog[b].end());
+    }
+    start[ctas] = (int)flat.size();
+
+    ar_plan *p = new (std::nothrow) ar_plan();
+    if (!p)
+        return AR_ERR_NOMEM;
+    p->R = R;
+    p->dtype = info.dtype;
+    p->G = G;
+    p->nchunks = nchunks;
+    p->device = dev;
+    p->N = info.N;
+    p->esz = info.elem_size;
+    const uint64_t per_vec = 16 / p->esz;
+    p->chunk = ceil_div_u(ceil_div_u(p->N, (uint64_t)nchunks), per_vec) * per_vec;
+    p->ntasks = (int)tasks.size();
+    p->nwaits = nwaits;
+    p->nsignals = nsems;
+    const size_t b_steps = sizeof(PlanStep) * steps.size();
+    const size_t b_instr = sizeof(int4) * (flat.size() + 1);
+    const size_t b_start = sizeof(int) * start.size();
+    const size_t b_sems = sizeof(uint32_t) * (nsems + 1);
+    const size_t b_epoch = sizeof(uint32_t) * (ctas + 1);    // + the plan's abort word
+    auto up = [](size_t x) { return (x + 255) / 256 * 256; };
+    const size_t total = up(b_steps) + up(b_instr) + up(b_start) + up(b_sems) + up(b_epoch);
+    if (cudaMalloc(&p->dev, total) != cudaSuccess) {
+        (void)cudaGetLastError();
+        delete p;
+        return AR_ERR_NOMEM;
+    }
+    uint8_t *base = static_cast<uint8_t *>(p->dev);
+    p->steps = reinterpret_cast<PlanStep *>(base);
+    p->instr = reinterpret_cast<int4 *>(base + up(b_steps));
+    p->start = reinterpret_cast<int *>(base + up(b_steps) + up(b_instr));
+    p->sems = reinterpret_cast<uint32_t *>(base + up(b_steps) + up(b_instr) + up(b_start));
+    p->epoch = reinterpret_cast<uint32_t *>(base + up(b_steps) + up(b_instr) + up(b_start) +
+                                            up(b_sems));
+    if (cudaMemset(p->dev, 0, total) != cudaSuccess ||
+        cudaMemcpy(p->steps, steps.data(), b_steps, cudaMemcpyHostToDevice) != cudaSuccess ||
+        (flat.size() && cudaMemcpy(p->instr, flat.data(), sizeof(int4) * flat.size(),
+                                   cudaMemcpyHostToDevice) != cudaSuccess) ||
+        cudaMemcpy(p->start, start.data(), b_start, cudaMemcpyHostToDevice) != cudaSuccess ||
+        cudaDeviceSynchronize() != cudaSuccess) {
+        (void)cudaGetLastError();
+        cudaFree(p->dev);
+        delete p;
+        return AR_ERR_CUDA;
+    }
+    // status word and wait limit from the handle (ar_status reports plan
+    // errors); an abort word of the plan's own, since plan runs and LL calls
+    // name themselves with unrelated counters
+    p->ctl = handle_ctl(h);
+    p->ctl.abort = p->epoch + ctas;
+    *out = p;
+    return AR_OK;
+}
+
+extern "C" int ar_plan_builtin(ar_handle_t h, int algo, int chunks_per_rank, int ctas_per_rank,
+                               ar_plan_t *out) {
+    ar_info info;
+    if (!out || !h || ar_get_info(h, &info) != AR_OK || chunks_per_rank < 1 ||
+        (algo != AR_ONE_SHOT && algo != AR_TWO_SHOT))
+        return AR_ERR_INVALID;
+    const int R = info.R, K = chunks_per_rank;
+    std::vector<ar_op> ops;
+    ar_op o = {};
+    o.kind = AR_OP_REDUCE;
+    o.src_buf = AR_BUF_IN;
+    o.nsrc = R;
+    for (int k = 0; k < R; ++k)
+        o.src_rank[k] = k;
+    o.dst_buf = AR_BUF_OUT;
+    if (algo == AR_ONE_SHOT) {
+        // every rank folds every input into its own output
+        for (int r = 0; r < R; ++r) {
+            o.rank = o.dst_rank = r;
+            o.chunk_begin = 0;
+            o.chunk_end = R * K;
+            ops.push_back(o);
+        }
+    } else {
+        // reduce-scatter: rank j folds shard j into out[j] ...
+        for (int j = 0; j < R; ++j) {
+            o.rank = o.dst_rank = j;
+            o.chunk_begin = j * K;
+            o.chunk_end = (j + 1) * K;
+            ops.push_back(o);
+        }
+        // ... all-gather: rank r puts every other shard into its output
+        ar_op c = {};
+        c.kind = AR_OP_COPY;
+        c.src_buf = AR_BUF_OUT;
+        c.dst_buf = AR_BUF_OUT;
+        c.nsrc = 1;
+        for (int r = 0; r < R; ++r)
+            for (int j = 0; j < R; ++j) {
+                if (j == r)
+                    continue;
+                c.rank = c.dst_rank = r;
+                c.src_rank[0] = j;
+                c.chunk_begin = j * K;
+                c.chunk_end = (j + 1) * K;
+                ops.push_back(c);
+            }
+    }
+    return ar_plan_compile(h, ops.data(), (int)ops.size(), R * K, ctas_per_rank, out);
+}
+
+extern "C" int ar_plan_execute(ar_plan_t p, const void *const in[], void *const out[],
+                               cudaStream_t stream) {
+    if (!p || !in || !out)
+        return AR_ERR_INVALID;
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev != p->device)
+        return AR_ERR_INVALID;
+    const size_t len = p->N * p->esz;
+    uintptr_t all = 0;
+    for (int r = 0; r < p->R; ++r) {
+        if (!in[r] || !out[r] || ((uintptr_t)in[r] % p->esz) || ((uintptr_t)out[r] % p->esz))
+            return AR_ERR_INVALID;
+        all |= (uintptr_t)in[r] | (uintptr_t)out[r];
+    }
+    // the compiler reasoned about 2R distinct buffers: no overlaps at all
+    for (int a = 0; a < 2 * p->R; ++a) {
+        const uintptr_t x = a < p->R ? (uintptr_t)in[a] : (uintptr_t)out[a - p->R];
+        for (int b = a + 1; b < 2 * p->R; ++b) {
+            const uintptr_t y = b < p->R ? (uintptr_t)in[b] : (uintptr_t)out[b - p->R];
+            if (x < y + len && y < x + len)
+                return AR_ERR_INVALID;
+        }
+    }
+    PlanArgs a;
+    for (int r = 0; r < AR_MAX_RANKS; ++r) {
+        a.p.in[r] = r < p->R ? in[r] : nullptr;
+        a.p.out[r] = r < p->R ? out[r] : nullptr;
+    }
+    a.n = p->N;
+    a.chunk = p->chunk;
+    a.steps = p->steps;
+    a.instr = p->instr;
+    a.start = p->start;
+    a.sems = p->sems;
+    a.epoch = p->epoch;
+    a.R = p->R;
+    a.vec = (all & 15u) == 0;
+    a.c = p->ctl;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)(p->R * p->G));
+    cfg.blockDim = dim3(kRegThreads);
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeCooperative;
+    attr[0].val.cooperative = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    void *args[] = {&a};
+    if (cudaLaunchKernelExC(&cfg, plan_kernel_for(p->dtype), args) != cudaSuccess) {
+        (void)cudaGetLastError();
+        return AR_ERR_CUDA;
+    }
+    return AR_OK;
+}
+
+extern "C" int ar_plan_stats(ar_plan_t p, int *tasks, int *waits, int *signals) {
+    if (!p)
+        return AR_ERR_INVALID;
+    if (tasks)
+        *tasks = p->ntasks;
+    if (waits)
+        *waits = p->nwaits;
+    if (signals)
+        *signals = p->nsignals;
+    return AR_OK;
+}
+
+extern "C" int ar_plan_destroy(ar_plan_t p) {
+    if (!p)
+        return AR_OK;
+    int rc = AR_OK;
+    if (cudaDeviceSynchronize() != cudaSuccess || cudaFree(p->dev) != cudaSuccess)
+        rc = AR_ERR_CUDA;
+    delete p;
+    return rc;
+}

@@ -300,6 +300,79 @@ int ar_get_info(ar_handle_t h, ar_info *info);
 /* Static string naming an ar_status_code. */
 const char *ar_strerror(int code);
 
+/* ---------------------------------------------------------------------------
+ * Plans: an algorithm written as steps, compiled, then executed.
+ *
+ * "【论文分享】MSCCL++：让 GPU 通信像 CUDA 一样可编程", section
+ * "第二层：DSL API": an algorithm author writes channel put / wait / reduce
+ * steps; a compiler analyses the data dependencies, inserts the
+ * synchronisation and emits an execution plan that a runtime interprets.
+ * Here a step is a copy (a put into a peer's buffer; every virtual peer's
+ * buffer is in this GPU's memory) or a reduce over chunks of the rank
+ * buffers; ar_plan_compile adds the waits and signals; ar_plan_execute runs
+ * the plan as one cooperative kernel in which every CTA interprets its own
+ * instruction stream.  A plan means exactly its steps executed one after
+ * another in the order written.
+ * ------------------------------------------------------------------------- */
+enum ar_op_kind {
+    AR_OP_COPY = 0,            /* dst[c] = src[0][c] (bits unchanged)          */
+    AR_OP_REDUCE = 1           /* dst[c] = round(fold of src[0..nsrc-1][c])    */
+};
+enum ar_buf_kind {
+    AR_BUF_IN = 0,             /* the in[] buffer of a rank                   */
+    AR_BUF_OUT = 1             /* the out[] buffer of a rank                  */
+};
+
+/* One step.  Buffers are cut into `nchunks` chunks (ar_plan_compile): chunk
+ * c holds elements [c*C, min((c+1)*C, N)), C = ceil(N / nchunks) rounded up
+ * to a whole 16-byte vector.  The step runs on chunks [chunk_begin,
+ * chunk_end) in the program of virtual rank `rank`.  A reduce folds its
+ * sources in the order listed (binary32, left to right) and rounds once. */
+typedef struct ar_op {
+    int kind;                  /* enum ar_op_kind                              */
+    int rank;                  /* whose program runs the step, 0..R-1         */
+    int dst_buf, dst_rank;     /* destination: enum ar_buf_kind, rank         */
+    int src_buf;               /* sources' buffer kind                        */
+    int nsrc;                  /* 1 for a copy, 1..R for a reduce             */
+    int src_rank[AR_MAX_RANKS];/* sources' ranks, in fold order               */
+    int chunk_begin, chunk_end;
+} ar_op;
+
+typedef struct ar_plan *ar_plan_t;
+
+/* Compile `nops` steps for the handle's R, N and dtype.  Each step over k
+ * chunks becomes k tasks; task (step, c) runs on CTA rank * ctas_per_rank +
+ * c % ctas_per_rank.  A task waits for every earlier task in another CTA
+ * whose chunk it reads after a write, writes after a read, or writes after
+ * a write; those producers signal a semaphore.  Allocates the plan's device
+ * memory and waits for the upload (not a hot-path call).
+ * Errors: AR_ERR_INVALID (bad step, range), AR_ERR_UNSUPPORTED (R *
+ * ctas_per_rank CTAs cannot all be resident), AR_ERR_NOMEM, AR_ERR_CUDA. */
+int ar_plan_compile(ar_handle_t h, const ar_op *ops, int nops, int nchunks,
+                    int ctas_per_rank, ar_plan_t *out);
+
+/* The two all-reduce algorithms as plans, with chunks_per_rank * R chunks:
+ *   AR_ONE_SHOT: rank r reduces every input into out[r];
+ *   AR_TWO_SHOT: rank j reduces shard j (chunks [j*K, (j+1)*K)) into out[j],
+ *                then every rank copies every other shard into its output.
+ * Same results as ar_allreduce.  Errors as ar_plan_compile. */
+int ar_plan_builtin(ar_handle_t h, int algo, int chunks_per_rank, int ctas_per_rank,
+                    ar_plan_t *out);
+
+/* Run the plan once on these buffers (host arrays of R device pointers, N
+ * elements each; the 2R buffers must not overlap).  Capturable in a CUDA
+ * graph: the run index comes from device-side epoch words.  Waits are
+ * bounded by the handle's timeout; a timed-out run reports AR_ERR_TIMEOUT
+ * through ar_status on the handle, and the plan must then be rebuilt. */
+int ar_plan_execute(ar_plan_t p, const void *const in[], void *const out[], cudaStream_t stream);
+
+/* Tasks, inserted waits and signalling tasks of a compiled plan (any
+ * pointer may be NULL). */
+int ar_plan_stats(ar_plan_t p, int *tasks, int *waits, int *signals);
+
+/* Free a plan (waits for the device first).  NULL is accepted. */
+int ar_plan_destroy(ar_plan_t p);
+
 /* Bytes of packet scratch compiled into the library for
  * ar_allreduce_ll_static (every GPU that loads the library holds this much
  * static device memory, plus 33 KiB of control words, until the process
