@@ -207,22 +207,39 @@ def hbm_peak():
         return FALLBACK_HBM_GBS, "fallback"
 
 
-def kernel_source_digest() -> str:
+# device sources of each kernel family (the key's leading words)
+KERNEL_SOURCES = {
+    "one_shot_ll_global": ["ar_ll.cu"],
+    "two_shot_ll": ["ar_ll.cu"],
+    "one_shot_ll_cluster": ["ar_ll_cluster.cu"],
+    "one_shot_hb": ["ar_hb.cu"],
+    "two_shot_hb": ["ar_tma.cu"],
+}
+
+
+def kernel_source_digest(kernel_key: str) -> str:
+    """Digest of the device code a kernel key names: its .cu file plus the
+    shared device header.  Any edit to them invalidates recorded counters."""
+    files = None
+    for prefix, fs in KERNEL_SOURCES.items():
+        if kernel_key.startswith(prefix):
+            files = fs
+    if files is None:
+        return "unknown"
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "all_reduce_reduction_gb300", "csrc")
-    for fn in sorted(os.listdir(csrc)):
-        if fn.endswith((".cu", ".cuh", ".h")):
-            h.update(open(os.path.join(csrc, fn), "rb").read())
+    for fn in files + ["ar_device.cuh"]:
+        h.update(open(os.path.join(csrc, fn), "rb").read())
     return h.hexdigest()[:16]
 
 
 def committed_traffic(kernel_key: str):
     """DRAM bytes per launch recorded by an ncu capture in profiles/, if the
-    kernels have not changed since (same source digest); else None."""
+    kernel's device code has not changed since (same digest); else None."""
     path = os.path.join(ROOT, "profiles", "traffic.txt")
     if not os.path.exists(path):
         return None
-    digest = kernel_source_digest()
+    digest = kernel_source_digest(kernel_key)
     for line in open(path):
         f = line.split()
         if len(f) >= 3 and f[0] == kernel_key and f[2] == digest:
@@ -349,8 +366,9 @@ def run_ours(args, dist: Dist):
     launch_s = per_case[dom] * 1e-3 / (args.steps * dr.c["calls"])
     peak, peak_kind = hbm_peak()
     achieved = dr.bytes / launch_s / 1e9
-    kkey = "%s_%s_r%d_n%d_%s" % (dr.c["algo"], dr.c["proto"], dr.w.R, dr.w.n, dr.w.dtype)
-    if dr.c["proto"] == "ll" and dr.c["algo"] == "one_shot":
+    path = dr.choice or "%s_%s" % (dr.c["algo"], dr.c["proto"])
+    kkey = "%s_r%d_n%d_%s" % (path, dr.w.R, dr.w.n, dr.w.dtype)
+    if path == "one_shot_ll":
         info = ar.ar_get_info(dr.h.h)
         tr = dr.c.get("transport", ar.AR_LL_AUTO)
         cluster = bool(info["ll_cluster_ok"]) and tr == ar.AR_LL_CLUSTER

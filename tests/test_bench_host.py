@@ -89,7 +89,8 @@ def test_clock_rows():
     assert not bench.clocks_rejected(bench.parse_clock_rows(capped, None))
 
 
-def test_traffic_lookup_needs_matching_digest(tmp_path, monkeypatch):
-    d = bench.kernel_source_digest()
+def test_traffic_lookup_needs_matching_digest():
+    d = bench.kernel_source_digest("two_shot_hb_r16_n67108864_bf16")
     assert len(d) == 16
+    assert bench.kernel_source_digest("no_such_kernel") == "unknown"
     assert bench.committed_traffic("no_such_kernel") is None
