@@ -66,8 +66,16 @@ __device__ __forceinline__ const void *buf_ptr(const PlanArgs &a, int id) {
     return id < a.R ? a.p.in[id] : a.p.out[id - a.R];
 }
 
+// The step's buffer pointers, resolved once per task into shared memory (the
+// step table itself lives in global memory).
+struct TaskPtrs {
+    const void *src[AR_MAX_RANKS];
+    void *dst;
+    int kind, nsrc;
+};
+
 template <int DT>
-__device__ void run_task(const PlanArgs &a, const PlanStep &st, uint64_t chunk) {
+__device__ void run_task(const PlanArgs &a, const TaskPtrs &t, uint64_t chunk) {
     constexpr int PV = Elem<DT>::kPerVec;
     const uint64_t lo = chunk * a.chunk;
     uint64_t hi = lo + a.chunk;
@@ -75,32 +83,45 @@ __device__ void run_task(const PlanArgs &a, const PlanStep &st, uint64_t chunk) 
         hi = a.n;
     if (lo >= hi)
         return;
-    void *dst = const_cast<void *>(buf_ptr(a, st.dst));
+    const int nsrc = t.nsrc;
     uint64_t vhi = lo;                                   // [lo, vhi): whole vectors
     if (a.vec) {
         vhi = lo + (hi - lo) / PV * PV;
         for (uint64_t u = lo / PV + threadIdx.x; u < vhi / PV; u += blockDim.x) {
-            if (st.kind == AR_OP_COPY) {
-                st_v4(reinterpret_cast<uint4 *>(dst) + u,
-                      ld_v4_stream(reinterpret_cast<const uint4 *>(buf_ptr(a, st.src[0])) + u));
-            } else {
-                VecAcc<DT> acc;
-                acc.init(ld_v4_stream(reinterpret_cast<const uint4 *>(buf_ptr(a, st.src[0])) + u));
-                for (int k = 1; k < st.nsrc; ++k)
-                    acc.add(ld_v4_stream(reinterpret_cast<const uint4 *>(buf_ptr(a, st.src[k])) + u));
-                st_v4(reinterpret_cast<uint4 *>(dst) + u, acc.result());
+            if (t.kind == AR_OP_COPY) {
+                st_v4(reinterpret_cast<uint4 *>(t.dst) + u,
+                      ld_v4_stream(reinterpret_cast<const uint4 *>(t.src[0]) + u));
+                continue;
             }
+            // fold the sources in their order, eight loads in flight at a time
+            VecAcc<DT> acc;
+            for (int k0 = 0; k0 < nsrc; k0 += 8) {
+                uint4 v[8];
+#pragma unroll
+                for (int j = 0; j < 8; ++j)
+                    if (k0 + j < nsrc)
+                        v[j] = ld_v4_stream(reinterpret_cast<const uint4 *>(t.src[k0 + j]) + u);
+#pragma unroll
+                for (int j = 0; j < 8; ++j)
+                    if (k0 + j < nsrc) {
+                        if (k0 + j == 0)
+                            acc.init(v[j]);
+                        else
+                            acc.add(v[j]);
+                    }
+            }
+            st_v4(reinterpret_cast<uint4 *>(t.dst) + u, acc.result());
         }
     }
     for (uint64_t e = vhi + threadIdx.x; e < hi; e += blockDim.x) {
-        if (st.kind == AR_OP_COPY) {
-            st_elem<DT>(dst, e, ld_elem<DT>(buf_ptr(a, st.src[0]), e));
+        if (t.kind == AR_OP_COPY) {
+            st_elem<DT>(t.dst, e, ld_elem<DT>(t.src[0], e));
         } else {
             ElemAcc<DT> acc;
-            acc.init(ld_elem<DT>(buf_ptr(a, st.src[0]), e));
-            for (int k = 1; k < st.nsrc; ++k)
-                acc.add(ld_elem<DT>(buf_ptr(a, st.src[k]), e));
-            st_elem<DT>(dst, e, acc.result());
+            acc.init(ld_elem<DT>(t.src[0], e));
+            for (int k = 1; k < nsrc; ++k)
+                acc.add(ld_elem<DT>(t.src[k], e));
+            st_elem<DT>(t.dst, e, acc.result());
         }
     }
 }
@@ -108,6 +129,7 @@ __device__ void run_task(const PlanArgs &a, const PlanStep &st, uint64_t chunk) 
 template <int DT>
 __global__ void __launch_bounds__(kRegThreads) k_plan(const __grid_constant__ PlanArgs a) {
     __shared__ int give_up;
+    __shared__ TaskPtrs tp;
     kernel_prologue();
     const uint32_t run = ld_u32_relaxed(a.epoch + blockIdx.x);
     const uint32_t target = run + 1u;                    // what a producer's semaphore reaches
@@ -149,8 +171,18 @@ __global__ void __launch_bounds__(kRegThreads) k_plan(const __grid_constant__ Pl
             }
             __syncthreads();
         } else if (in.x == kInstrTask) {
-            if (!give_up)
-                run_task<DT>(a, a.steps[in.y], (uint64_t)in.z);
+            if (!give_up) {
+                const PlanStep &st = a.steps[in.y];
+                if (threadIdx.x < (unsigned)st.nsrc)
+                    tp.src[threadIdx.x] = buf_ptr(a, st.src[threadIdx.x]);
+                if (threadIdx.x == 0) {
+                    tp.dst = const_cast<void *>(buf_ptr(a, st.dst));
+                    tp.kind = st.kind;
+                    tp.nsrc = st.nsrc;
+                }
+                __syncthreads();
+                run_task<DT>(a, tp, (uint64_t)in.z);
+            }
             __syncthreads();
         } else {
             // every thread's writes of the task are done (barrier above);

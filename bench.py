@@ -52,9 +52,12 @@ def workload_cases(name: str, args=None):
         w = wl.Workload(9, "custom_r%d_n%d_%s" % (args.R, args.n, args.dtype), args.R, args.n,
                         args.dtype, dist_name)
         big = 2 * w.R * w.n * wl.ELEM_SIZE[w.dtype] > (256 << 20)
-        cases = [dict(w=w, algo=args.algo, proto=args.proto, calls=args.calls, flush=not big)]
-        desc = "custom: R=%d, N=%d %s per rank, %s %s, %d calls per CUDA graph" % (
-            args.R, args.n, args.dtype, args.algo, args.proto, args.calls)
+        cases = [dict(w=w, algo=args.algo, proto=args.proto, calls=args.calls, flush=not big,
+                      plan=args.plan, plan_chunks=args.plan_chunks, plan_ctas=args.plan_ctas)]
+        desc = "custom: R=%d, N=%d %s per rank, %s, %d calls per CUDA graph" % (
+            args.R, args.n, args.dtype,
+            ("%s plan (%d chunks/rank, %d CTAs/rank)" % (args.plan, args.plan_chunks, args.plan_ctas))
+            if args.plan else "%s %s" % (args.algo, args.proto), args.calls)
     elif name == "sweep":
         cases = [dict(w=w, algo="one_shot", proto="ll", calls=10, flush=True) for w in wl.LL_SWEEP]
         desc = ("r8_bf16_ll_sweep: R=8 virtual ranks, bf16, N=2^9..2^18 elements per rank "
@@ -272,13 +275,26 @@ class CaseRunner:
             a, p, _ = ar.ar_get_tuning(self.h.h, w.n * wl.ELEM_SIZE[w.dtype])
             self.choice = "%s_%s" % ({0: "one_shot", 1: "two_shot"}[a], {0: "ll", 1: "hb"}[p])
         self.bytes = case_bytes(c)
+        self.plan = None
+        if c.get("plan"):
+            # the same all-reduce as a compiled plan run by the interpreter kernel
+            self.plan = ar.ar_plan_builtin(self.h.h, c["plan"], c.get("plan_chunks", 4),
+                                           c.get("plan_ctas", 4))
+
+        def call():
+            if self.plan:
+                ar.ar_plan_execute(self.plan, self.ins, self.outs, stream=stream)
+            else:
+                ar.ar_allreduce(self.h.h, self.ins, self.outs, self.algo, self.proto,
+                                stream=stream)
+
         with torch.cuda.stream(stream):
-            ar.ar_allreduce(self.h.h, self.ins, self.outs, self.algo, self.proto, stream=stream)
+            call()
         stream.synchronize()
         self.graph = torch.cuda.CUDAGraph()
         with torch.cuda.graph(self.graph, stream=stream):
             for _ in range(c["calls"]):
-                ar.ar_allreduce(self.h.h, self.ins, self.outs, self.algo, self.proto, stream=stream)
+                call()
         for _ in range(2):
             self.graph.replay()
         torch.cuda.synchronize()
@@ -288,6 +304,9 @@ class CaseRunner:
         self.pinned_out = [torch.empty_like(t).pin_memory() for t in self.cpu_inputs]
 
     def close(self):
+        import all_reduce_reduction_gb300 as ar
+        if self.plan:
+            ar.ar_plan_destroy(self.plan)
         self.h.close()
 
 
@@ -366,7 +385,8 @@ def run_ours(args, dist: Dist):
     launch_s = per_case[dom] * 1e-3 / (args.steps * dr.c["calls"])
     peak, peak_kind = hbm_peak()
     achieved = dr.bytes / launch_s / 1e9
-    path = dr.choice or "%s_%s" % (dr.c["algo"], dr.c["proto"])
+    path = dr.choice or ("plan_" + dr.c["plan"] if dr.c.get("plan") else
+                         "%s_%s" % (dr.c["algo"], dr.c["proto"]))
     kkey = "%s_r%d_n%d_%s" % (path, dr.w.R, dr.w.n, dr.w.dtype)
     if path == "one_shot_ll":
         info = ar.ar_get_info(dr.h.h)
@@ -593,6 +613,10 @@ def main():
     p.add_argument("--algo", default="one_shot", choices=["one_shot", "two_shot", "auto"])
     p.add_argument("--proto", default="ll", choices=["ll", "hb", "auto"])
     p.add_argument("--calls", type=int, default=10)
+    p.add_argument("--plan", default=None, choices=["one_shot", "two_shot"],
+                   help="custom workload: run the built-in plan of that algorithm")
+    p.add_argument("--plan-chunks", type=int, default=4)
+    p.add_argument("--plan-ctas", type=int, default=4)
     p.add_argument("--ll-transport", default="auto", choices=["auto", "global", "cluster"])
     p.add_argument("--no-pdl", action="store_true",
                    help="launch without programmatic dependent launch")
