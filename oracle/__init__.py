@@ -76,6 +76,8 @@ def _bind(lib: ctypes.CDLL) -> ctypes.CDLL:
     ip = ctypes.POINTER(ctypes.c_int)
     lib.oracle_plan_run.argtypes = [i32, sz, i32, i32, i32, ip, ip, ip, ip, ip, ip, vpp, vpp]
     lib.oracle_plan_run.restype = i32
+    lib.oracle_combine.argtypes = [i32, sz, sz, i32, vpp, vp, vp]
+    lib.oracle_combine.restype = i32
     lib.oracle_round_f32.argtypes, lib.oracle_round_f32.restype = [i32, vp, sz, vp], None
     lib.oracle_widen.argtypes, lib.oracle_widen.restype = [i32, vp, sz, vp], None
     return lib
@@ -181,3 +183,15 @@ def plan_run(steps, ins, outs, dtype: int, nchunks: int, lib=None):
     if rc != 0:
         raise ValueError("oracle_plan_run rejected the plan")
     return outs
+
+
+def combine(ys, w: np.ndarray, T: int, H: int, dtype: int, lib=None) -> np.ndarray:
+    """out[t*H+h] = round(fold_k w[t,k] * ys[k][t*H+h]) (see oracle_combine).
+    ``w`` is a float32 array of T*K weights, row-major."""
+    lib = lib or load()
+    w = np.ascontiguousarray(w, dtype=np.float32)
+    out = np.empty(T * H, dtype=STORAGE[dtype])
+    rc = lib.oracle_combine(len(ys), T, H, dtype, _ptr_array(ys), _ptr(w), _ptr(out))
+    if rc != 0:
+        raise ValueError("oracle_combine rejected its arguments")
+    return out

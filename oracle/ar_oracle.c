@@ -376,6 +376,39 @@ int oracle_plan_run(int R, size_t N, int dtype, int nchunks, int nsteps, const i
 }
 
 /* ---------------------------------------------------------------------------
+ * Weighted per-token combine.
+ *
+ * "NCCL EP统一MoE通信生态", section 3.1 and Table III: in the low-latency
+ * mode the combine reduces every token at the receiver, weighting each
+ * expert's output.  Reading used here: K sources y[k] hold T tokens of H
+ * elements (row-major), w holds T x K binary32 weights (row-major), and
+ *   out[t][h] = round_dtype( fold over k = 0..K-1 of  w[t][k] * y[k][t][h] )
+ * with every product rounded to binary32 on its own (no fused multiply-add),
+ * the products folded left to right from k = 0, and one final rounding to
+ * the dtype -- the all-reduce fold with a weight per (token, source).
+ * ------------------------------------------------------------------------- */
+int oracle_combine(int K, size_t T, size_t H, int dtype, const void *const *y, const float *w,
+                   void *out)
+{
+    size_t t, h;
+    int k;
+    if (K < 1 || oracle_elem_size(dtype) == 0)
+        return -1;
+    for (t = 0; t < T; ++t) {
+        for (h = 0; h < H; ++h) {
+            size_t i = t * H + h;
+            float acc = w[t * (size_t)K] * load_widened(dtype, y[0], i);
+            for (k = 1; k < K; ++k) {
+                float p = w[t * (size_t)K + (size_t)k] * load_widened(dtype, y[k], i);
+                acc = acc + p;
+            }
+            store_narrowed(dtype, out, i, acc);
+        }
+    }
+    return 0;
+}
+
+/* ---------------------------------------------------------------------------
  * LL packets.
  * ------------------------------------------------------------------------- */
 

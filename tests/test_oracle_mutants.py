@@ -36,6 +36,9 @@ MUTANTS = {
     "fp16_decode_bias_off": ("mag = ldexpf((float)(1024u + m), (int)e - 25);",
                              "mag = ldexpf((float)(1024u + m), (int)e - 24);"),
     "packet_bytes_big_endian": ("payload |= byte << (8 * j);", "payload |= byte << (8 * (3 - j));"),
+    "combine_fuses_multiply_add": ("                float p = w[t * (size_t)K + (size_t)k] * load_widened(dtype, y[k], i);\n                acc = acc + p;",
+                                   "                acc = fmaf(w[t * (size_t)K + (size_t)k], load_widened(dtype, y[k], i), acc);"),
+    "combine_weights_transposed": ("float p = w[t * (size_t)K + (size_t)k]", "float p = w[(size_t)k * T + t]"),
     "flag_in_low_half": ("pkts[p] = ((uint64_t)flag << 32) | (uint64_t)payload;",
                          "pkts[p] = ((uint64_t)payload << 32) | (uint64_t)flag;"),
 }
@@ -82,6 +85,21 @@ def _pins_pass(lib) -> bool:
         ok = ~np.isnan(ref)
         if not np.array_equal(w[ok].view(np.uint32), ref[ok].view(np.uint32)):
             return False
+    # weighted combine: hand-derived cases and power-of-two weights
+    for case in golden("combine_cases.json")["cases"]:
+        dt = case["dtype"]
+        ys = [hex_array([h], dt) for h in case["y"]]
+        w = np.array([int(x, 16) for x in case["w"]], dtype=np.uint32).view(np.float32)
+        if int(as_uint(oracle.combine(ys, w, 1, 1, DT_CODE[dt], lib=lib), dt)[0]) != int(case["expected"], 16):
+            return False
+    ys = [wl.bits(t) for t in wl.make_inputs(88, 3, 4 * 8, "fp32", "uniform")]
+    e = np.array([[0, 1, 2], [3, -1, 0], [1, 1, -2], [2, 0, 1]])
+    scaled = [(ys[k].reshape(4, 8).astype(np.float64) * np.ldexp(1.0, e[:, k])[:, None])
+              .astype(np.float32).reshape(-1) for k in range(3)]
+    want = oracle.allreduce(scaled, DT_CODE["fp32"], lib=lib)[0]
+    got = oracle.combine(ys, np.ldexp(1.0, e).astype(np.float32).reshape(-1), 4, 8, DT_CODE["fp32"], lib=lib)
+    if not np.array_equal(got.view(np.uint32), want.view(np.uint32)):
+        return False
     # packets
     for case in golden("ll_packets.json")["cases"]:
         dt = case["dtype"]
