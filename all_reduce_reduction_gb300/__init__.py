@@ -102,6 +102,7 @@ SIGNATURES = {
     "ar_allreduce": ([_VP, _VPP, _VPP, _I, _I, _VP], _I),
     "ar_allreduce_n": ([_VP, _VPP, _VPP, _SZ, _I, _I, _VP], _I),
     "ar_tune": ([_VP, _VP], _I),
+    "ar_combine": ([_VP, _VPP, _VP, _VP, _SZ, _SZ, _VP], _I),
     "ar_get_tuning": ([_VP, _SZ, ctypes.POINTER(_I), ctypes.POINTER(_I),
                        ctypes.POINTER(ctypes.c_float)], _I),
     "ar_reduce_scatter": ([_VP, _VPP, _VPP, _VP], _I),
@@ -199,6 +200,11 @@ def ar_allreduce_n(h: int, ins, outs, n: int, algo=AR_ALGO_AUTO, proto=AR_PROTO_
     proto = PROTOS[proto] if isinstance(proto, str) else proto
     _check(load_library().ar_allreduce_n(h, _ptr_array(ins), _ptr_array(outs), n, algo, proto,
                                          _stream(stream)), "ar_allreduce_n")
+
+
+def ar_combine(h: int, ys, w, out, T: int, H: int, stream=None) -> None:
+    _check(load_library().ar_combine(h, _ptr_array(ys), _ptr(w), _ptr(out), T, H,
+                                      _stream(stream)), "ar_combine")
 
 
 def ar_tune(h: int, stream=None) -> None:
@@ -304,7 +310,7 @@ def ar_plan_compile(h: int, ops, nchunks: int, ctas_per_rank: int = 1) -> int:
     return p.value
 
 
-def ar_plan_builtin(h: int, algo, chunks_per_rank: int = 4, ctas_per_rank: int = 4) -> int:
+def ar_plan_builtin(h: int, algo, chunks_per_rank: int = 0, ctas_per_rank: int = 0) -> int:
     algo = ALGOS[algo] if isinstance(algo, str) else algo
     p = ctypes.c_void_p()
     _check(load_library().ar_plan_builtin(h, algo, chunks_per_rank, ctas_per_rank,

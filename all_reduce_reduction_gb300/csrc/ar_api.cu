@@ -509,6 +509,42 @@ int ar_all_gather(ar_handle_t h, void *const out[], cudaStream_t stream) {
     return from_cuda(launch_all_gather(a, h->dtype, c.vec16, grid, stream, h->pdl));
 }
 
+int ar_combine(ar_handle_t h, const void *const y[], const float *w, void *out, size_t T,
+               size_t H, cudaStream_t stream) {
+    if (!h || !y || !w || !out || T < 1 || H < 1 || !on_device(h))
+        return AR_ERR_INVALID;
+    if (T > h->N / H)
+        return AR_ERR_INVALID;                       // T * H elements must fit the handle
+    const int K = h->R;
+    const size_t len = T * H * h->esz;
+    const uintptr_t o = (uintptr_t)out, wb = (uintptr_t)w;
+    const size_t wlen = T * (size_t)K * sizeof(float);
+    if ((o % h->esz) != 0 || (wb % 4) != 0 || (o < wb + wlen && wb < o + len))
+        return AR_ERR_INVALID;                       // misaligned, or out overlaps w
+    uintptr_t all = o;
+    for (int k = 0; k < K; ++k) {
+        const uintptr_t a = (uintptr_t)y[k];
+        if (!y[k] || (a % h->esz) != 0)
+            return AR_ERR_INVALID;
+        if (ranges_overlap(a, o, len) && a != o)
+            return AR_ERR_INVALID;                   // out may only be a source exactly
+        all |= a;
+    }
+    const bool vec = (all & 15u) == 0 && (H * h->esz) % 16 == 0;
+    CombineArgs a;
+    for (int r = 0; r < AR_MAX_RANKS; ++r) {
+        a.p.in[r] = r < K ? y[r] : nullptr;
+        a.p.out[r] = r == 0 ? out : nullptr;
+    }
+    a.w = w;
+    a.T = T;
+    a.H = H;
+    a.K = K;
+    const uint64_t units = vec ? T * (H / (16 / h->esz)) : T * H;
+    const int grid = clamp_grid(ceil_div(units, kRegThreads), h->reg_cap);
+    return from_cuda(launch_combine(a, h->dtype, vec, grid, stream, h->pdl));
+}
+
 int ar_tune(ar_handle_t h, cudaStream_t stream) {
     if (!h || !on_device(h))
         return AR_ERR_INVALID;

@@ -113,6 +113,14 @@ struct LlClusterArgs {
 constexpr int kLlClusterMaxSmem = 96 * 1024;
 constexpr int kLlClusterTargetSmem = 64 * 1024;
 
+// Weighted per-token combine: K sources in p.in[0..K-1], the output in p.out[0].
+struct CombineArgs {
+    RankPtrs p;
+    const float *w;          // T x K weights, row-major
+    uint64_t T, H;           // tokens, elements per token
+    int K;
+};
+
 // Standalone packet encode/decode and rounding.
 struct PackArgs {
     const void *src;
@@ -153,6 +161,10 @@ cudaError_t launch_pack(const PackArgs &a, int dtype, bool vec, int grid, cudaSt
                         bool pdl = false);
 cudaError_t launch_unpack(const PackArgs &a, int dtype, bool vec, int grid, cudaStream_t s,
                           bool pdl = false);
+
+// ar_combine.cu
+cudaError_t launch_combine(const CombineArgs &a, int dtype, bool vec, int grid, cudaStream_t s,
+                           bool pdl = false);
 
 // ar_ll_cluster.cu
 size_t ll_cluster_smem_bytes(int R, uint64_t units_per_chunk);

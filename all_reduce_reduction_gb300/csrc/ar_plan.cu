@@ -234,6 +234,22 @@ struct ar_plan {
 
 namespace {
 
+// CTAs per rank that fill the device's co-resident capacity.
+int plan_ctas_per_rank(int R, int dtype) {
+    int per_sm = 0, dev = 0, sms = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, plan_kernel_for(dtype),
+                                                      kRegThreads, 0) != cudaSuccess) {
+        (void)cudaGetLastError();
+        return 0;
+    }
+    int g = per_sm * sms / R;
+    if (g > kEpochWords / R)
+        g = kEpochWords / R;
+    return g;
+}
+
 struct Task {
     int step, chunk, cta;
     std::vector<int> deps;   // producer tasks in other CTAs
@@ -251,9 +267,15 @@ extern "C" int ar_plan_compile(ar_handle_t h, const ar_op *ops, int nops, int nc
     if (!out)
         return AR_ERR_INVALID;
     *out = nullptr;
-    if (!h || !ops || nops < 1 || nchunks < 1 || ctas_per_rank < 1 ||
+    if (!h || !ops || nops < 1 || nchunks < 1 || ctas_per_rank < 0 ||
         ar_get_info(h, &info) != AR_OK)
         return AR_ERR_INVALID;
+    if (ctas_per_rank == 0) {
+        // as many CTAs per rank as can be resident together
+        ctas_per_rank = plan_ctas_per_rank(info.R, info.dtype);
+        if (ctas_per_rank < 1)
+            return AR_ERR_UNSUPPORTED;
+    }
     const int R = info.R;
     for (int k = 0; k < nops; ++k) {
         const ar_op &o = ops[k];
@@ -267,8 +289,6 @@ extern "C" int ar_plan_compile(ar_handle_t h, const ar_op *ops, int nops, int nc
             if (o.src_rank[i] < 0 || o.src_rank[i] >= R)
                 return AR_ERR_INVALID;
     }
-    const int G = ctas_per_rank;
-    const int ctas = R * G;
     int per_sm = 0, dev = 0, sms = 0;
     if (cudaGetDevice(&dev) != cudaSuccess ||
         cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
@@ -277,6 +297,8 @@ extern "C" int ar_plan_compile(ar_handle_t h, const ar_op *ops, int nops, int nc
         (void)cudaGetLastError();
         return AR_ERR_CUDA;
     }
+    const int G = ctas_per_rank;
+    const int ctas = R * G;
     if (ctas > per_sm * sms || ctas > kEpochWords)
         return AR_ERR_UNSUPPORTED;                       // not all CTAs can be resident
 
@@ -407,9 +429,15 @@ extern "C" int ar_plan_compile(ar_handle_t h, const ar_op *ops, int nops, int nc
 extern "C" int ar_plan_builtin(ar_handle_t h, int algo, int chunks_per_rank, int ctas_per_rank,
                                ar_plan_t *out) {
     ar_info info;
-    if (!out || !h || ar_get_info(h, &info) != AR_OK || chunks_per_rank < 1 ||
-        (algo != AR_ONE_SHOT && algo != AR_TWO_SHOT))
+    if (!out || !h || ar_get_info(h, &info) != AR_OK || chunks_per_rank < 0 ||
+        ctas_per_rank < 0 || (algo != AR_ONE_SHOT && algo != AR_TWO_SHOT))
         return AR_ERR_INVALID;
+    if (ctas_per_rank == 0)
+        ctas_per_rank = plan_ctas_per_rank(info.R, info.dtype);
+    if (ctas_per_rank < 1)
+        return AR_ERR_UNSUPPORTED;
+    if (chunks_per_rank == 0)
+        chunks_per_rank = ctas_per_rank;     // one chunk per CTA and step
     const int R = info.R, K = chunks_per_rank;
     std::vector<ar_op> ops;
     ar_op o = {};

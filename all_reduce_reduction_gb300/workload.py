@@ -135,6 +135,44 @@ class Workload:
         return make_inputs(self.config, self.R, self.n, self.dtype, self.dist, threads)
 
 
+def gate_weights(seed: int, T: int, K: int) -> np.ndarray:
+    """Per-token gate weights: K draws in (0, 1] per token, divided by their
+    token's sum in binary64 and cast to binary32 (row-major T x K)."""
+    u = 1.0 - _unit(splitmix64(seed, np.arange(T * K, dtype=np.uint64))).reshape(T, K)
+    return (u / u.sum(axis=1, keepdims=True)).astype(np.float32).reshape(-1)
+
+
+@dataclass(frozen=True)
+class CombineWorkload:
+    """Weighted per-token combine: K sources of T tokens x H elements."""
+    config: int
+    name: str
+    K: int
+    T: int
+    H: int
+    dtype: str
+    dist: str
+
+    @property
+    def R(self) -> int:          # sources, as "ranks"
+        return self.K
+
+    @property
+    def n(self) -> int:          # elements per source
+        return self.T * self.H
+
+    def inputs(self, threads: int = 0) -> list[torch.Tensor]:
+        return make_inputs(self.config, self.K, self.T * self.H, self.dtype, self.dist, threads)
+
+    def weights(self) -> np.ndarray:
+        return gate_weights(seed_for(self.config, 1000), self.T, self.K)
+
+
+# The combine workloads: K = 8 sources (top-8 experts), hidden 8192, decode
+# batches of 1..128 tokens and one prefill-sized batch of 4096 tokens.
+COMBINE = [CombineWorkload(5, "k8_combine_t%d_h8192_bf16_normal" % t, 8, t, 8192, "bf16", "normal")
+           for t in (1, 16, 128, 4096)]
+
 # The five workloads.
 SMALL = Workload(0, "r8_n512_bf16_uniform", 8, 512, "bf16", "uniform")
 LL_SWEEP = [Workload(1, "r8_ll_sweep_n%d_bf16_uniform" % (1 << i), 8, 1 << i, "bf16", "uniform")

@@ -66,6 +66,11 @@ def workload_cases(name: str, args=None):
         cases = [dict(w=w, algo="auto", proto="auto", calls=10, flush=True) for w in wl.DECODE]
         desc = ("r8_bf16_decode: R=8, bf16 [B, 8192] for B in 1,8,32,128,256, N(0,1), "
                 "AUTO (tuned) schedule and protocol, 10 calls per CUDA graph")
+    elif name == "combine":
+        cases = [dict(w=w, combine=True, algo="combine", proto="hb", calls=10,
+                      flush=True) for w in wl.COMBINE]
+        desc = ("k8_bf16_combine: weighted per-token combine of K=8 sources, T in 1,16,128,4096 "
+                "tokens x H=8192 bf16, N(0,1) values, normalised gate weights; 10 calls per graph")
     elif name == "prefill":
         cases = [dict(w=wl.PREFILL, algo="two_shot", proto="hb", calls=1, flush=False)]
         desc = ("r16_bf16_prefill: R=16, bf16 [8192, 8192] per rank (128 MiB), N(0,1), "
@@ -81,8 +86,12 @@ def workload_cases(name: str, args=None):
 
 
 def case_bytes(c) -> int:
+    """Minimal bytes of one call: every input byte read once, every output
+    byte written once (combine: K sources + the weights + one output)."""
     w = c["w"]
     from all_reduce_reduction_gb300 import workload as wl
+    if c.get("combine"):
+        return (w.K + 1) * w.T * w.H * wl.ELEM_SIZE[w.dtype] + 4 * w.T * w.K
     return 2 * w.R * w.n * wl.ELEM_SIZE[w.dtype]
 
 
@@ -264,12 +273,17 @@ class CaseRunner:
         w = self.w
         self.cpu_inputs = w.inputs(threads=16)
         self.ins = [t.cuda() for t in self.cpu_inputs]
-        self.outs = [torch.empty_like(t) for t in self.ins]
-        self.h = ar.Handle(w.R, w.n, w.dtype)
+        if c.get("combine"):
+            self.weights = torch.from_numpy(w.weights()).cuda()
+            self.outs = [torch.empty_like(self.ins[0])]
+            self.h = ar.Handle(w.K, w.T * w.H, w.dtype)
+        else:
+            self.outs = [torch.empty_like(t) for t in self.ins]
+            self.h = ar.Handle(w.R, w.n, w.dtype)
         ar.ar_set_ll_transport(self.h.h, c.get("transport", ar.AR_LL_AUTO))
         ar.ar_set_pdl(self.h.h, c.get("pdl", 1))
-        self.algo, self.proto = ar.ALGOS[c["algo"]], ar.PROTOS[c["proto"]]
-        self.choice = None
+        self.algo, self.proto = ar.ALGOS.get(c["algo"], 0), ar.PROTOS[c["proto"]]
+        self.choice = "combine" if c.get("combine") else None
         if c["algo"] == "auto" or c["proto"] == "auto":
             ar.ar_tune(self.h.h, stream)
             a, p, _ = ar.ar_get_tuning(self.h.h, w.n * wl.ELEM_SIZE[w.dtype])
@@ -278,11 +292,14 @@ class CaseRunner:
         self.plan = None
         if c.get("plan"):
             # the same all-reduce as a compiled plan run by the interpreter kernel
-            self.plan = ar.ar_plan_builtin(self.h.h, c["plan"], c.get("plan_chunks", 4),
-                                           c.get("plan_ctas", 4))
+            self.plan = ar.ar_plan_builtin(self.h.h, c["plan"], c.get("plan_chunks", 0),
+                                           c.get("plan_ctas", 0))
 
         def call():
-            if self.plan:
+            if c.get("combine"):
+                ar.ar_combine(self.h.h, self.ins, self.weights, self.outs[0], w.T, w.H,
+                              stream=stream)
+            elif self.plan:
                 ar.ar_plan_execute(self.plan, self.ins, self.outs, stream=stream)
             else:
                 ar.ar_allreduce(self.h.h, self.ins, self.outs, self.algo, self.proto,
@@ -531,13 +548,19 @@ def cpu_baseline(runners, seconds: float):
         ins = [wl.bits(t) for t in r.cpu_inputs]
         if r.w.n > (1 << 22):           # large messages: a leading slice of every rank
             ins = [a[: 1 << 22].copy() for a in ins]
-        sample.append(ins)
+        sample.append((r, ins))
     done_bytes, t0 = 0, time.perf_counter()
     passes = 0
     while True:
-        for ins in sample:
-            oracle.allreduce(ins, wl.DTYPE_CODE[runners[0].w.dtype], lib=lib)
-            done_bytes += 2 * len(ins) * ins[0].nbytes
+        for r, ins in sample:
+            dt = wl.DTYPE_CODE[r.w.dtype]
+            if r.c.get("combine"):
+                T = ins[0].size // r.w.H
+                oracle.combine(ins, r.w.weights()[: T * r.w.K], T, r.w.H, dt, lib=lib)
+                done_bytes += (len(ins) + 1) * ins[0].nbytes + 4 * T * r.w.K
+            else:
+                oracle.allreduce(ins, dt, lib=lib)
+                done_bytes += 2 * len(ins) * ins[0].nbytes
         passes += 1
         if time.perf_counter() - t0 >= seconds:
             break
@@ -561,15 +584,23 @@ def run_reference(args, world: int):
     for c in cases:
         w = c["w"]
         n = min(w.n, 1 << 20)
+        if c.get("combine"):
+            n = min(w.T, max(1, (1 << 20) // w.H)) * w.H
         ins = [wl.bits(t) for t in wl.make_inputs(w.config, w.R, n, w.dtype, w.dist)]
-        sample.append(ins)
+        sample.append((c, ins))
     dt_code = wl.DTYPE_CODE[cases[0]["w"].dtype]
 
     def step():
         b = 0
-        for ins in sample:
-            oracle.allreduce(ins, dt_code, lib=lib)
-            b += 2 * len(ins) * ins[0].nbytes
+        for c, ins in sample:
+            if c.get("combine"):
+                w = c["w"]
+                T = ins[0].size // w.H
+                oracle.combine(ins, w.weights()[: T * w.K], T, w.H, dt_code, lib=lib)
+                b += (len(ins) + 1) * ins[0].nbytes + 4 * T * w.K
+            else:
+                oracle.allreduce(ins, dt_code, lib=lib)
+                b += 2 * len(ins) * ins[0].nbytes
         return b
 
     for _ in range(args.warmup):
@@ -605,7 +636,7 @@ def main():
     p.add_argument("--steps", type=int, default=1000)
     p.add_argument("--warmup", type=int, default=10)
     p.add_argument("--workload", default="sweep",
-                   choices=["sweep", "decode", "prefill", "edge", "custom"])
+                   choices=["sweep", "decode", "prefill", "edge", "combine", "custom"])
     # --workload custom: one case (used for profiling single kernels)
     p.add_argument("--R", type=int, default=8)
     p.add_argument("--n", type=int, default=1 << 18)
@@ -615,8 +646,8 @@ def main():
     p.add_argument("--calls", type=int, default=10)
     p.add_argument("--plan", default=None, choices=["one_shot", "two_shot"],
                    help="custom workload: run the built-in plan of that algorithm")
-    p.add_argument("--plan-chunks", type=int, default=4)
-    p.add_argument("--plan-ctas", type=int, default=4)
+    p.add_argument("--plan-chunks", type=int, default=0, help="0: one chunk per CTA")
+    p.add_argument("--plan-ctas", type=int, default=0, help="0: fill the resident capacity")
     p.add_argument("--ll-transport", default="auto", choices=["auto", "global", "cluster"])
     p.add_argument("--no-pdl", action="store_true",
                    help="launch without programmatic dependent launch")

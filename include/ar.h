@@ -221,6 +221,21 @@ int ar_tune(ar_handle_t h, cudaStream_t stream);
  * one-shot LL, one-shot HB, two-shot LL, two-shot HB (0 = not timed). */
 int ar_get_tuning(ar_handle_t h, size_t bytes, int *algo, int *proto, float us[4]);
 
+/* Weighted per-token combine ("NCCL EP统一MoE通信生态", section 3.1 and
+ * Table III: the low-latency mode reduces each token at the receiver with a
+ * weight per expert).  With K = the handle's R sources:
+ *   out[t*H + h] = round_dtype( fold over k = 0..K-1 of w[t*K + k] * y[k][t*H + h] )
+ * every product rounded to binary32 on its own (no fused multiply-add), the
+ * products folded left to right from k = 0, one final rounding.
+ *   y:   host array of K device pointers, T*H elements each (row-major).
+ *   w:   device pointer, T*K binary32 weights (row-major), 4-byte aligned.
+ *   out: device pointer, T*H elements; may be one of the y[k] exactly,
+ *        otherwise must not overlap them or w.
+ *   T*H <= the handle's N.  16-byte aligned buffers with H*elem_size a
+ *   multiple of 16 take the vector path.  Errors: AR_ERR_INVALID. */
+int ar_combine(ar_handle_t h, const void *const y[], const float *w, void *out, size_t T,
+               size_t H, cudaStream_t stream);
+
 /* Reduce-scatter step of the two-shot schedule (HB): for every shard j,
  *   out[j][i] = round_dtype(fold of in[0..R-1][i])  for i in shard j,
  * and nothing else is written.  Shards as in enum ar_algo.  Arguments,
@@ -350,12 +365,16 @@ typedef struct ar_plan *ar_plan_t;
  * ctas_per_rank CTAs cannot all be resident), AR_ERR_NOMEM, AR_ERR_CUDA. */
 int ar_plan_compile(ar_handle_t h, const ar_op *ops, int nops, int nchunks,
                     int ctas_per_rank, ar_plan_t *out);
+/* (ctas_per_rank == 0: as many as can be resident together, R * that <= the
+ * device's capacity for the interpreter kernel.) */
 
 /* The two all-reduce algorithms as plans, with chunks_per_rank * R chunks:
  *   AR_ONE_SHOT: rank r reduces every input into out[r];
  *   AR_TWO_SHOT: rank j reduces shard j (chunks [j*K, (j+1)*K)) into out[j],
  *                then every rank copies every other shard into its output.
- * Same results as ar_allreduce.  Errors as ar_plan_compile. */
+ * Same results as ar_allreduce.  chunks_per_rank == 0 picks ctas_per_rank
+ * chunks; ctas_per_rank == 0 fills the resident capacity.  Errors as
+ * ar_plan_compile. */
 int ar_plan_builtin(ar_handle_t h, int algo, int chunks_per_rank, int ctas_per_rank,
                     ar_plan_t *out);
 

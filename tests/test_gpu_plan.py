@@ -117,3 +117,22 @@ def test_plan_misaligned_buffers_and_rejections():
         with pytest.raises(ar.ArError):                  # chunk range beyond nchunks
             ar.ar_plan_compile(h.h, [bad], 4, 1)
         ar.ar_plan_destroy(p)
+
+
+@pytest.mark.parametrize("algo", ["one_shot", "two_shot"])
+def test_builtin_plan_fills_the_gpu_by_default(algo):
+    need_gpu()
+    R, n, dtype = 8, (1 << 19) + 3, "bf16"
+    cpu = wl.make_inputs(86, R, n, dtype, "uniform")
+    ins = device_inputs(cpu)
+    outs = _outs(R, n, dtype)
+    with ar.Handle(R, n, dtype) as h:
+        p = ar.ar_plan_builtin(h.h, algo)                # chunks and CTAs chosen by the library
+        tasks, _, _ = ar.ar_plan_stats(p)
+        assert tasks >= R * 8                            # at least a few CTAs' worth per rank
+        ar.ar_plan_execute(p, ins, outs)
+        assert ar.ar_status(h.h) == ar.AR_OK
+        ar.ar_plan_destroy(p)
+    want = expected(cpu, dtype)
+    for r in range(R):
+        assert_bits_equal(outs[r], want, dtype, "rank %d" % r)
