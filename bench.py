@@ -318,7 +318,7 @@ class CaseRunner:
         if ar.ar_status(self.h.h) != ar.AR_OK:
             raise RuntimeError("device status after warm-up: " + ar.ar_strerror(ar.ar_status(self.h.h)))
         self.pinned_in = [t.pin_memory() for t in self.cpu_inputs]
-        self.pinned_out = [torch.empty_like(t).pin_memory() for t in self.cpu_inputs]
+        self.pinned_out = [torch.empty(o.shape, dtype=o.dtype).pin_memory() for o in self.outs]
 
     def close(self):
         import all_reduce_reduction_gb300 as ar
