@@ -44,7 +44,7 @@ __device__ __forceinline__ void st_v2(void *p, uint2 v) {
 // 0..R-1, in rank order.  Loads of eight ranks are issued before any flag is
 // checked, so a ready message costs one round trip per eight ranks.
 template <int DT>
-__device__ __forceinline__ bool fold_pair(Poller &w, const uint64_t *base, uint64_t ppad, int R,
+__device__ __forceinline__ bool fold_pair(Poller &w, const uint64_t *base, uint32_t ppad, int R,
                                           uint2 &out) {
     WordAcc<DT> a0, a1;
 #pragma unroll 1
@@ -53,12 +53,12 @@ __device__ __forceinline__ bool fold_pair(Poller &w, const uint64_t *base, uint6
 #pragma unroll
         for (int j = 0; j < 8; ++j)
             if (k0 + j < R)
-                ld_pkt2(base + (uint64_t)(k0 + j) * ppad, p0[j], p1[j]);
+                ld_pkt2(base + (uint32_t)(k0 + j) * ppad, p0[j], p1[j]);
 #pragma unroll
         for (int j = 0; j < 8; ++j) {
             if (k0 + j < R) {
                 if (pkt_flag(p0[j]) != w.flag || pkt_flag(p1[j]) != w.flag) {
-                    if (!poll_pkt2(w, base + (uint64_t)(k0 + j) * ppad, p0[j], p1[j]))
+                    if (!poll_pkt2(w, base + (uint32_t)(k0 + j) * ppad, p0[j], p1[j]))
                         return false;
                 }
                 if (k0 + j == 0) {
@@ -77,7 +77,7 @@ __device__ __forceinline__ bool fold_pair(Poller &w, const uint64_t *base, uint6
 
 // Same for a single packet.
 template <int DT>
-__device__ __forceinline__ bool fold_one(Poller &w, const uint64_t *base, uint64_t ppad, int R,
+__device__ __forceinline__ bool fold_one(Poller &w, const uint64_t *base, uint32_t ppad, int R,
                                          uint32_t &out) {
     WordAcc<DT> acc;
 #pragma unroll 1
@@ -86,11 +86,11 @@ __device__ __forceinline__ bool fold_one(Poller &w, const uint64_t *base, uint64
 #pragma unroll
         for (int j = 0; j < 8; ++j)
             if (k0 + j < R)
-                p[j] = ld_pkt(base + (uint64_t)(k0 + j) * ppad);
+                p[j] = ld_pkt(base + (uint32_t)(k0 + j) * ppad);
 #pragma unroll
         for (int j = 0; j < 8; ++j) {
             if (k0 + j < R) {
-                if (pkt_flag(p[j]) != w.flag && !poll_pkt(w, base + (uint64_t)(k0 + j) * ppad, p[j]))
+                if (pkt_flag(p[j]) != w.flag && !poll_pkt(w, base + (uint32_t)(k0 + j) * ppad, p[j]))
                     return false;
                 if (k0 + j == 0)
                     acc.init(pkt_payload(p[j]));
@@ -111,23 +111,23 @@ __global__ void __launch_bounds__(kLlThreads) k_ll(const __grid_constant__ LlArg
     constexpr int ESZ = Elem<DT>::kSize;
     const int R = a.R, G = a.G;
     const int r = blockIdx.x % R, gi = blockIdx.x / R;
-    const uint64_t tid = threadIdx.x, T = blockDim.x;
+    const uint32_t tid = threadIdx.x, T = blockDim.x;
     kernel_prologue();
     const uint32_t flag = call_flag(a.c);
     Poller w{&a.c, flag, 0};
 
-    const uint64_t nbytes = a.n * ESZ;
-    const uint64_t P = (nbytes + 3) / 4;                  // packets per rank
-    const uint64_t U = nbytes / 8;                        // packet pairs (VEC)
-    const uint64_t first1 = VEC ? 2 * U : 0;              // first single packet
+    const uint32_t nbytes = (uint32_t)a.n * ESZ;
+    const uint32_t P = (nbytes + 3) / 4;                  // packets per rank
+    const uint32_t U = nbytes / 8;                        // packet pairs (VEC)
+    const uint32_t first1 = VEC ? 2 * U : 0;              // first single packet
     // this thread's single packets (same set in every phase that uses them)
-    const uint64_t q0 = VEC ? (gi == 0 ? first1 + tid : P) : (uint64_t)gi * T + tid;
-    const uint64_t qstep = VEC ? T : (uint64_t)G * T;
-    const uint64_t ustart = (uint64_t)gi * T + tid, ustep = (uint64_t)G * T;
+    const uint32_t q0 = VEC ? (gi == 0 ? first1 + tid : P) : (uint32_t)gi * T + tid;
+    const uint32_t qstep = VEC ? T : (uint32_t)G * T;
+    const uint32_t ustart = (uint32_t)gi * T + tid, ustep = (uint32_t)G * T;
 
-    const uint64_t ppad = a.ppad;
-    uint64_t *const slot_r = a.slots + (uint64_t)r * ppad;
-    uint64_t *const res = a.slots + (uint64_t)R * ppad;   // two-shot results
+    const uint32_t ppad = (uint32_t)a.ppad;
+    uint64_t *const slot_r = a.slots + (uint32_t)r * ppad;
+    uint64_t *const res = a.slots + (uint32_t)R * ppad;   // two-shot results
     bool ok = true;
 
     // ---- put: rank r's input -> slot r (one 8-byte store per packet) -------
@@ -136,7 +136,7 @@ __global__ void __launch_bounds__(kLlThreads) k_ll(const __grid_constant__ LlArg
             // four units' loads are in flight before the first packet store
             constexpr int kPut = 4;
             const uint2 *src = reinterpret_cast<const uint2 *>(a.p.in[r]);
-            for (uint64_t u0 = ustart; u0 < U; u0 += kPut * ustep) {
+            for (uint32_t u0 = ustart; u0 < U; u0 += kPut * ustep) {
                 uint2 v[kPut];
 #pragma unroll
                 for (int j = 0; j < kPut; ++j)
@@ -144,13 +144,13 @@ __global__ void __launch_bounds__(kLlThreads) k_ll(const __grid_constant__ LlArg
                         v[j] = ld_v2(src + u0 + j * ustep);
 #pragma unroll
                 for (int j = 0; j < kPut; ++j) {
-                    const uint64_t u = u0 + j * ustep;
+                    const uint32_t u = u0 + j * ustep;
                     if (u < U)
                         st_pkt2(slot_r + 2 * u, make_pkt(v[j].x, flag), make_pkt(v[j].y, flag));
                 }
             }
         }
-        for (uint64_t q = q0; q < P; q += qstep)
+        for (uint32_t q = q0; q < P; q += qstep)
             st_pkt(slot_r + q, make_pkt(load_payload<ESZ>(a.p.in[r], a.n, q), flag));
     }
 
@@ -158,14 +158,14 @@ __global__ void __launch_bounds__(kLlThreads) k_ll(const __grid_constant__ LlArg
         // ---- one-shot: out[r] = fold of every slot -------------------------
         if constexpr (VEC) {
             uint2 *dst = reinterpret_cast<uint2 *>(a.p.out[r]);
-            for (uint64_t u = ustart; ok && u < U; u += ustep) {
+            for (uint32_t u = ustart; ok && u < U; u += ustep) {
                 uint2 y;
                 ok = fold_pair<DT>(w, a.slots + 2 * u, ppad, R, y);
                 if (ok)
                     st_v2(dst + u, y);
             }
         }
-        for (uint64_t q = q0; ok && q < P; q += qstep) {
+        for (uint32_t q = q0; ok && q < P; q += qstep) {
             uint32_t y;
             ok = fold_one<DT>(w, a.slots + q, ppad, R, y);
             if (ok)
@@ -173,13 +173,13 @@ __global__ void __launch_bounds__(kLlThreads) k_ll(const __grid_constant__ LlArg
         }
     } else {
         // ---- reduce-scatter: rank r folds shard r into result packets ------
-        const uint64_t shard_pk = a.shard * ESZ / 4;      // packets per shard
+        const uint32_t shard_pk = (uint32_t)(a.shard * ESZ / 4);   // packets per shard
         if constexpr (VEC) {
-            const uint64_t lo = (uint64_t)r * shard_pk / 2;
-            uint64_t hi = lo + shard_pk / 2;
+            const uint32_t lo = (uint32_t)r * (shard_pk / 2);
+            uint32_t hi = lo + shard_pk / 2;
             if (hi > U)
                 hi = U;
-            for (uint64_t u = lo + ustart; ok && u < hi; u += ustep) {
+            for (uint32_t u = lo + ustart; ok && u < hi; u += ustep) {
                 uint2 y;
                 ok = fold_pair<DT>(w, a.slots + 2 * u, ppad, R, y);
                 if (ok)
@@ -187,7 +187,7 @@ __global__ void __launch_bounds__(kLlThreads) k_ll(const __grid_constant__ LlArg
             }
             // single packets belong to the shard that holds them
             if (gi == 0) {
-                for (uint64_t q = first1 + tid; ok && q < P; q += T) {
+                for (uint32_t q = first1 + tid; ok && q < P; q += T) {
                     int owner = (int)(q / shard_pk);
                     if (owner > R - 1)
                         owner = R - 1;
@@ -200,11 +200,11 @@ __global__ void __launch_bounds__(kLlThreads) k_ll(const __grid_constant__ LlArg
                 }
             }
         } else {
-            const uint64_t lo = (uint64_t)r * shard_pk;
-            uint64_t hi = lo + shard_pk;
+            const uint32_t lo = (uint32_t)r * shard_pk;
+            uint32_t hi = lo + shard_pk;
             if (hi > P)
                 hi = P;
-            for (uint64_t q = lo + ustart; ok && q < hi; q += ustep) {
+            for (uint32_t q = lo + ustart; ok && q < hi; q += ustep) {
                 uint32_t y;
                 ok = fold_one<DT>(w, a.slots + q, ppad, R, y);
                 if (ok)
@@ -214,14 +214,14 @@ __global__ void __launch_bounds__(kLlThreads) k_ll(const __grid_constant__ LlArg
         // ---- all-gather: out[r] <- result packets (same units as the put) --
         if constexpr (VEC) {
             uint2 *dst = reinterpret_cast<uint2 *>(a.p.out[r]);
-            for (uint64_t u = ustart; ok && u < U; u += ustep) {
+            for (uint32_t u = ustart; ok && u < U; u += ustep) {
                 uint64_t p0, p1;
                 ok = poll_pkt2(w, res + 2 * u, p0, p1);
                 if (ok)
                     st_v2(dst + u, make_uint2(pkt_payload(p0), pkt_payload(p1)));
             }
         }
-        for (uint64_t q = q0; ok && q < P; q += qstep) {
+        for (uint32_t q = q0; ok && q < P; q += qstep) {
             uint64_t p;
             ok = poll_pkt(w, res + q, p);
             if (ok)
