@@ -343,6 +343,11 @@ def run_ours(args, dist: Dist):
 
     torch.cuda.set_device(dist.local_rank)
     desc, cases = workload_cases(args.workload, args)
+    if args.only:
+        cases = [c for c in cases if c["w"].n == args.only]
+        if not cases:
+            raise SystemExit("--only %d matches no case of the workload" % args.only)
+        desc += " (only the case of %d elements per rank)" % args.only
     for c in cases:
         c["transport"] = TRANSPORTS[args.ll_transport]
         c["pdl"] = 0 if args.no_pdl else 1
@@ -661,6 +666,8 @@ def main():
                    help="launch without programmatic dependent launch")
     p.add_argument("--impl", default="ours", choices=["ours", "reference"])
     p.add_argument("--cpu-seconds", type=float, default=10.0)
+    p.add_argument("--only", type=int, default=0,
+                   help="run only the workload's case with this many elements per rank")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-variants", action="store_true")
     args = p.parse_args()
