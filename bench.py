@@ -226,6 +226,7 @@ KERNEL_SOURCES = {
     "one_shot_ll_cluster": ["ar_ll_cluster.cu"],
     "one_shot_hb": ["ar_hb.cu"],
     "two_shot_hb": ["ar_tma.cu"],
+    "combine": ["ar_combine.cu"],
 }
 
 
