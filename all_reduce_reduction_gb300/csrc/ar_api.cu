@@ -163,9 +163,10 @@ int one_shot_hb(ar_handle *h, const Call &c) {
     const HbArgs a = hb_args(h, c);
     const uint64_t units = c.vec16 ? c.n / (16 / h->esz) : c.n;
     const uint64_t per_blk = (uint64_t)(h->one_shot_warps / h->R) * 32;
-    const int grid = clamp_grid(ceil_div(units, per_blk), h->one_shot_cap);
-    return from_cuda(
-        launch_one_shot_hb(a, h->dtype, c.vec16, grid, 32 * h->one_shot_warps, c.s, h->pdl));
+    const uint64_t runs = ceil_div(units, per_blk);
+    const int grid = clamp_grid(runs, h->one_shot_cap);
+    return from_cuda(launch_one_shot_hb(a, h->dtype, c.vec16, runs <= (uint64_t)grid, grid,
+                                        32 * h->one_shot_warps, c.s, h->pdl));
 }
 
 int two_shot_hb(ar_handle *h, const Call &c) {
@@ -377,6 +378,7 @@ int ar_create(int R, size_t N, int dtype, ar_handle_t *out) {
         }
     h->one_shot_warps = R <= 8 ? R * ((8 + R - 1) / R) : R;
     h->one_shot_cap = h->num_sms * (2048 / (32 * h->one_shot_warps));
+    err |= one_shot_prepare() != cudaSuccess;
     h->reg_cap = h->num_sms * (2048 / kRegThreads);
     int smem_limit = 0;
     err |= tma_prepare(dtype, &smem_limit) != cudaSuccess;
@@ -395,15 +397,16 @@ int ar_create(int R, size_t N, int dtype, ar_handle_t *out) {
     h->tma_tile = tile;
     h->tma_stages = stages;
 
-    // cluster LL: one CTA per virtual rank in a cluster (portable up to 8,
-    // 16 with the non-portable size); receive buffers of ~64 KiB per CTA
-    h->tuned_max = -1;
+    h->tuned_max = -1;                       // AUTO uses the fixed rule until ar_tune
     for (int b = 0; b < kBuckets; ++b)
         for (int a = 0; a < 2; ++a)
             for (int p = 0; p < 2; ++p)
                 h->tuned_us[b][a][p] = 0.f;
     h->pdl = 1;
     h->ll_transport = AR_LL_AUTO;
+
+    // cluster LL: one CTA per virtual rank in a cluster (portable up to 8,
+    // 16 with the non-portable size); receive buffers of ~64 KiB per CTA
     h->cluster_ok = false;
     if (ll_capable && R <= 16) {
         uint64_t uc = ((uint64_t)kLlClusterTargetSmem / (8u * R) - 4) / 4;

@@ -50,14 +50,35 @@ __device__ __forceinline__ uint32_t fold_elem(const void *const *in, int R, uint
 // ---------------------------------------------------------------------------
 // One-shot HB.  Virtual rank r's output reads all R inputs: warp w of a CTA
 // computes out[w % R] for a run of 32 units (16-byte vectors, or elements
-// when some buffer is not 16-byte aligned), so the R warps that read the
-// same input lines run side by side and the lines come from HBM once, the
-// other R - 1 reads hitting L1/L2.  In place (in[r] == out[r]) is safe: a
-// CTA's units belong to it alone, and it finishes every read of its units
-// (barrier) before any store.
+// when some buffer is not 16-byte aligned).
+//
+// With vectors the CTA stages the inputs in shared memory through a ring of
+// kOneShotStages slots filled by cp.async: in each slot, warp w holds rank
+// w % R's 512 bytes of its run, loaded once, and after a barrier every warp
+// folds all R staged vectors of its run in rank order.  So each input byte
+// crosses L2 once per CTA instead of R times, and the loads of the next
+// kOneShotStages - 1 iterations are in flight while one is folded.  When the
+// grid covers the message (small messages: every CTA has one run) the host
+// launches the SINGLE instantiation instead, which skips the ring.  In place
+// (in[r] == out[r]) is safe: a CTA's units belong to it alone, an iteration
+// stores only units whose loads have completed, and the loads in flight are
+// of later iterations' units.
 // ---------------------------------------------------------------------------
-template <int DT, bool VEC>
+__device__ __forceinline__ void cp_async16(void *smem, const void *gmem) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;"
+                 :: "r"((uint32_t)__cvta_generic_to_shared(smem)), "l"(gmem)
+                 : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() {
+    asm volatile("cp.async.commit_group;" ::: "memory");
+}
+template <int PENDING> __device__ __forceinline__ void cp_async_wait() {
+    asm volatile("cp.async.wait_group %0;" :: "n"(PENDING) : "memory");
+}
+
+template <int DT, bool VEC, bool SINGLE>
 __global__ void __launch_bounds__(1024) k_one_shot_hb(const __grid_constant__ HbArgs a) {
+    extern __shared__ uint4 ring[];                      // VEC: [kOneShotStages][W * 32]
     kernel_prologue();
     constexpr int PV = VEC ? Elem<DT>::kPerVec : 1;
     const int R = a.R;
@@ -70,18 +91,80 @@ __global__ void __launch_bounds__(1024) k_one_shot_hb(const __grid_constant__ Hb
     const uint64_t per_blk = (uint64_t)m * 32;
     const uint64_t nblk = (units + per_blk - 1) / per_blk;
 
-    for (uint64_t blk = blockIdx.x; blk < nblk; blk += gridDim.x) {
-        const uint64_t u = blk * per_blk + (uint64_t)g * 32 + lane;
-        const bool live = u < units && g < m;
-        if (VEC) {
+    if constexpr (VEC && SINGLE) {
+        // Every CTA has at most one run (the grid covers the message), so
+        // there is nothing to overlap.  Up to 16 ranks, fold straight from
+        // global memory (the R warps of a run read the same lines side by
+        // side, and all but the first read hit L1); above, the R^2 loads
+        // through L1 cost more than one staging pass.
+        if (blockIdx.x < nblk) {
+            const uint64_t u = (uint64_t)blockIdx.x * per_blk + (uint64_t)g * 32 + lane;
+            const bool live = g < m && u < units;
             uint4 res = make_uint4(0, 0, 0, 0);
-            if (live)
-                res = fold_vec<DT, true>(a.p.in, R, u);
+            if (R <= 16) {
+                if (live)
+                    res = fold_vec<DT, true>(a.p.in, R, u);
+            } else {
+                if (live)
+                    ring[threadIdx.x] =
+                        ld_v4_stream(reinterpret_cast<const uint4 *>(a.p.in[r]) + u);
+                __syncthreads();
+                if (live) {
+                    const uint4 *run = ring + g * R * 32 + lane;
+                    VecAcc<DT> acc;
+                    acc.init(run[0]);
+                    for (int k = 1; k < R; ++k)
+                        acc.add(run[k * 32]);
+                    res = acc.result();
+                }
+            }
             if (a.inplace)
                 __syncthreads();
             if (live)
                 st_v4(reinterpret_cast<uint4 *>(a.p.out[r]) + u, res);
-        } else {
+        }
+    } else if constexpr (VEC) {
+        constexpr int S = kOneShotStages;
+        const uint64_t iters =
+            blockIdx.x < nblk ? (nblk - 1 - blockIdx.x) / gridDim.x + 1 : 0;
+        if (iters > 0) {
+            const uint4 *src = reinterpret_cast<const uint4 *>(a.p.in[r]);
+            // iteration j: this warp's run of rank r into slot j % S (one
+            // group per iteration, empty past the last so the wait count
+            // stays fixed)
+            auto issue = [&](uint64_t j) {
+                if (j < iters && g < m) {
+                    const uint64_t u =
+                        (blockIdx.x + j * gridDim.x) * per_blk + (uint64_t)g * 32 + lane;
+                    if (u < units)
+                        cp_async16(&ring[(int)(j % S) * (W * 32) + threadIdx.x], src + u);
+                }
+                cp_async_commit();
+            };
+#pragma unroll
+            for (int j = 0; j < S - 1; ++j)
+                issue(j);
+            for (uint64_t it = 0; it < iters; ++it) {
+                cp_async_wait<S - 2>();                  // this thread's copies of iteration it
+                __syncthreads();                         // ... and everyone's; slot (it-1) % S is free
+                issue(it + S - 1);
+                const uint64_t u =
+                    (blockIdx.x + it * gridDim.x) * per_blk + (uint64_t)g * 32 + lane;
+                if (g < m && u < units) {
+                    const uint4 *slot = ring + (int)(it % S) * (W * 32) + g * R * 32 + lane;
+                    VecAcc<DT> acc;
+                    acc.init(slot[0]);
+                    for (int k = 1; k < R; ++k)
+                        acc.add(slot[k * 32]);
+                    st_v4(reinterpret_cast<uint4 *>(a.p.out[r]) + u, acc.result());
+                }
+            }
+            cp_async_wait<0>();
+        }
+    } else {
+        for (uint64_t blk = blockIdx.x; blk < nblk; blk += gridDim.x) {
+            const uint64_t u = blk * per_blk + (uint64_t)g * 32 + lane;
+            const bool live = u < units && g < m;
             uint32_t res = 0;
             if (live)
                 res = fold_elem<DT>(a.p.in, R, u);
@@ -218,20 +301,45 @@ __global__ void __launch_bounds__(kRegThreads) k_round(const float *src, void *d
 // ---------------------------------------------------------------------------
 // Launchers.
 // ---------------------------------------------------------------------------
-template <int DT>
-static cudaError_t one_shot_dt(const HbArgs &a, bool vec, int grid, int block, cudaStream_t s,
-                               bool pdl) {
-    if (vec)
-        return launch_kernel(k_one_shot_hb<DT, true>, grid, block, 0, s, pdl, a);
-    return launch_kernel(k_one_shot_hb<DT, false>, grid, block, 0, s, pdl, a);
+// Dynamic shared memory of a one-shot launch: the ring's kOneShotStages
+// slots of one 16-byte vector per thread, or one slot when a single run is
+// staged (more than 16 ranks), or none.
+static size_t one_shot_smem(bool vec, bool single, int R, int block) {
+    if (!vec || (single && R <= 16))
+        return 0;
+    return (size_t)(single ? 1 : kOneShotStages) * block * sizeof(uint4);
 }
 
-cudaError_t launch_one_shot_hb(const HbArgs &a, int dtype, bool vec, int grid, int block,
+template <int DT>
+static cudaError_t one_shot_dt(const HbArgs &a, bool vec, bool single, int grid, int block,
                                cudaStream_t s, bool pdl) {
+    const size_t smem = one_shot_smem(vec, single, a.R, block);
+    if (vec && single)
+        return launch_kernel(k_one_shot_hb<DT, true, true>, grid, block, smem, s, pdl, a);
+    if (vec)
+        return launch_kernel(k_one_shot_hb<DT, true, false>, grid, block, smem, s, pdl, a);
+    return launch_kernel(k_one_shot_hb<DT, false, false>, grid, block, smem, s, pdl, a);
+}
+
+cudaError_t one_shot_prepare() {
+    const int bytes = (int)one_shot_smem(true, false, 0, 1024);
+    cudaError_t e = cudaFuncSetAttribute(k_one_shot_hb<AR_BF16, true, false>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+    if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(k_one_shot_hb<AR_FP16, true, false>,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+    if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(k_one_shot_hb<AR_FP32, true, false>,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+    return e;
+}
+
+cudaError_t launch_one_shot_hb(const HbArgs &a, int dtype, bool vec, bool single, int grid,
+                               int block, cudaStream_t s, bool pdl) {
     switch (dtype) {
-    case AR_BF16: return one_shot_dt<AR_BF16>(a, vec, grid, block, s, pdl);
-    case AR_FP16: return one_shot_dt<AR_FP16>(a, vec, grid, block, s, pdl);
-    default: return one_shot_dt<AR_FP32>(a, vec, grid, block, s, pdl);
+    case AR_BF16: return one_shot_dt<AR_BF16>(a, vec, single, grid, block, s, pdl);
+    case AR_FP16: return one_shot_dt<AR_FP16>(a, vec, single, grid, block, s, pdl);
+    default: return one_shot_dt<AR_FP32>(a, vec, single, grid, block, s, pdl);
     }
 }
 

@@ -20,6 +20,9 @@ constexpr int kEpochWords = 8192;
 constexpr int kRegThreads = 256;
 constexpr int kLlThreads = 128;
 
+// One-shot HB: slots of the shared-memory ring that stages the inputs.
+constexpr int kOneShotStages = 4;
+
 // TMA two-shot kernel: one producer warp and kTmaConsumerWarps consumer warps.
 constexpr int kTmaConsumerWarps = 8;
 constexpr int kTmaThreads = 32 * (1 + kTmaConsumerWarps);
@@ -138,8 +141,10 @@ struct PackArgs {
 Ctl handle_ctl(ar_handle_t h);
 
 // ar_hb.cu
-cudaError_t launch_one_shot_hb(const HbArgs &a, int dtype, bool vec, int grid, int block,
-                               cudaStream_t s, bool pdl = false);
+cudaError_t one_shot_prepare();                 // opt in to the one-shot ring's shared memory
+// `single`: the grid covers the message, every CTA has at most one run
+cudaError_t launch_one_shot_hb(const HbArgs &a, int dtype, bool vec, bool single, int grid,
+                               int block, cudaStream_t s, bool pdl = false);
 cudaError_t launch_reduce(const HbArgs &a, int dtype, bool vec, bool scatter_only, int grid,
                           cudaStream_t s, bool pdl = false);
 cudaError_t launch_all_gather(const HbArgs &a, int dtype, bool vec, int grid, cudaStream_t s,
