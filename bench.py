@@ -551,9 +551,80 @@ def measure_variants(runners, stream, flush, K):
     return out
 
 
+def host_threads() -> int:
+    """Host cores this process may run on."""
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
+
+
+def split_range(n: int, parts: int, align: int):
+    """At most `parts` [lo, hi) ranges covering 0..n, each a multiple of
+    `align` long except the last."""
+    step = max(1, -(-n // max(1, parts)))
+    step = -(-step // align) * align
+    return [(lo, min(n, lo + step)) for lo in range(0, n, step)]
+
+
+def oracle_case(lib, case, pool=None, threads=1) -> int:
+    """One oracle call over one case's sample; returns its minimal bytes.
+    `case` = (workload, combine?, input bit arrays, gate weights or None).
+    With a pool the call is split by element range (by token range for the
+    combine) over `threads` host threads: the oracle releases the GIL, so
+    the unchanged oracle code runs on every core."""
+    import oracle
+    from all_reduce_reduction_gb300 import workload as wl
+    w, combine, ins, wts = case
+    dt = wl.DTYPE_CODE[w.dtype]
+    if combine:
+        T = ins[0].size // w.H
+        ranges = split_range(T, threads, 1)
+
+        def part(rg):
+            t0, t1 = rg
+            oracle.combine([a[t0 * w.H: t1 * w.H] for a in ins], wts[t0 * w.K: t1 * w.K],
+                           t1 - t0, w.H, dt, lib=lib)
+        nbytes = (len(ins) + 1) * ins[0].nbytes + 4 * T * w.K
+    else:
+        ranges = split_range(ins[0].size, threads, 64)
+
+        def part(rg):
+            oracle.allreduce([a[rg[0]: rg[1]] for a in ins], dt, lib=lib)
+        nbytes = 2 * len(ins) * ins[0].nbytes
+    if pool is None or len(ranges) == 1:
+        for rg in ranges:
+            part(rg)
+    else:
+        list(pool.map(part, ranges))
+    return nbytes
+
+
+def time_oracle(lib, sample, seconds: float, threads: int):
+    """Passes over the sample's cases until `seconds` have elapsed; returns
+    (GB/s, passes, elapsed seconds)."""
+    from concurrent.futures import ThreadPoolExecutor
+    pool = ThreadPoolExecutor(threads) if threads > 1 else None
+    try:
+        done, passes, t0 = 0, 0, time.perf_counter()
+        while True:
+            for case in sample:
+                done += oracle_case(lib, case, pool, threads)
+            passes += 1
+            if time.perf_counter() - t0 >= seconds:
+                break
+        dt = time.perf_counter() - t0
+    finally:
+        if pool is not None:
+            pool.shutdown()
+    return done / dt / 1e9, passes, dt
+
+
 def cpu_baseline(runners, seconds: float):
-    """The oracle, as it stands (one thread), on a bounded sample of the same
-    workload: the step's cases one call each, repeated for ~`seconds`."""
+    """The oracle, as it stands, on a bounded sample of the same workload:
+    the step's cases one call each, repeated for ~`seconds` on all host
+    cores (each call split by element range), then for ~`seconds`/2 on one
+    thread."""
     import oracle
     from all_reduce_reduction_gb300 import workload as wl
     lib = oracle.load()
@@ -562,34 +633,26 @@ def cpu_baseline(runners, seconds: float):
         ins = [wl.bits(t) for t in r.cpu_inputs]
         if r.w.n > (1 << 22):           # large messages: a leading slice of every rank
             ins = [a[: 1 << 22].copy() for a in ins]
-        sample.append((r, ins))
-    done_bytes, t0 = 0, time.perf_counter()
-    passes = 0
-    while True:
-        for r, ins in sample:
-            dt = wl.DTYPE_CODE[r.w.dtype]
-            if r.c.get("combine"):
-                T = ins[0].size // r.w.H
-                oracle.combine(ins, r.w.weights()[: T * r.w.K], T, r.w.H, dt, lib=lib)
-                done_bytes += (len(ins) + 1) * ins[0].nbytes + 4 * T * r.w.K
-            else:
-                oracle.allreduce(ins, dt, lib=lib)
-                done_bytes += 2 * len(ins) * ins[0].nbytes
-        passes += 1
-        if time.perf_counter() - t0 >= seconds:
-            break
-    dt = time.perf_counter() - t0
-    return {"value": round(done_bytes / dt / 1e9, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
-            "sample": "%d passes over the step's %d cases, one call each%s (%.1f s)" % (
-                passes, len(sample),
-                ", first 2^22 elements per rank" if any(r.w.n > (1 << 22) for r in runners) else "",
-                dt)}
+        combine = bool(r.c.get("combine"))
+        wts = r.w.weights() if combine else None
+        sample.append((r.w, combine, ins, wts))
+    threads = host_threads()
+    value, passes, dt = time_oracle(lib, sample, seconds, threads)
+    one, passes1, dt1 = time_oracle(lib, sample, seconds / 2, 1)
+    sliced = ", first 2^22 elements per rank" if any(r.w.n > (1 << 22) for r in runners) else ""
+    return {"value": round(value, 4), "unit": "GB/s", "cores": threads, "kind": "oracle",
+            "sample": "%d passes over the step's %d cases, one call each%s, every call split "
+                      "by element range over %d threads (%.1f s)" % (
+                          passes, len(sample), sliced, threads, dt),
+            "one_thread": {"value": round(one, 4), "cores": 1,
+                           "sample": "%d passes, same cases, one thread (%.1f s)" % (passes1, dt1)}}
 
 
 # ---------------------------------------------------------------------------
 # reference arm: the CPU oracle on the host cores
 # ---------------------------------------------------------------------------
 def run_reference(args, world: int):
+    from concurrent.futures import ThreadPoolExecutor
     from all_reduce_reduction_gb300 import workload as wl
     import oracle
     desc, cases = workload_cases(args.workload, args)
@@ -601,34 +664,30 @@ def run_reference(args, world: int):
         if c.get("combine"):
             n = min(w.T, max(1, (1 << 20) // w.H)) * w.H
         ins = [wl.bits(t) for t in wl.make_inputs(w.config, w.R, n, w.dtype, w.dist)]
-        sample.append((c, ins))
-    dt_code = wl.DTYPE_CODE[cases[0]["w"].dtype]
+        sample.append((w, bool(c.get("combine")), ins, w.weights() if c.get("combine") else None))
+    threads = host_threads()
+    pool = ThreadPoolExecutor(threads) if threads > 1 else None
 
     def step():
-        b = 0
-        for c, ins in sample:
-            if c.get("combine"):
-                w = c["w"]
-                T = ins[0].size // w.H
-                oracle.combine(ins, w.weights()[: T * w.K], T, w.H, dt_code, lib=lib)
-                b += (len(ins) + 1) * ins[0].nbytes + 4 * T * w.K
-            else:
-                oracle.allreduce(ins, dt_code, lib=lib)
-                b += 2 * len(ins) * ins[0].nbytes
-        return b
+        return sum(oracle_case(lib, case, pool, threads) for case in sample)
 
-    for _ in range(args.warmup):
-        step()
-    t0 = time.perf_counter()
-    done = 0
-    for _ in range(args.steps):
-        done += step()
-    dt = time.perf_counter() - t0
+    try:
+        for _ in range(args.warmup):
+            step()
+        t0 = time.perf_counter()
+        done = 0
+        for _ in range(args.steps):
+            done += step()
+        dt = time.perf_counter() - t0
+    finally:
+        if pool is not None:
+            pool.shutdown()
     value = done / dt / 1e9
-    sample_desc = ("per step: each of the %d cases once (the GPU arm's step runs each %d times)%s"
+    sample_desc = ("per step: each of the %d cases once (the GPU arm's step runs each %d times)%s; "
+                   "every call split by element range over %d threads"
                    % (len(sample), cases[0]["calls"],
                       "; at most 2^20 elements per rank" if any(c["w"].n > (1 << 20) for c in cases)
-                      else ""))
+                      else "", threads))
     return {
         "impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "GB/s",
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
@@ -637,8 +696,8 @@ def run_reference(args, world: int):
         "config": {"workload": desc, "R": cases[0]["w"].R,
                    "sizes_elems_per_rank": [c["w"].n for c in cases],
                    "algo": cases[0]["algo"], "proto": cases[0]["proto"]},
-        "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
-                         "sample": sample_desc},
+        "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": threads,
+                         "kind": "oracle", "sample": sample_desc},
         "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
     }

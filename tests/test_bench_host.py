@@ -94,3 +94,31 @@ def test_traffic_lookup_needs_matching_digest():
     assert len(d) == 16
     assert bench.kernel_source_digest("no_such_kernel") == "unknown"
     assert bench.committed_traffic("no_such_kernel") is None
+
+
+@pytest.mark.parametrize("n", [0, 1, 63, 64, 65, 1000, 4097 * 4096 + 3])
+@pytest.mark.parametrize("parts", [1, 3, 8, 16])
+def test_split_range_covers_every_element_once(n, parts):
+    rs = bench.split_range(n, parts, 64)
+    assert len(rs) <= parts
+    assert all(rs[i][1] == rs[i + 1][0] for i in range(len(rs) - 1))      # contiguous
+    if n:
+        assert rs[0][0] == 0 and rs[-1][1] == n
+        assert all((hi - lo) % 64 == 0 for lo, hi in rs[:-1]) and all(hi > lo for lo, hi in rs)
+    else:
+        assert rs == []
+
+
+def test_threaded_oracle_timing_runs_every_case():
+    import oracle
+    from all_reduce_reduction_gb300 import workload as wl
+    lib = oracle.load()
+    w = wl.SMALL
+    ar_case = (w, False, [wl.bits(t) for t in w.inputs()], None)
+    cw = wl.COMBINE[1]
+    small = wl.CombineWorkload(cw.config, cw.name, cw.K, 3, 64, cw.dtype, cw.dist)
+    cb_case = (small, True, [wl.bits(t) for t in small.inputs()], small.weights())
+    assert bench.oracle_case(lib, ar_case) == 2 * 8 * 512 * 2
+    assert bench.oracle_case(lib, cb_case) == (8 + 1) * 3 * 64 * 2 + 4 * 3 * 8
+    gbs, passes, dt = bench.time_oracle(lib, [ar_case, cb_case], 0.05, 3)
+    assert gbs > 0 and passes >= 1 and dt >= 0.05

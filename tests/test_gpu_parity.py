@@ -113,6 +113,31 @@ def test_in_place_misaligned(path):
     run_case(3, 999, "bf16", *path, offset=1, inplace=True)
 
 
+def one_shot_hb_span(R, dtype):
+    """Elements the one-shot HB grid covers with one run per CTA on this GPU:
+    R warps per run of 32 vectors, at least 8 warps per CTA, 2048 threads
+    per SM.  One more vector makes some CTA take a second run (the ring)."""
+    W = R * -(-8 // R) if R <= 8 else R
+    ctas = torch.cuda.get_device_properties(0).multi_processor_count * (2048 // (32 * W))
+    return ctas * (W // R) * 32 * (16 // wl.ELEM_SIZE[dtype])
+
+
+@pytest.mark.parametrize("inplace", [False, True], ids=["out", "inplace"])
+@pytest.mark.parametrize("dtype", ["bf16", "fp32"])
+@pytest.mark.parametrize("R", [3, 8, 17, 32])
+@pytest.mark.parametrize("extra", ["exact", "tail", "one_more_vector", "runs_and_tail"])
+def test_one_shot_hb_single_and_ring(extra, R, dtype, inplace):
+    """Both sides of the switch from one run per CTA (folded from global, or
+    staged once above 16 ranks) to the shared-memory ring, with and without
+    a ragged tail, in place and not."""
+    need_gpu()
+    pv = 16 // wl.ELEM_SIZE[dtype]
+    add = {"exact": 0, "tail": pv - 1, "one_more_vector": pv,
+           "runs_and_tail": 3 * 32 * pv + pv - 1}[extra]
+    run_case(R, one_shot_hb_span(R, dtype) + add, dtype, ar.AR_ONE_SHOT, ar.AR_HB,
+             dist="normal", inplace=inplace)
+
+
 @pytest.mark.parametrize("dtype", DTYPES)
 @pytest.mark.parametrize("R,n", [(4, 4097 * 3 + 3), (16, 1001), (5, 9), (32, 70001), (8, 1 << 20)])
 def test_reduce_scatter_then_all_gather(dtype, R, n):
