@@ -263,6 +263,13 @@ def committed_traffic(kernel_key: str):
 # ---------------------------------------------------------------------------
 # our arm
 # ---------------------------------------------------------------------------
+def rank_stride(n: int, elem_size: int) -> int:
+    """Elements between the starts of consecutive ranks' buffers in a block:
+    n rounded up to a whole 256 bytes."""
+    per = 256 // elem_size
+    return -(-n // per) * per
+
+
 class CaseRunner:
     """Handle, device inputs/outputs and a captured graph for one case."""
 
@@ -274,17 +281,22 @@ class CaseRunner:
         w = self.w
         self.cpu_inputs = w.inputs(threads=16)
         # the R rank buffers of each direction are views of one allocation, so
-        # the end-to-end leg moves them with one copy each way
+        # the end-to-end leg moves them with one copy each way; every rank
+        # starts on a 256-byte boundary, as separately allocated buffers would
+        # (an odd N would otherwise leave ranks 1.. off 16-byte alignment and
+        # send them down the element-wise paths)
         n = self.cpu_inputs[0].numel()
-        in_block = torch.empty(len(self.cpu_inputs) * n, dtype=self.cpu_inputs[0].dtype,
-                               device="cuda")
-        self.ins = [in_block[r * n:(r + 1) * n] for r in range(len(self.cpu_inputs))]
+        self.stride = rank_stride(n, self.cpu_inputs[0].element_size())
+        nin = len(self.cpu_inputs)
+        in_block = torch.zeros(nin * self.stride, dtype=self.cpu_inputs[0].dtype, device="cuda")
+        self.ins = [in_block[r * self.stride:r * self.stride + n] for r in range(nin)]
         for d, t in zip(self.ins, self.cpu_inputs):
             d.copy_(t)
         self.in_block = in_block
-        nout = 1 if c.get("combine") else len(self.cpu_inputs)
-        self.out_block = torch.empty(nout * n, dtype=in_block.dtype, device="cuda")
-        self.outs = [self.out_block[r * n:(r + 1) * n] for r in range(nout)]
+        nout = 1 if c.get("combine") else nin
+        self.out_block = torch.zeros(nout * self.stride, dtype=in_block.dtype, device="cuda")
+        self.outs = [self.out_block[r * self.stride:r * self.stride + n] for r in range(nout)]
+        assert all(t.data_ptr() % 256 == 0 for t in self.ins + self.outs)
         if c.get("combine"):
             self.weights = torch.from_numpy(w.weights()).cuda()
             self.h = ar.Handle(w.K, w.T * w.H, w.dtype)
@@ -327,7 +339,9 @@ class CaseRunner:
         torch.cuda.synchronize()
         if ar.ar_status(self.h.h) != ar.AR_OK:
             raise RuntimeError("device status after warm-up: " + ar.ar_strerror(ar.ar_status(self.h.h)))
-        self.pinned_in = torch.cat(self.cpu_inputs).pin_memory()
+        self.pinned_in = torch.zeros(in_block.shape, dtype=in_block.dtype).pin_memory()
+        for r, t in enumerate(self.cpu_inputs):
+            self.pinned_in[r * self.stride:r * self.stride + n].copy_(t)
         self.pinned_out = torch.empty(self.out_block.shape, dtype=self.out_block.dtype).pin_memory()
 
     def close(self):

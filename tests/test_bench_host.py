@@ -122,3 +122,10 @@ def test_threaded_oracle_timing_runs_every_case():
     assert bench.oracle_case(lib, cb_case) == (8 + 1) * 3 * 64 * 2 + 4 * 3 * 8
     gbs, passes, dt = bench.time_oracle(lib, [ar_case, cb_case], 0.05, 3)
     assert gbs > 0 and passes >= 1 and dt >= 0.05
+
+
+@pytest.mark.parametrize("n", [1, 7, 512, 4097 * 4096 + 3, 8192 * 8192])
+@pytest.mark.parametrize("esz", [2, 4])
+def test_rank_stride_keeps_every_rank_256_byte_aligned(n, esz):
+    st = bench.rank_stride(n, esz)
+    assert st >= n and (st * esz) % 256 == 0 and (st - n) * esz < 256
