@@ -261,12 +261,13 @@ uint64_t ceil_div_u(uint64_t a, uint64_t b) { return (a + b - 1) / b; }
 
 }  // namespace
 
-extern "C" int ar_plan_compile(ar_handle_t h, const ar_op *ops, int nops, int nchunks,
-                               int ctas_per_rank, ar_plan_t *out) {
+// Largest plan, in tasks (one step on one chunk); keeps the host-side
+// compilation and the instruction streams bounded.
+constexpr uint64_t kMaxPlanTasks = 1u << 20;
+
+static int compile_plan(ar_handle_t h, const ar_op *ops, int nops, int nchunks,
+                        int ctas_per_rank, ar_plan_t *out) {
     ar_info info;
-    if (!out)
-        return AR_ERR_INVALID;
-    *out = nullptr;
     if (!h || !ops || nops < 1 || nchunks < 1 || ctas_per_rank < 0 ||
         ar_get_info(h, &info) != AR_OK)
         return AR_ERR_INVALID;
@@ -289,6 +290,11 @@ extern "C" int ar_plan_compile(ar_handle_t h, const ar_op *ops, int nops, int nc
             if (o.src_rank[i] < 0 || o.src_rank[i] >= R)
                 return AR_ERR_INVALID;
     }
+    uint64_t ntasks = 0;
+    for (int k = 0; k < nops; ++k)
+        ntasks += (uint64_t)(ops[k].chunk_end - ops[k].chunk_begin);
+    if (ntasks > kMaxPlanTasks)
+        return AR_ERR_UNSUPPORTED;
     int per_sm = 0, dev = 0, sms = 0;
     if (cudaGetDevice(&dev) != cudaSuccess ||
         cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
@@ -426,8 +432,22 @@ extern "C" int ar_plan_compile(ar_handle_t h, const ar_op *ops, int nops, int nc
     return AR_OK;
 }
 
-extern "C" int ar_plan_builtin(ar_handle_t h, int algo, int chunks_per_rank, int ctas_per_rank,
-                               ar_plan_t *out) {
+extern "C" int ar_plan_compile(ar_handle_t h, const ar_op *ops, int nops, int nchunks,
+                               int ctas_per_rank, ar_plan_t *out) {
+    if (!out)
+        return AR_ERR_INVALID;
+    *out = nullptr;
+    // host containers may throw; nothing that needs releasing exists before
+    // the last of them is built
+    try {
+        return compile_plan(h, ops, nops, nchunks, ctas_per_rank, out);
+    } catch (const std::bad_alloc &) {
+        return AR_ERR_NOMEM;
+    }
+}
+
+static int builtin_plan(ar_handle_t h, int algo, int chunks_per_rank, int ctas_per_rank,
+                        ar_plan_t *out) {
     ar_info info;
     if (!out || !h || ar_get_info(h, &info) != AR_OK || chunks_per_rank < 0 ||
         ctas_per_rank < 0 || (algo != AR_ONE_SHOT && algo != AR_TWO_SHOT))
@@ -438,6 +458,8 @@ extern "C" int ar_plan_builtin(ar_handle_t h, int algo, int chunks_per_rank, int
         return AR_ERR_UNSUPPORTED;
     if (chunks_per_rank == 0)
         chunks_per_rank = ctas_per_rank;     // one chunk per CTA and step
+    if ((uint64_t)chunks_per_rank * (uint64_t)info.R > kMaxPlanTasks)
+        return AR_ERR_UNSUPPORTED;           // R * K chunks, at least as many tasks
     const int R = info.R, K = chunks_per_rank;
     std::vector<ar_op> ops;
     ar_op o = {};
@@ -481,6 +503,15 @@ extern "C" int ar_plan_builtin(ar_handle_t h, int algo, int chunks_per_rank, int
             }
     }
     return ar_plan_compile(h, ops.data(), (int)ops.size(), R * K, ctas_per_rank, out);
+}
+
+extern "C" int ar_plan_builtin(ar_handle_t h, int algo, int chunks_per_rank, int ctas_per_rank,
+                               ar_plan_t *out) {
+    try {
+        return builtin_plan(h, algo, chunks_per_rank, ctas_per_rank, out);
+    } catch (const std::bad_alloc &) {
+        return AR_ERR_NOMEM;
+    }
 }
 
 extern "C" int ar_plan_execute(ar_plan_t p, const void *const in[], void *const out[],

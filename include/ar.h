@@ -362,7 +362,8 @@ typedef struct ar_plan *ar_plan_t;
  * a write; those producers signal a semaphore.  Allocates the plan's device
  * memory and waits for the upload (not a hot-path call).
  * Errors: AR_ERR_INVALID (bad step, range), AR_ERR_UNSUPPORTED (R *
- * ctas_per_rank CTAs cannot all be resident), AR_ERR_NOMEM, AR_ERR_CUDA. */
+ * ctas_per_rank CTAs cannot all be resident, or the steps make more than
+ * 2^20 tasks), AR_ERR_NOMEM (device or host memory), AR_ERR_CUDA. */
 int ar_plan_compile(ar_handle_t h, const ar_op *ops, int nops, int nchunks,
                     int ctas_per_rank, ar_plan_t *out);
 /* (ctas_per_rank == 0: as many as can be resident together, R * that <= the

@@ -116,6 +116,14 @@ def test_plan_misaligned_buffers_and_rejections():
         bad = ar.make_op(ar.AR_OP_COPY, 0, (ar.AR_BUF_OUT, 0), [(ar.AR_BUF_IN, 1)], 0, 9)
         with pytest.raises(ar.ArError):                  # chunk range beyond nchunks
             ar.ar_plan_compile(h.h, [bad], 4, 1)
+        huge = (1 << 20) + 1
+        big = ar.make_op(ar.AR_OP_COPY, 0, (ar.AR_BUF_OUT, 0), [(ar.AR_BUF_IN, 1)], 0, huge)
+        with pytest.raises(ar.ArError) as e:             # more tasks than a plan may hold
+            ar.ar_plan_compile(h.h, [big], huge, 1)
+        assert e.value.code == ar.AR_ERR_UNSUPPORTED
+        with pytest.raises(ar.ArError) as e:             # R * chunks_per_rank beyond it too
+            ar.ar_plan_builtin(h.h, "one_shot", 1 << 30, 2)
+        assert e.value.code == ar.AR_ERR_UNSUPPORTED
         ar.ar_plan_destroy(p)
 
 
