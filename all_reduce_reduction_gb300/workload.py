@@ -117,6 +117,52 @@ def from_bits(a: np.ndarray, dtype: str) -> torch.Tensor:
         TORCH_DTYPE[dtype])
 
 
+# Bit patterns at the edges of each format, for the special-value cases.  The
+# first TINY_COUNT entries of a pool are signed zeros, subnormals and the
+# smallest normals (their binary32 sums are subnormal or cancel into the
+# subnormal range); the rest are ones and values near the largest finite one
+# (their sums overflow to infinity).
+SPECIAL_BITS = {
+    "bf16": [0x0000, 0x8000, 0x0001, 0x8001, 0x0002, 0x8002, 0x007F, 0x807F, 0x0040, 0x8040,
+             0x0080, 0x8080, 0x0081, 0x8081,
+             0x3F80, 0xBF80, 0x7F7F, 0xFF7F, 0x7F00, 0xFF00, 0x4000, 0x3C00],
+    "fp16": [0x0000, 0x8000, 0x0001, 0x8001, 0x0002, 0x8002, 0x03FF, 0x83FF, 0x0200, 0x8200,
+             0x0400, 0x8400, 0x0401, 0x8401,
+             0x3C00, 0xBC00, 0x7BFF, 0xFBFF, 0x7800, 0xF800, 0x4000, 0x1000],
+    "fp32": [0x00000000, 0x80000000, 0x00000001, 0x80000001, 0x00000002, 0x80000002,
+             0x007FFFFF, 0x807FFFFF, 0x00400000, 0x80400000, 0x00800000, 0x80800000,
+             0x00800001, 0x80800001,
+             0x3F800000, 0xBF800000, 0x7F7FFFFF, 0xFF7FFFFF, 0x7F000000, 0xFF000000,
+             0x40000000, 0x33800000],
+}
+TINY_COUNT = 14
+
+# binary32 gate weights for the special combine cases: signs, zeros, a
+# subnormal, the smallest normal, small scales and the largest value below 1.
+# All at most 1 in magnitude, so no product of finite values is infinite and
+# no sum of opposite infinities (a NaN) can arise.
+SPECIAL_WEIGHT_BITS = [0x3F800000, 0xBF800000, 0x3F000000, 0x00000000, 0x80000000, 0x00800000,
+                       0x00000001, 0x3E800000, 0x3F7FFFFF, 0x0D800000]
+
+
+def special_inputs(seed: int, R: int, n: int, dtype: str) -> list[torch.Tensor]:
+    """R buffers of n elements picked from SPECIAL_BITS[dtype] by SplitMix64
+    draws (stream seed + rank): even-indexed elements pick only among the
+    tiny entries, odd ones among the whole pool."""
+    pool = np.array(SPECIAL_BITS[dtype], dtype=np.uint32 if dtype == "fp32" else np.uint16)
+    idx = np.arange(n, dtype=np.uint64)
+    size = np.where(idx % np.uint64(2) == 0, np.uint64(TINY_COUNT), np.uint64(pool.size))
+    return [from_bits(pool[(splitmix64(seed + r, idx) % size).astype(np.int64)].view(
+        np.float32 if dtype == "fp32" else np.uint16), dtype) for r in range(R)]
+
+
+def special_weights(seed: int, T: int, K: int) -> np.ndarray:
+    """T x K binary32 gate weights picked from SPECIAL_WEIGHT_BITS."""
+    pool = np.array(SPECIAL_WEIGHT_BITS, dtype=np.uint32)
+    d = splitmix64(seed, np.arange(T * K, dtype=np.uint64)) % np.uint64(pool.size)
+    return pool[d.astype(np.int64)].view(np.float32)
+
+
 @dataclass(frozen=True)
 class Workload:
     """One workload: R virtual ranks of n elements each."""
