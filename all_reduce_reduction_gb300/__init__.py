@@ -163,7 +163,16 @@ def _stream(s) -> int:
 
 
 def _ptr_array(bufs):
-    return (ctypes.c_void_p * len(bufs))(*[_ptr(b) for b in bufs])
+    """Host array of device pointers, always AR_MAX_RANKS long: entries past
+    the given buffers are NULL, so passing fewer buffers than the handle's
+    ranks is rejected by the library (AR_ERR_INVALID) instead of reading past
+    the end of the array."""
+    if len(bufs) > AR_MAX_RANKS:
+        raise ValueError("at most %d buffers" % AR_MAX_RANKS)
+    arr = (ctypes.c_void_p * AR_MAX_RANKS)()
+    for i, b in enumerate(bufs):
+        arr[i] = _ptr(b)
+    return arr
 
 
 def _check(code: int, where: str) -> None:

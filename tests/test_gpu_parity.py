@@ -283,6 +283,22 @@ def test_ll_rejected_above_cap():
         ar.ar_allreduce(h.h, x, x, ar.AR_TWO_SHOT, ar.AR_HB)   # HB still serves it
 
 
+def test_too_few_buffers_rejected():
+    """The binding pads pointer arrays with NULL: fewer buffers than ranks is
+    an argument error, never a read past the array."""
+    need_gpu()
+    R, n = 4, 1000
+    ins = [torch.zeros(n, dtype=torch.bfloat16, device="cuda") for _ in range(R)]
+    outs = [torch.empty_like(t) for t in ins]
+    with ar.Handle(R, n, "bf16") as h:
+        for a, b in [(ins[:3], outs), (ins, outs[:2]), ([], [])]:
+            with pytest.raises(ar.ArError) as e:
+                ar.ar_allreduce(h.h, a, b, ar.AR_TWO_SHOT, ar.AR_HB)
+            assert e.value.code == ar.AR_ERR_INVALID
+        with pytest.raises(ValueError):
+            ar.ar_allreduce(h.h, ins * 9, outs, ar.AR_ONE_SHOT, ar.AR_HB)
+
+
 def test_invalid_aliasing_rejected():
     need_gpu()
     R, n = 3, 100
