@@ -76,12 +76,14 @@ template <int PENDING> __device__ __forceinline__ void cp_async_wait() {
     asm volatile("cp.async.wait_group %0;" :: "n"(PENDING) : "memory");
 }
 
-template <int DT, bool VEC, bool SINGLE>
+// RC > 0: the kernel is instantiated for R == RC, so the ring path's fold is
+// unrolled and its shared-memory reads are issued eight at a time.
+template <int DT, bool VEC, bool SINGLE, int RC = 0>
 __global__ void __launch_bounds__(1024) k_one_shot_hb(const __grid_constant__ HbArgs a) {
     extern __shared__ uint4 ring[];                      // VEC: [kOneShotStages][W * 32]
     kernel_prologue();
     constexpr int PV = VEC ? Elem<DT>::kPerVec : 1;
-    const int R = a.R;
+    const int R = RC ? RC : a.R;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int W = blockDim.x >> 5;
     const int r = warp % R;
@@ -154,8 +156,23 @@ __global__ void __launch_bounds__(1024) k_one_shot_hb(const __grid_constant__ Hb
                     const uint4 *slot = ring + (int)(it % S) * (W * 32) + g * R * 32 + lane;
                     VecAcc<DT> acc;
                     acc.init(slot[0]);
-                    for (int k = 1; k < R; ++k)
-                        acc.add(slot[k * 32]);
+                    if constexpr (RC > 0) {
+#pragma unroll
+                        for (int k0 = 1; k0 < RC; k0 += 8) {
+                            uint4 x[8];
+#pragma unroll
+                            for (int j = 0; j < 8; ++j)
+                                if (k0 + j < RC)
+                                    x[j] = slot[(k0 + j) * 32];
+#pragma unroll
+                            for (int j = 0; j < 8; ++j)
+                                if (k0 + j < RC)
+                                    acc.add(x[j]);
+                        }
+                    } else {
+                        for (int k = 1; k < R; ++k)
+                            acc.add(slot[k * 32]);
+                    }
                     st_v4(reinterpret_cast<uint4 *>(a.p.out[r]) + u, acc.result());
                 }
             }
@@ -316,21 +333,40 @@ static cudaError_t one_shot_dt(const HbArgs &a, bool vec, bool single, int grid,
     const size_t smem = one_shot_smem(vec, single, a.R, block);
     if (vec && single)
         return launch_kernel(k_one_shot_hb<DT, true, true>, grid, block, smem, s, pdl, a);
-    if (vec)
-        return launch_kernel(k_one_shot_hb<DT, true, false>, grid, block, smem, s, pdl, a);
+    if (vec) {
+        // rank counts with an unrolled fold: those where it measured faster
+        // (R = 4 measured slower unrolled and keeps the loop)
+        switch (a.R) {
+        case 2: return launch_kernel(k_one_shot_hb<DT, true, false, 2>, grid, block, smem, s, pdl, a);
+        case 8: return launch_kernel(k_one_shot_hb<DT, true, false, 8>, grid, block, smem, s, pdl, a);
+        case 16: return launch_kernel(k_one_shot_hb<DT, true, false, 16>, grid, block, smem, s, pdl, a);
+        default: return launch_kernel(k_one_shot_hb<DT, true, false>, grid, block, smem, s, pdl, a);
+        }
+    }
     return launch_kernel(k_one_shot_hb<DT, false, false>, grid, block, smem, s, pdl, a);
+}
+
+template <int DT> static cudaError_t one_shot_prepare_dt(int bytes) {
+    const void *fns[] = {reinterpret_cast<const void *>(&k_one_shot_hb<DT, true, false>),
+                         reinterpret_cast<const void *>(&k_one_shot_hb<DT, true, false, 2>),
+                         reinterpret_cast<const void *>(&k_one_shot_hb<DT, true, false, 8>),
+                         reinterpret_cast<const void *>(&k_one_shot_hb<DT, true, false, 16>)};
+    for (const void *f : fns) {
+        const cudaError_t e =
+            cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+        if (e != cudaSuccess)
+            return e;
+    }
+    return cudaSuccess;
 }
 
 cudaError_t one_shot_prepare() {
     const int bytes = (int)one_shot_smem(true, false, 0, 1024);
-    cudaError_t e = cudaFuncSetAttribute(k_one_shot_hb<AR_BF16, true, false>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+    cudaError_t e = one_shot_prepare_dt<AR_BF16>(bytes);
     if (e == cudaSuccess)
-        e = cudaFuncSetAttribute(k_one_shot_hb<AR_FP16, true, false>,
-                                 cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+        e = one_shot_prepare_dt<AR_FP16>(bytes);
     if (e == cudaSuccess)
-        e = cudaFuncSetAttribute(k_one_shot_hb<AR_FP32, true, false>,
-                                 cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+        e = one_shot_prepare_dt<AR_FP32>(bytes);
     return e;
 }
 
