@@ -20,6 +20,14 @@
 //     task depends on the last writer of every region it reads or writes
 //     (read-after-write, write-after-write) and on the readers since that
 //     write of every region it writes (write-after-read).
+//   * Fusion (the DSL compiler's operator fusion): a copy task whose source
+//     region was last written by task t, and whose destination region no
+//     task has touched since t, becomes an extra destination of t: t stores
+//     its result there too and the copy disappears.  The copy would have
+//     stored exactly t's result, and nothing in between could tell the
+//     difference, so the final state is the sequential one.  A two-shot
+//     plan's all-gather copies fuse into the shard reductions this way: no
+//     re-read of the reduced shards, and no semaphores left.
 //   * A dependency inside one CTA needs nothing beyond program order (the
 //     CTA syncs its threads between tasks).  One across CTAs gets a
 //     semaphore: the producer task signals it once per run, the consumer
@@ -41,6 +49,9 @@ namespace ar {
 
 enum : int { kInstrWait = 0, kInstrTask = 1, kInstrSignal = 2 };
 
+// Most destinations a task can gain by fusion: every other buffer.
+constexpr int kPlanMaxExtraDst = 2 * AR_MAX_RANKS - 1;
+
 struct PlanStep {            // device copy of one step
     int kind;                // AR_OP_COPY / AR_OP_REDUCE
     int dst;                 // buffer id: < R in[], else out[id - R]
@@ -53,7 +64,9 @@ struct PlanArgs {
     uint64_t n;
     uint64_t chunk;          // elements per chunk (multiple of a 16-byte vector)
     const PlanStep *steps;
-    const int4 *instr;       // {kind, a, b, 0}: wait(sem a) / task(step a, chunk b) / signal(sem a)
+    const int4 *instr;       // {kind, a, b, x}: wait(sem a) / task(step a, chunk b, extra
+                             // destinations at xdst[x] when x >= 0) / signal(sem a)
+    const int *xdst;         // extra destination lists: count, then buffer ids
     const int *start;        // instr[start[b] .. start[b + 1]) belong to CTA b
     uint32_t *sems;
     uint32_t *epoch;         // one word per CTA: completed runs
@@ -71,7 +84,8 @@ __device__ __forceinline__ const void *buf_ptr(const PlanArgs &a, int id) {
 struct TaskPtrs {
     const void *src[AR_MAX_RANKS];
     void *dst;
-    int kind, nsrc;
+    void *xdst[kPlanMaxExtraDst];   // fused copies' destinations
+    int kind, nsrc, nx;
 };
 
 template <int DT>
@@ -88,41 +102,48 @@ __device__ void run_task(const PlanArgs &a, const TaskPtrs &t, uint64_t chunk) {
     if (a.vec) {
         vhi = lo + (hi - lo) / PV * PV;
         for (uint64_t u = lo / PV + threadIdx.x; u < vhi / PV; u += blockDim.x) {
+            uint4 y;
             if (t.kind == AR_OP_COPY) {
-                st_v4(reinterpret_cast<uint4 *>(t.dst) + u,
-                      ld_v4_stream(reinterpret_cast<const uint4 *>(t.src[0]) + u));
-                continue;
-            }
-            // fold the sources in their order, eight loads in flight at a time
-            VecAcc<DT> acc;
-            for (int k0 = 0; k0 < nsrc; k0 += 8) {
-                uint4 v[8];
+                y = ld_v4_stream(reinterpret_cast<const uint4 *>(t.src[0]) + u);
+            } else {
+                // fold the sources in their order, eight loads in flight at a time
+                VecAcc<DT> acc;
+                for (int k0 = 0; k0 < nsrc; k0 += 8) {
+                    uint4 v[8];
 #pragma unroll
-                for (int j = 0; j < 8; ++j)
-                    if (k0 + j < nsrc)
-                        v[j] = ld_v4_stream(reinterpret_cast<const uint4 *>(t.src[k0 + j]) + u);
+                    for (int j = 0; j < 8; ++j)
+                        if (k0 + j < nsrc)
+                            v[j] = ld_v4_stream(reinterpret_cast<const uint4 *>(t.src[k0 + j]) + u);
 #pragma unroll
-                for (int j = 0; j < 8; ++j)
-                    if (k0 + j < nsrc) {
-                        if (k0 + j == 0)
-                            acc.init(v[j]);
-                        else
-                            acc.add(v[j]);
-                    }
+                    for (int j = 0; j < 8; ++j)
+                        if (k0 + j < nsrc) {
+                            if (k0 + j == 0)
+                                acc.init(v[j]);
+                            else
+                                acc.add(v[j]);
+                        }
+                }
+                y = acc.result();
             }
-            st_v4(reinterpret_cast<uint4 *>(t.dst) + u, acc.result());
+            st_v4(reinterpret_cast<uint4 *>(t.dst) + u, y);
+            for (int d = 0; d < t.nx; ++d)
+                st_v4(reinterpret_cast<uint4 *>(t.xdst[d]) + u, y);
         }
     }
     for (uint64_t e = vhi + threadIdx.x; e < hi; e += blockDim.x) {
+        uint32_t y;
         if (t.kind == AR_OP_COPY) {
-            st_elem<DT>(t.dst, e, ld_elem<DT>(t.src[0], e));
+            y = ld_elem<DT>(t.src[0], e);
         } else {
             ElemAcc<DT> acc;
             acc.init(ld_elem<DT>(t.src[0], e));
             for (int k = 1; k < nsrc; ++k)
                 acc.add(ld_elem<DT>(t.src[k], e));
-            st_elem<DT>(t.dst, e, acc.result());
+            y = acc.result();
         }
+        st_elem<DT>(t.dst, e, y);
+        for (int d = 0; d < t.nx; ++d)
+            st_elem<DT>(t.xdst[d], e, y);
     }
 }
 
@@ -173,12 +194,16 @@ __global__ void __launch_bounds__(kRegThreads) k_plan(const __grid_constant__ Pl
         } else if (in.x == kInstrTask) {
             if (!give_up) {
                 const PlanStep &st = a.steps[in.y];
+                const int nx = in.w >= 0 ? a.xdst[in.w] : 0;
                 if (threadIdx.x < (unsigned)st.nsrc)
                     tp.src[threadIdx.x] = buf_ptr(a, st.src[threadIdx.x]);
+                if (threadIdx.x < (unsigned)nx)
+                    tp.xdst[threadIdx.x] = const_cast<void *>(buf_ptr(a, a.xdst[in.w + 1 + threadIdx.x]));
                 if (threadIdx.x == 0) {
                     tp.dst = const_cast<void *>(buf_ptr(a, st.dst));
                     tp.kind = st.kind;
                     tp.nsrc = st.nsrc;
+                    tp.nx = nx;
                 }
                 __syncthreads();
                 run_task<DT>(a, tp, (uint64_t)in.z);
@@ -223,10 +248,11 @@ struct ar_plan {
     uint64_t N, chunk;
     size_t esz;
     int ntasks, nwaits, nsignals;
-    void *dev;               // one allocation: steps | instr | start | sems | epoch
+    void *dev;               // one allocation: steps | instr | start | sems | epoch | xdst
     PlanStep *steps;
     int4 *instr;
     int *start;
+    int *xdst;               // extra destination lists of fused tasks
     uint32_t *sems;
     uint32_t *epoch;
     Ctl ctl;                 // the handle's status / abort words and timeout
@@ -252,6 +278,8 @@ int plan_ctas_per_rank(int R, int dtype) {
 
 struct Task {
     int step, chunk, cta;
+    std::vector<int> xdst;   // destinations gained by fusing later copies
+    bool fused = false;      // this copy became an extra destination of another task
     std::vector<int> deps;   // producer tasks in other CTAs
     bool signals = false;
     int sem = -1;
@@ -308,10 +336,6 @@ static int compile_plan(ar_handle_t h, const ar_op *ops, int nops, int nchunks,
     if (ctas > per_sm * sms || ctas > kEpochWords)
         return AR_ERR_UNSUPPORTED;                       // not all CTAs can be resident
 
-    // tasks in program order, with their dependencies
-    std::vector<Task> tasks;
-    std::map<std::pair<int, int>, int> last_writer;            // (buffer id, chunk) -> task
-    std::map<std::pair<int, int>, std::vector<int>> readers;   // since that write
     std::vector<PlanStep> steps(nops);
     for (int k = 0; k < nops; ++k) {
         const ar_op &o = ops[k];
@@ -321,24 +345,87 @@ static int compile_plan(ar_handle_t h, const ar_op *ops, int nops, int nchunks,
         st.nsrc = o.nsrc;
         for (int i = 0; i < AR_MAX_RANKS; ++i)
             st.src[i] = i < o.nsrc ? o.src_buf * R + o.src_rank[i] : 0;
-        for (int c = o.chunk_begin; c < o.chunk_end; ++c) {
+    }
+    // tasks in program order
+    std::vector<Task> tasks;
+    tasks.reserve((size_t)ntasks);
+    for (int k = 0; k < nops; ++k)
+        for (int c = ops[k].chunk_begin; c < ops[k].chunk_end; ++c) {
             Task t;
             t.step = k;
             t.chunk = c;
-            t.cta = o.rank * G + c % G;
-            const int id = (int)tasks.size();
-            std::vector<int> deps;
-            for (int i = 0; i < o.nsrc; ++i) {
-                auto w = last_writer.find({st.src[i], c});
+            t.cta = ops[k].rank * G + c % G;
+            tasks.push_back(t);
+        }
+
+    // fusion: copy u of region (S, c) into (E, c) joins t = the last writer
+    // of (S, c) when no task at or after t has touched (E, c) and E is none
+    // of t's own buffers
+    using Region = std::pair<int, int>;                          // (buffer id, chunk)
+    {
+        std::map<Region, int> writer;       // last writer (a task that stays)
+        std::map<Region, int> touched;      // last task reading or writing it
+        for (int i = 0; i < (int)tasks.size(); ++i) {
+            Task &u = tasks[i];
+            const PlanStep &st = steps[u.step];
+            const int c = u.chunk;
+            if (st.kind == AR_OP_COPY && st.src[0] != st.dst) {
+                auto w = writer.find({st.src[0], c});
+                if (w != writer.end()) {
+                    Task &t = tasks[w->second];
+                    const PlanStep &ts = steps[t.step];
+                    const int E = st.dst;
+                    bool clash = E == ts.dst ||
+                                 std::find(t.xdst.begin(), t.xdst.end(), E) != t.xdst.end() ||
+                                 (int)t.xdst.size() >= kPlanMaxExtraDst;
+                    for (int k = 0; k < ts.nsrc && !clash; ++k)
+                        clash = ts.src[k] == E;
+                    auto seen = touched.find({E, c});
+                    if (!clash && (seen == touched.end() || seen->second < w->second)) {
+                        t.xdst.push_back(E);
+                        u.fused = true;
+                        writer[{E, c}] = w->second;
+                        touched[{E, c}] = w->second;
+                        continue;
+                    }
+                }
+            }
+            for (int k = 0; k < st.nsrc; ++k)
+                touched[{st.src[k], c}] = i;
+            writer[{st.dst, c}] = i;
+            touched[{st.dst, c}] = i;
+        }
+    }
+
+    // dependencies between the tasks that stay: on the last writer of every
+    // region read or written, and on the readers since of every region written
+    std::vector<int> live;                                       // task indices that stay
+    for (int i = 0; i < (int)tasks.size(); ++i)
+        if (!tasks[i].fused)
+            live.push_back(i);
+    {
+        std::map<Region, int> last_writer;
+        std::map<Region, std::vector<int>> readers;               // since that write
+        std::vector<int> dsts, deps;
+        for (int id : live) {
+            Task &t = tasks[id];
+            const PlanStep &st = steps[t.step];
+            const int c = t.chunk;
+            dsts.assign(1, st.dst);
+            dsts.insert(dsts.end(), t.xdst.begin(), t.xdst.end());
+            deps.clear();
+            for (int k = 0; k < st.nsrc; ++k) {
+                auto w = last_writer.find({st.src[k], c});
                 if (w != last_writer.end())
                     deps.push_back(w->second);
             }
-            const std::pair<int, int> dkey{st.dst, c};
-            auto w = last_writer.find(dkey);
-            if (w != last_writer.end())
-                deps.push_back(w->second);
-            for (int rd : readers[dkey])
-                deps.push_back(rd);
+            for (int d : dsts) {
+                auto w = last_writer.find({d, c});
+                if (w != last_writer.end())
+                    deps.push_back(w->second);
+                for (int rd : readers[{d, c}])
+                    deps.push_back(rd);
+            }
             std::sort(deps.begin(), deps.end());
             deps.erase(std::unique(deps.begin(), deps.end()), deps.end());
             for (int d : deps)
@@ -346,27 +433,36 @@ static int compile_plan(ar_handle_t h, const ar_op *ops, int nops, int nchunks,
                     t.deps.push_back(d);
                     tasks[d].signals = true;
                 }
-            for (int i = 0; i < o.nsrc; ++i)
-                if (st.src[i] != st.dst)
-                    readers[{st.src[i], c}].push_back(id);
-            last_writer[dkey] = id;
-            readers[dkey].clear();
-            tasks.push_back(t);
+            for (int k = 0; k < st.nsrc; ++k)
+                if (std::find(dsts.begin(), dsts.end(), st.src[k]) == dsts.end())
+                    readers[{st.src[k], c}].push_back(id);
+            for (int d : dsts) {
+                last_writer[{d, c}] = id;
+                readers[{d, c}].clear();
+            }
         }
     }
     int nsems = 0, nwaits = 0;
-    for (auto &t : tasks)
-        if (t.signals)
-            t.sem = nsems++;
-    // one instruction stream per CTA, in program order
+    for (int id : live)
+        if (tasks[id].signals)
+            tasks[id].sem = nsems++;
+    // one instruction stream per CTA, in program order; the extra
+    // destination lists go to a table of their own
     std::vector<std::vector<int4>> prog(ctas);
-    for (size_t id = 0; id < tasks.size(); ++id) {
+    std::vector<int> xtable;
+    for (int id : live) {
         const Task &t = tasks[id];
         for (int d : t.deps) {
             prog[t.cta].push_back(make_int4(kInstrWait, tasks[d].sem, 0, 0));
             ++nwaits;
         }
-        prog[t.cta].push_back(make_int4(kInstrTask, t.step, t.chunk, 0));
+        int x = -1;
+        if (!t.xdst.empty()) {
+            x = (int)xtable.size();
+            xtable.push_back((int)t.xdst.size());
+            xtable.insert(xtable.end(), t.xdst.begin(), t.xdst.end());
+        }
+        prog[t.cta].push_back(make_int4(kInstrTask, t.step, t.chunk, x));
         if (t.signals)
             prog[t.cta].push_back(make_int4(kInstrSignal, t.sem, 0, 0));
     }
@@ -390,7 +486,7 @@ static int compile_plan(ar_handle_t h, const ar_op *ops, int nops, int nchunks,
     p->esz = info.elem_size;
     const uint64_t per_vec = 16 / p->esz;
     p->chunk = ceil_div_u(ceil_div_u(p->N, (uint64_t)nchunks), per_vec) * per_vec;
-    p->ntasks = (int)tasks.size();
+    p->ntasks = (int)live.size();
     p->nwaits = nwaits;
     p->nsignals = nsems;
     const size_t b_steps = sizeof(PlanStep) * steps.size();
@@ -398,8 +494,10 @@ static int compile_plan(ar_handle_t h, const ar_op *ops, int nops, int nchunks,
     const size_t b_start = sizeof(int) * start.size();
     const size_t b_sems = sizeof(uint32_t) * (nsems + 1);
     const size_t b_epoch = sizeof(uint32_t) * (ctas + 1);    // + the plan's abort word
+    const size_t b_xdst = sizeof(int) * (xtable.size() + 1);
     auto up = [](size_t x) { return (x + 255) / 256 * 256; };
-    const size_t total = up(b_steps) + up(b_instr) + up(b_start) + up(b_sems) + up(b_epoch);
+    const size_t total =
+        up(b_steps) + up(b_instr) + up(b_start) + up(b_sems) + up(b_epoch) + up(b_xdst);
     if (cudaMalloc(&p->dev, total) != cudaSuccess) {
         (void)cudaGetLastError();
         delete p;
@@ -412,11 +510,15 @@ static int compile_plan(ar_handle_t h, const ar_op *ops, int nops, int nchunks,
     p->sems = reinterpret_cast<uint32_t *>(base + up(b_steps) + up(b_instr) + up(b_start));
     p->epoch = reinterpret_cast<uint32_t *>(base + up(b_steps) + up(b_instr) + up(b_start) +
                                             up(b_sems));
+    p->xdst = reinterpret_cast<int *>(base + up(b_steps) + up(b_instr) + up(b_start) +
+                                      up(b_sems) + up(b_epoch));
     if (cudaMemset(p->dev, 0, total) != cudaSuccess ||
         cudaMemcpy(p->steps, steps.data(), b_steps, cudaMemcpyHostToDevice) != cudaSuccess ||
         (flat.size() && cudaMemcpy(p->instr, flat.data(), sizeof(int4) * flat.size(),
                                    cudaMemcpyHostToDevice) != cudaSuccess) ||
         cudaMemcpy(p->start, start.data(), b_start, cudaMemcpyHostToDevice) != cudaSuccess ||
+        (xtable.size() && cudaMemcpy(p->xdst, xtable.data(), sizeof(int) * xtable.size(),
+                                     cudaMemcpyHostToDevice) != cudaSuccess) ||
         cudaDeviceSynchronize() != cudaSuccess) {
         (void)cudaGetLastError();
         cudaFree(p->dev);
@@ -546,6 +648,7 @@ extern "C" int ar_plan_execute(ar_plan_t p, const void *const in[], void *const 
     a.chunk = p->chunk;
     a.steps = p->steps;
     a.instr = p->instr;
+    a.xdst = p->xdst;
     a.start = p->start;
     a.sems = p->sems;
     a.epoch = p->epoch;

@@ -355,12 +355,18 @@ typedef struct ar_op {
 
 typedef struct ar_plan *ar_plan_t;
 
-/* Compile `nops` steps for the handle's R, N and dtype.  Each step over k
+/* Compile `nops` steps for the handle's R, N and dtype ("【论文分享】MSCCL++：
+ * 让 GPU 通信像 CUDA 一样可编程", section "第二层：DSL API": dependency analysis,
+ * synchronisation, operator fusion, an execution plan).  Each step over k
  * chunks becomes k tasks; task (step, c) runs on CTA rank * ctas_per_rank +
- * c % ctas_per_rank.  A task waits for every earlier task in another CTA
- * whose chunk it reads after a write, writes after a read, or writes after
- * a write; those producers signal a semaphore.  Allocates the plan's device
- * memory and waits for the upload (not a hot-path call).
+ * c % ctas_per_rank.  A copy task whose source chunk was last written by an
+ * earlier task t, and whose destination chunk no task has touched since t,
+ * is fused into t (t also stores its result there) and disappears; the
+ * results are those of running the steps one after another.  A task waits
+ * for every earlier task in another CTA whose chunk it reads after a write,
+ * writes after a read, or writes after a write; those producers signal a
+ * semaphore.  Allocates the plan's device memory and waits for the upload
+ * (not a hot-path call).
  * Errors: AR_ERR_INVALID (bad step, range), AR_ERR_UNSUPPORTED (R *
  * ctas_per_rank CTAs cannot all be resident, or the steps make more than
  * 2^20 tasks), AR_ERR_NOMEM (device or host memory), AR_ERR_CUDA. */
@@ -386,8 +392,8 @@ int ar_plan_builtin(ar_handle_t h, int algo, int chunks_per_rank, int ctas_per_r
  * through ar_status on the handle, and the plan must then be rebuilt. */
 int ar_plan_execute(ar_plan_t p, const void *const in[], void *const out[], cudaStream_t stream);
 
-/* Tasks, inserted waits and signalling tasks of a compiled plan (any
- * pointer may be NULL). */
+/* Tasks (after fusion), inserted waits and signalling tasks of a compiled
+ * plan (any pointer may be NULL). */
 int ar_plan_stats(ar_plan_t p, int *tasks, int *waits, int *signals);
 
 /* Free a plan (waits for the device first).  NULL is accepted. */

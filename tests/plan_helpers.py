@@ -24,14 +24,15 @@ def builtin_steps(R, algo, K):
     return steps
 
 
-def random_steps(R, nchunks, nsteps, seed):
-    """Random copy/reduce steps with plenty of cross-rank dependencies."""
+def random_steps(R, nchunks, nsteps, seed, copy_weight=1):
+    """Random copy/reduce steps with plenty of cross-rank dependencies
+    (copies are `copy_weight` times as likely as with the default mix)."""
     rng = random.Random(seed)
     steps = []
     for _ in range(nsteps):
         cb = rng.randrange(nchunks)
         ce = rng.randrange(cb + 1, nchunks + 1)
-        kind = rng.choice(["copy", "reduce", "reduce"])
+        kind = rng.choice(["copy"] * copy_weight + ["reduce", "reduce"])
         src_kind = rng.choice([0, 1])
         if kind == "copy":
             srcs = [src_kind * R + rng.randrange(R)]

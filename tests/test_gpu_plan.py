@@ -31,10 +31,11 @@ def test_builtin_plans(algo, dtype, R, n, K, G):
     with ar.Handle(R, n, dtype) as h:
         p = ar.ar_plan_builtin(h.h, algo, K, G)
         tasks, waits, signals = ar.ar_plan_stats(p)
-        if algo == "one_shot":
-            assert waits == 0 and signals == 0          # no dependencies at all
-        else:
-            assert waits > 0 and signals > 0
+        # one-shot: R ranks reduce every chunk, no dependencies at all;
+        # two-shot: every all-gather copy fuses into its shard's reduction,
+        # which leaves R * K reductions with R destinations and no waits
+        assert tasks == (R * R * K if algo == "one_shot" else R * K)
+        assert waits == 0 and signals == 0
         for _ in range(2):                               # two runs: run index advances
             ar.ar_plan_execute(p, ins, outs)
         assert ar.ar_status(h.h) == ar.AR_OK
@@ -65,6 +66,75 @@ def test_random_programs(seed, G):
     for r in range(R):
         assert_bits_equal(outs[r], want_out[r], dtype, "seed %d out %d" % (seed, r))
         assert_bits_equal(ins[r], want_in[r], dtype, "seed %d in %d" % (seed, r))
+
+
+@pytest.mark.parametrize("seed", range(8))
+def test_random_copy_heavy_programs(seed):
+    """Mostly copies between outputs: long chains the compiler fuses into
+    earlier tasks, and copies it must not fuse."""
+    need_gpu()
+    R, n, nch, dtype = 5, 30001, 5, ["bf16", "fp16", "fp32"][seed % 3]
+    steps = random_steps(R, nch, 40, 1000 + seed, copy_weight=3)
+    _run_program(steps, R, n, nch, dtype, G=2, seed=seed)
+
+
+def _run_program(steps, R, n, nch, dtype, G, seed, want_tasks=None):
+    cpu = wl.make_inputs(87, R, n, dtype, "uniform")
+    start = [wl.bits(t) for t in wl.make_inputs(88, R, n, dtype, "uniform")]
+    want_in = [wl.bits(t).copy() for t in cpu]
+    want_out = oracle.plan_run(steps, want_in, [a.copy() for a in start],
+                               wl.DTYPE_CODE[dtype], nch)
+    ins = device_inputs(cpu)
+    outs = [wl.from_bits(a, dtype).cuda() for a in start]
+    with ar.Handle(R, n, dtype) as h:
+        p = ar.ar_plan_compile(h.h, to_ops(steps, R), nch, G)
+        tasks, _, _ = ar.ar_plan_stats(p)
+        ar.ar_plan_execute(p, ins, outs)
+        assert ar.ar_status(h.h) == ar.AR_OK
+        ar.ar_plan_destroy(p)
+    if want_tasks is not None:
+        assert tasks == want_tasks
+    for r in range(R):
+        assert_bits_equal(outs[r], want_out[r], dtype, "case %s out %d" % (seed, r))
+        assert_bits_equal(ins[r], want_in[r], dtype, "case %s in %d" % (seed, r))
+
+
+def _red(rank, dst, srcs, nch):
+    return dict(kind="reduce", rank=rank, dst=dst, srcs=srcs, cbeg=0, cend=nch)
+
+
+def _cp(rank, dst, src, nch):
+    return dict(kind="copy", rank=rank, dst=dst, srcs=[src], cbeg=0, cend=nch)
+
+
+# Buffer ids with R = 4: in[b] = b, out[r] = 4 + r.  Every case runs on 3
+# chunks, so a step is 3 tasks; `fused` is how many copy steps the compiler
+# may fold into earlier tasks.
+FUSION_CASES = {
+    # out1 is read between the reduce and the copy into it: no fusion
+    "read_between": ([_red(0, 4, [0, 1], 3), _cp(1, 6, 5, 3), _cp(2, 5, 4, 3)], 0),
+    # out1 is written between the reduce and the copy into it: no fusion
+    "write_between": ([_red(0, 4, [0, 1], 3), _cp(1, 5, 3, 3), _cp(2, 5, 4, 3)], 0),
+    # the copy's destination is one of the reduce's sources: no fusion
+    "dst_is_source": ([_red(0, 4, [5, 6], 3), _cp(1, 5, 4, 3)], 0),
+    # a chain out0 -> out1 -> out2 -> out3: all three copies fold into the reduce
+    "chain": ([_red(0, 4, [0, 1, 2, 3], 3), _cp(1, 5, 4, 3), _cp(2, 6, 5, 3),
+               _cp(3, 7, 6, 3)], 3),
+    # the source is rewritten before the copy: it folds into the later writer
+    "rewritten_source": ([_red(0, 4, [0, 1], 3), _red(1, 4, [2, 3], 3), _cp(2, 5, 4, 3)], 1),
+    # two copies into one destination: each folds into its own producer
+    "two_producers": ([_red(0, 4, [0, 1], 3), _cp(1, 6, 4, 3), _red(2, 5, [2, 3], 3),
+                       _cp(3, 6, 5, 3)], 2),
+    # copy from an input (never written by the plan): nothing to fold into
+    "from_input": ([_cp(0, 4, 1, 3), _red(1, 5, [4, 6], 3)], 0),
+}
+
+
+@pytest.mark.parametrize("case", sorted(FUSION_CASES))
+def test_fusion_rules(case):
+    need_gpu()
+    steps, fused = FUSION_CASES[case]
+    _run_program(steps, 4, 5003, 3, "bf16", G=2, seed=case, want_tasks=3 * (len(steps) - fused))
 
 
 def test_plan_in_a_captured_graph_with_new_inputs():
