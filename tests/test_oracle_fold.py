@@ -1,6 +1,9 @@
 """Pins for the oracle's all-reduce fold and its reduce-scatter step.
 
-None of these re-types the fold.  They check it against:
+The first four kinds of check below do not restate the fold.  The last
+restates it with independent host libraries (numpy's binary32 adds, torch's
+narrowing casts) that share no code with the oracle's C arithmetic.  The
+oracle is checked against:
   * hand-derived IEEE cases (tests/golden/fold_cases.json), which fix the rank
     order, binary32 accumulation, a single final rounding, the start from
     rank 0's value (signed zeros), subnormals and overflow;
@@ -10,7 +13,9 @@ None of these re-types the fold.  They check it against:
   * brute-force binary64 sums within the error bound of an (R-1)-add binary32
     fold plus one final rounding;
   * invariants: identical outputs, a single non-zero rank, x and -x,
-    R = 1, rank permutation.
+    R = 1, rank permutation;
+  * torch on the host: for R = 2, (a.float() + b.float()).to(dtype); for any
+    R, an elementwise numpy binary32 left fold narrowed by torch's cast.
 """
 import numpy as np
 import pytest
@@ -192,3 +197,30 @@ def test_reduce_scatter_writes_only_its_shard(dtype, R, n):
         o = as_uint(outs[j], dtype)
         assert np.array_equal(o[lo:hi], as_uint(full, dtype)[lo:hi])
         assert np.all(o[:lo] == sentinel) and np.all(o[hi:] == sentinel)
+
+
+@pytest.mark.parametrize("dtype", DTYPES)
+@pytest.mark.parametrize("dist", ["uniform", "normal", "loguniform"])
+def test_two_ranks_equal_torch_add(dtype, dist):
+    """R = 2: one binary32 add and one rounding, i.e. torch's own
+    (a.float() + b.float()).to(dtype) on the host."""
+    a, b = wl.make_inputs(60, 2, 20011, dtype, dist)
+    want = wl.bits((a.float() + b.float()).to(wl.TORCH_DTYPE[dtype]))
+    got = _run([wl.bits(a), wl.bits(b)], dtype)[0]
+    assert np.array_equal(as_uint(got, dtype), as_uint(want, dtype))
+
+
+@pytest.mark.parametrize("dtype", DTYPES)
+@pytest.mark.parametrize("R", [3, 8, 32])
+@pytest.mark.parametrize("dist", ["normal", "loguniform"])
+def test_equals_numpy_binary32_left_fold(dtype, R, dist):
+    """Any R: numpy's elementwise binary32 adds in rank order (IEEE round to
+    nearest even, no contraction), narrowed once by torch's cast."""
+    ins = wl.make_inputs(61, R, 7001, dtype, dist)
+    acc = ins[0].float().numpy().copy()
+    with np.errstate(over="ignore"):
+        for t in ins[1:]:
+            acc = acc + t.float().numpy()
+    want = wl.bits(torch.from_numpy(acc).to(wl.TORCH_DTYPE[dtype]))
+    got = _run([wl.bits(t) for t in ins], dtype)[0]
+    assert np.array_equal(as_uint(got, dtype), as_uint(want, dtype))
