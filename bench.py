@@ -327,6 +327,7 @@ class CaseRunner:
                 ar.ar_allreduce(self.h.h, self.ins, self.outs, self.algo, self.proto,
                                 stream=stream)
 
+        self.call = call
         with torch.cuda.stream(stream):
             call()
         stream.synchronize()
@@ -517,9 +518,53 @@ def run_ours(args, dist: Dist):
     }
     if variants is not None:
         line["variants_us_per_call"] = variants
+    if args.workload in ("sweep", "decode"):
+        eager = measure_eager(runners, stream, flush)
+        line["eager_us_per_call"] = eager
+        if dist.rank == 0:
+            print_table(runners, sweep, eager)
     for r in runners:
         r.close()
     return line
+
+
+def measure_eager(runners, stream, flush, warmup=2, calls=10):
+    """µs/call of the same calls launched one by one, without a graph: two
+    warm-up calls, then the mean of `calls` calls after an L2 flush
+    (informative; not part of `value`)."""
+    import torch
+    out = {}
+    for r in runners:
+        with torch.cuda.stream(stream):
+            for _ in range(warmup):
+                r.call()
+            flush.fill_(3)
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            for _ in range(calls):
+                r.call()
+            e1.record(stream)
+        e1.synchronize()
+        out[str(r.w.n)] = round(e0.elapsed_time(e1) * 1e3 / calls, 3)
+    return out
+
+
+def print_table(runners, sweep, eager):
+    """GitHub-style markdown table of the sweep, on stderr (stdout carries
+    the one JSON line)."""
+    from all_reduce_reduction_gb300 import workload as wl
+    rows = ["| msg_size | eager µs/call | graph µs/call | algbw GB/s | busbw GB/s | min-bytes GB/s |",
+            "|---|---|---|---|---|---|"]
+    for r in runners:
+        k = str(r.w.n)
+        sw = sweep[k]
+        size = r.w.n * wl.ELEM_SIZE[r.w.dtype]
+        label = "%d KiB" % (size >> 10) if size < (1 << 20) else "%d MiB" % (size >> 20)
+        rows.append("| %s | %.2f | %.2f | %.1f | %.1f | %.1f |" % (
+            label, eager[k], sw["us_per_call"], sw["algbw_GBps"], sw["busbw_GBps"],
+            sw["min_bytes_GBps"]))
+    sys.stderr.write("\n".join(rows) + "\n")
 
 
 def measure_variants(runners, stream, flush, K):
