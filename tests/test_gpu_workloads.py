@@ -33,6 +33,8 @@ def run_graph(w, algo, proto, cpu, calls=10, warm=2, transport=ar.AR_LL_AUTO):
     s = torch.cuda.Stream()
     with ar.Handle(w.R, w.n, w.dtype) as h:
         ar.ar_set_ll_transport(h.h, transport)
+        if algo == ar.AR_ALGO_AUTO or proto == ar.AR_PROTO_AUTO:
+            ar.ar_tune(h.h, s)                           # as the decode benchmark does
         with torch.cuda.stream(s):
             ar.ar_allreduce(h.h, ins, outs, algo, proto, stream=s)
         s.synchronize()
@@ -62,7 +64,8 @@ def test_ll_sweep_sizes(path, transport):
             assert_bits_equal(outs[r], want, w.dtype, "%s rank %d" % (w.name, r))
 
 
-@pytest.mark.parametrize("path", ALL_PATHS, ids=PATH_IDS)
+@pytest.mark.parametrize("path", ALL_PATHS + [(ar.AR_ALGO_AUTO, ar.AR_PROTO_AUTO)],
+                         ids=PATH_IDS + ["auto_tuned"])
 def test_decode_shapes(path):
     """R=8 bf16 [B, 8192], B in 1, 8, 32, 128, 256, N(0, 1)."""
     need_gpu()
