@@ -227,6 +227,7 @@ KERNEL_SOURCES = {
     "one_shot_hb": ["ar_hb.cu"],
     "two_shot_hb": ["ar_tma.cu"],
     "combine": ["ar_combine.cu"],
+    "plan_": ["ar_plan.cu"],
 }
 
 
@@ -498,8 +499,11 @@ def run_ours(args, dist: Dist):
         "vs_baseline": None, "dtype": runners[0].w.dtype, "data": "synthetic",
         "config": {"workload": desc, "R": runners[0].w.R,
                    "sizes_elems_per_rank": [r.w.n for r in runners],
-                   "algo": cases[0]["algo"], "proto": cases[0]["proto"],
-                   "ll_transport": args.ll_transport if cases[0]["proto"] == "ll" else None,
+                   "algo": None if cases[0].get("plan") else cases[0]["algo"],
+                   "proto": None if cases[0].get("plan") else cases[0]["proto"],
+                   "plan": cases[0].get("plan"),
+                   "ll_transport": (args.ll_transport if cases[0]["proto"] == "ll"
+                                    and not cases[0].get("plan") else None),
                    "calls_per_graph": cases[0]["calls"],
                    "programmatic_dependent_launch": not args.no_pdl,
                    "l2": ("flushed (256 MiB write) before every graph replay, outside the timed events"
