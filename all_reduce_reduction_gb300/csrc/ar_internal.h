@@ -19,6 +19,7 @@ constexpr int kEpochWords = 8192;
 // Threads per CTA of the register (non-TMA) kernels and the LL kernels.
 constexpr int kRegThreads = 256;
 constexpr int kLlThreads = 128;
+constexpr int kLlStagedThreads = 256;   // one-shot LL with shared receive staging
 
 // One-shot HB: slots of the shared-memory ring that stages the inputs.
 constexpr int kOneShotStages = 4;
@@ -162,6 +163,9 @@ cudaError_t launch_two_shot_tma(const TmaArgs &a, int dtype, int grid, cudaStrea
 cudaError_t ll_occupancy(int dtype, bool vec, bool two_shot, int *blocks_per_sm);
 cudaError_t launch_ll(const LlArgs &a, int dtype, bool vec, bool two_shot, cudaStream_t s,
                       bool pdl = false);
+cudaError_t ll_staged_occupancy(int dtype, int *blocks_per_sm);
+cudaError_t launch_ll_staged(const LlArgs &a, int dtype, int ctas, cudaStream_t s,
+                             bool pdl = false);
 cudaError_t launch_pack(const PackArgs &a, int dtype, bool vec, int grid, cudaStream_t s,
                         bool pdl = false);
 cudaError_t launch_unpack(const PackArgs &a, int dtype, bool vec, int grid, cudaStream_t s,

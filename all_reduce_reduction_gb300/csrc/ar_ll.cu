@@ -232,6 +232,144 @@ __global__ void __launch_bounds__(kLlThreads) k_ll(const __grid_constant__ LlArg
     publish_epoch(a.c, flag);
 }
 
+// ---------------------------------------------------------------------------
+// One-shot LL with shared receive staging (every buffer 8-byte aligned).  A
+// CTA serves blocks of UB = blockDim / R units for all R virtual ranks.
+// Thread (k, j) = (tid / UB, tid % UB):
+//   put:     stores rank k's packet pair of unit j of the block after each
+//            of its blocks (block b + 1 mod nblk), so the packets a CTA
+//            receives were stored by another CTA;
+//   receive: polls sender k's pair of unit j of its own block once (bounded)
+//            and stages the payload in shared memory; after a barrier the
+//            same thread, now receiver k, folds the R staged payloads of
+//            unit j in rank order into out[k].
+// Every receiver still folds every sender's payload itself; the R receivers
+// of a unit share the one poll of each packet, as the one-shot HB shares its
+// input loads, so the packets cross L2 R times less often.  The last (< 8)
+// message bytes travel as single packets, put by the last CTA and received
+// by CTA 0.  Forward progress and in place: as for k_ll (all puts precede
+// all waits; out[k]'s unit is written only after its packet, hence its input
+// read, has been seen).
+// ---------------------------------------------------------------------------
+template <int DT>
+__global__ void __launch_bounds__(kLlStagedThreads) k_ll_staged(const __grid_constant__ LlArgs a) {
+    constexpr int ESZ = Elem<DT>::kSize;
+    __shared__ uint2 stage[kLlStagedThreads];
+    __shared__ uint32_t stage1[2 * AR_MAX_RANKS];        // single packets: [rank][0..1]
+    kernel_prologue();
+    const uint32_t flag = call_flag(a.c);
+    Poller w{&a.c, flag, 0};
+    const int R = a.R;
+    const uint32_t tid = threadIdx.x;
+    const uint32_t UB = blockDim.x / (uint32_t)R;         // units per block
+    const uint32_t k = tid / UB, j = tid - k * UB;
+    const bool member = k < (uint32_t)R;                  // tid < R * UB
+    const uint32_t nbytes = (uint32_t)a.n * ESZ;
+    const uint32_t U = nbytes / 8;                        // packet pairs per rank
+    const uint32_t ntail = (nbytes + 3) / 4 - 2 * U;      // 0, 1 or 2 single packets
+    const uint32_t nblk = (U + UB - 1) / UB;
+    const uint32_t ppad = (uint32_t)a.ppad;
+    uint64_t *const slot_k = a.slots + (member ? k : 0) * ppad;
+
+    // ---- put -----------------------------------------------------------------
+    if (member && a.c.drop_rank != (int)k) {
+        const uint2 *src = reinterpret_cast<const uint2 *>(a.p.in[k]);
+        for (uint32_t b = blockIdx.x; b < nblk; b += gridDim.x) {
+            const uint32_t u = (b + 1 == nblk ? 0 : b + 1) * UB + j;
+            if (u < U) {
+                const uint2 v = ld_v2(src + u);
+                st_pkt2(slot_k + 2 * u, make_pkt(v.x, flag), make_pkt(v.y, flag));
+            }
+        }
+        if (blockIdx.x == gridDim.x - 1 && j < ntail)
+            st_pkt(slot_k + 2 * U + j,
+                   make_pkt(load_payload<ESZ>(a.p.in[k], a.n, 2 * U + j), flag));
+    }
+
+    // ---- receive -----------------------------------------------------------------
+    bool ok = true, aborted = false;
+    for (uint32_t b = blockIdx.x; b < nblk; b += gridDim.x) {        // uniform per CTA
+        const uint32_t u = b * UB + j;
+        const bool live = member && u < U;
+        if (live && ok) {
+            uint64_t p0, p1;
+            ok = poll_pkt2(w, slot_k + 2 * u, p0, p1);
+            stage[tid] = make_uint2(pkt_payload(p0), pkt_payload(p1));
+        }
+        if (__syncthreads_or(!ok)) {
+            aborted = true;                               // someone gave up: all leave
+            break;
+        }
+        if (live) {
+            WordAcc<DT> a0, a1;
+            a0.init(stage[j].x);
+            a1.init(stage[j].y);
+            for (int s = 1; s < R; ++s) {
+                const uint2 x = stage[(uint32_t)s * UB + j];
+                a0.add(x.x);
+                a1.add(x.y);
+            }
+            st_v2(reinterpret_cast<uint2 *>(a.p.out[k]) + u, make_uint2(a0.result(), a1.result()));
+        }
+        __syncthreads();                                  // the stage is refilled next block
+    }
+    if (!aborted && blockIdx.x == 0 && ntail > 0) {
+        const bool tl = member && j < ntail;
+        if (tl) {
+            uint64_t p = 0;
+            ok = poll_pkt(w, slot_k + 2 * U + j, p);
+            stage1[2 * k + j] = pkt_payload(p);
+        }
+        if (!__syncthreads_or(!ok) && tl) {
+            WordAcc<DT> acc;
+            acc.init(stage1[j]);
+            for (int s = 1; s < R; ++s)
+                acc.add(stage1[2 * s + j]);
+            store_payload<ESZ>(a.p.out[k], a.n, 2 * U + j, acc.result());
+        }
+    }
+
+    publish_epoch(a.c, flag);
+}
+
+template <int DT> static const void *ll_staged_kernel() {
+    return reinterpret_cast<const void *>(&k_ll_staged<DT>);
+}
+
+static const void *ll_staged_for(int dtype) {
+    switch (dtype) {
+    case AR_BF16: return ll_staged_kernel<AR_BF16>();
+    case AR_FP16: return ll_staged_kernel<AR_FP16>();
+    default: return ll_staged_kernel<AR_FP32>();
+    }
+}
+
+cudaError_t ll_staged_occupancy(int dtype, int *blocks_per_sm) {
+    return cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks_per_sm, ll_staged_for(dtype),
+                                                         kLlStagedThreads, 0);
+}
+
+// gridDim = ctas, each serving all R ranks (a.G is not used).
+cudaError_t launch_ll_staged(const LlArgs &a, int dtype, int ctas, cudaStream_t s, bool pdl) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)ctas);
+    cfg.blockDim = dim3(kLlStagedThreads);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeCooperative;
+    attr[0].val.cooperative = 1;
+    cfg.numAttrs = 1;
+    if (pdl) {
+        attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[1].val.programmaticStreamSerializationAllowed = 1;
+        cfg.numAttrs = 2;
+    }
+    cfg.attrs = attr;
+    void *args[] = {const_cast<LlArgs *>(&a)};
+    return cudaLaunchKernelExC(&cfg, ll_staged_for(dtype), args);
+}
+
 template <int DT, bool VEC, bool TWO> static const void *ll_kernel() {
     return reinterpret_cast<const void *>(&k_ll<DT, VEC, TWO>);
 }
