@@ -9,6 +9,12 @@
 // all-gather all-reduce algorithms of "SGLang 中的 MSCCL++ All-Reduce 基准测试与
 // 推理集成指南", section 4.4.
 //
+// Two kernels.  k_ll_staged runs the one-shot schedule when every buffer is
+// 8-byte aligned: its CTAs serve all R ranks for a block of units, and the R
+// receivers of a unit share one poll of each packet (see its comment).
+// k_ll runs the two-shot schedule and the unaligned one-shot with per-rank
+// CTAs, as follows.
+//
 // Virtual peers.  The R ranks' kernels are emulated as one kernel over all
 // ranks' data: CTA b works for virtual rank r = b % R (CTA gi = b / R of its
 // G CTAs).  A rank "puts" its input into its own slot of the handle's

@@ -231,9 +231,35 @@ KERNEL_SOURCES = {
 }
 
 
+def strip_comments(src: str) -> str:
+    """C/C++ source without its comments and with whitespace runs collapsed
+    (string and character literals kept as they are)."""
+    out, i, n = [], 0, len(src)
+    while i < n:
+        c = src[i]
+        if c in "\"'":
+            j = i + 1
+            while j < n and src[j] != c:
+                j += 2 if src[j] == "\\" else 1
+            out.append(src[i:j + 1])
+            i = j + 1
+        elif src.startswith("//", i):
+            j = src.find("\n", i)
+            i = n if j < 0 else j
+        elif src.startswith("/*", i):
+            j = src.find("*/", i + 2)
+            out.append(" ")
+            i = n if j < 0 else j + 2
+        else:
+            out.append(c)
+            i += 1
+    return " ".join("".join(out).split())
+
+
 def kernel_source_digest(kernel_key: str) -> str:
     """Digest of the device code a kernel key names: its .cu file plus the
-    shared device header.  Any edit to them invalidates recorded counters."""
+    shared device header, comments and layout aside.  Any change to the code
+    invalidates recorded counters."""
     files = None
     for prefix, fs in KERNEL_SOURCES.items():
         if kernel_key.startswith(prefix):
@@ -243,7 +269,7 @@ def kernel_source_digest(kernel_key: str) -> str:
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "all_reduce_reduction_gb300", "csrc")
     for fn in files + ["ar_device.cuh"]:
-        h.update(open(os.path.join(csrc, fn), "rb").read())
+        h.update(strip_comments(open(os.path.join(csrc, fn)).read()).encode())
     return h.hexdigest()[:16]
 
 

@@ -129,3 +129,10 @@ def test_threaded_oracle_timing_runs_every_case():
 def test_rank_stride_keeps_every_rank_256_byte_aligned(n, esz):
     st = bench.rank_stride(n, esz)
     assert st >= n and (st * esz) % 256 == 0 and (st - n) * esz < 256
+
+
+def test_digest_ignores_comments_but_not_code():
+    src = 'int a = 1; // note\n/* block */ asm("ld.global.u32 %0, [%1]; // not a comment");\n'
+    assert bench.strip_comments(src) == bench.strip_comments(src.replace("note", "other words"))
+    assert "// not a comment" in bench.strip_comments(src)
+    assert bench.strip_comments(src) != bench.strip_comments(src.replace("a = 1", "a = 2"))
