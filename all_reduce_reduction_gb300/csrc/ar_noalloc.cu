@@ -33,7 +33,8 @@ struct DeviceState {
     bool ready;
     uint8_t *base;          // device address of g_noalloc_scratch on this device
     int num_sms;
-    int cap[3][2];          // co-resident one-shot LL CTAs [dtype][vec]
+    int cap[3][2];          // co-resident per-rank one-shot LL CTAs [dtype][vec]
+    int staged_cap[3];      // co-resident CTAs of the staged one-shot LL [dtype]
 };
 
 std::mutex g_setup_lock;
@@ -69,6 +70,14 @@ int setup(int dev, DeviceState **out) {
                 }
                 s.cap[dt][v] = per_sm * s.num_sms;
             }
+        for (int dt = 0; dt < 3; ++dt) {
+            int per_sm = 0;
+            if (ar::ll_staged_occupancy(dt, &per_sm) != cudaSuccess) {
+                (void)cudaGetLastError();
+                return AR_ERR_CUDA;
+            }
+            s.staged_cap[dt] = per_sm * s.num_sms;
+        }
         s.base = static_cast<uint8_t *>(ptr);
         s.ready = true;
     }
@@ -137,6 +146,26 @@ extern "C" int ar_allreduce_ll_static(int R, size_t N, int dtype, const void *co
     a.c.epoch = reinterpret_cast<uint32_t *>(s->base + kCtlBytes);
     a.c.timeout_ns = 1000000000ull;
     a.c.drop_rank = -1;
+    if (vec) {
+        // 8-byte aligned: the staged kernel (CTAs serving all R ranks)
+        int cap = s->staged_cap[dtype];
+        if (cap > ar::kEpochWords)
+            cap = ar::kEpochWords;
+        if (cap < 1)
+            return AR_ERR_UNSUPPORTED;
+        const uint64_t ub = ar::kLlStagedThreads / R;
+        uint64_t ctas = (N * esz / 8 + ub - 1) / ub;
+        if (ctas < 1)
+            ctas = 1;
+        if (ctas > (uint64_t)cap)
+            ctas = (uint64_t)cap;
+        a.G = 0;
+        if (ar::launch_ll_staged(a, dtype, (int)ctas, stream) != cudaSuccess) {
+            (void)cudaGetLastError();
+            return AR_ERR_CUDA;
+        }
+        return AR_OK;
+    }
     int gmax = s->cap[dtype][vec ? 1 : 0] / R;
     if (gmax > ar::kEpochWords / R)
         gmax = ar::kEpochWords / R;
