@@ -268,8 +268,10 @@ int bucket_of(uint64_t bytes) {
 
 // Resolve AR_ALGO_AUTO / AR_PROTO_AUTO for a message of `bytes` per rank:
 // the fastest tuned (algo, proto) allowed by the fixed half of the request,
-// or, before ar_tune, a fixed rule from GB300 measurements (one-shot HB up to
-// 256 KiB per rank, two-shot HB above; with LL forced, one-shot up to 2 MiB).
+// or, before ar_tune, a fixed rule from GB300 measurements: one-shot HB up to
+// 2 MiB / R per rank (its fold work grows with R^2: the measured crossovers
+// are about 512 KiB at R = 4, 256 KiB at R = 8, 128 KiB at R = 16, 32-128
+// KiB at R = 32), two-shot HB above; with LL forced, one-shot up to 2 MiB.
 void resolve(const ar_handle *h, uint64_t bytes, int *algo, int *proto) {
     const bool ll_ok = h->slots != nullptr;
     if (h->tuned_max >= 0) {
@@ -300,7 +302,7 @@ void resolve(const ar_handle *h, uint64_t bytes, int *algo, int *proto) {
     if (*proto == AR_PROTO_AUTO)
         *proto = AR_HB;
     if (*algo == AR_ALGO_AUTO) {
-        const uint64_t limit = *proto == AR_LL ? (2u << 20) : (256u << 10);
+        const uint64_t limit = *proto == AR_LL ? (2u << 20) : (2u << 20) / (uint64_t)h->R;
         *algo = bytes <= limit ? AR_ONE_SHOT : AR_TWO_SHOT;
     }
 }

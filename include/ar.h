@@ -197,7 +197,7 @@ int ar_allreduce(ar_handle_t h, const void *const in[], void *const out[],
  * ceil(n/R) rounded up to a 16-byte vector).  Buffers need n elements.
  * With AR_ALGO_AUTO and/or AR_PROTO_AUTO the library picks the half left
  * open, per message size: the tuned fastest choice after ar_tune, else a
- * fixed rule from GB300 measurements (HB; one-shot up to 256 KiB per rank,
+ * fixed rule from GB300 measurements (HB; one-shot up to 2 MiB / R per rank,
  * two-shot above; with AR_LL forced, one-shot up to 2 MiB).
  * Errors: as ar_allreduce; AR_ERR_INVALID also for n == 0 or n > N. */
 int ar_allreduce_n(ar_handle_t h, const void *const in[], void *const out[], size_t n,

@@ -53,13 +53,16 @@ def test_n_out_of_range_rejected():
             ar.ar_allreduce_n(h.h, x, y, 10, 7, ar.AR_HB)
 
 
-def test_untuned_rule():
+@pytest.mark.parametrize("R", [4, 8, 16, 32])
+def test_untuned_rule(R):
+    """Before ar_tune: HB, one-shot up to 2 MiB / R per rank, two-shot above."""
     need_gpu()
-    with ar.Handle(8, 1 << 22, "bf16") as h:
+    limit = (2 << 20) // R
+    with ar.Handle(R, 1 << 21, "bf16") as h:
         assert ar.ar_get_tuning(h.h, 4096)[:2] == (ar.AR_ONE_SHOT, ar.AR_HB)
-        assert ar.ar_get_tuning(h.h, 256 << 10)[:2] == (ar.AR_ONE_SHOT, ar.AR_HB)
-        assert ar.ar_get_tuning(h.h, (256 << 10) + 2)[:2] == (ar.AR_TWO_SHOT, ar.AR_HB)
-        assert ar.ar_get_tuning(h.h, 8 << 20)[2] == [0.0, 0.0, 0.0, 0.0]
+        assert ar.ar_get_tuning(h.h, limit)[:2] == (ar.AR_ONE_SHOT, ar.AR_HB)
+        assert ar.ar_get_tuning(h.h, limit + 2)[:2] == (ar.AR_TWO_SHOT, ar.AR_HB)
+        assert ar.ar_get_tuning(h.h, 4 << 20)[2] == [0.0, 0.0, 0.0, 0.0]
 
 
 @pytest.mark.parametrize("R,dtype", [(8, "bf16"), (4, "fp32"), (16, "fp16")])
