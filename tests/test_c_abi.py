@@ -65,3 +65,30 @@ def test_header_is_c11_and_every_entry_point_links(tmp_path):
            "-L" + os.path.dirname(lib), "-lar_gb300", "-Wl,-rpath," + os.path.dirname(lib)]
     res = subprocess.run(cmd, capture_output=True, text=True)
     assert res.returncode == 0, res.stderr
+
+
+@pytest.mark.skipif(shutil.which("g++") is None, reason="no C++ compiler")
+def test_header_is_usable_from_cpp17(tmp_path):
+    """The same header from C++ (its extern "C" block): a C++17 program
+    calling a few entry points compiles and links without name mangling."""
+    lib = cuda_build.build()
+    src = tmp_path / "use_ar.cpp"
+    src.write_text(r'''
+#include "ar.h"
+#include <cstdio>
+int main() {
+    ar_handle_t h = nullptr;
+    if (ar_create(8, 4096, AR_BF16, &h) != AR_OK)
+        return 1;
+    ar_info info{};
+    ar_get_info(h, &info);
+    std::printf("%s %d\n", ar_strerror(ar_status(h, nullptr)), info.R);
+    return ar_destroy(h);
+}
+''')
+    exe = tmp_path / "use_ar_cpp"
+    cmd = ["g++", "-std=c++17", "-Wall", "-Wextra", "-Werror", "-pedantic",
+           "-I" + os.path.join(ROOT, "include"), "-I" + CUDA_INC, str(src), "-o", str(exe),
+           "-L" + os.path.dirname(lib), "-lar_gb300", "-Wl,-rpath," + os.path.dirname(lib)]
+    res = subprocess.run(cmd, capture_output=True, text=True)
+    assert res.returncode == 0, res.stderr
