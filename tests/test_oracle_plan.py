@@ -87,3 +87,60 @@ def test_bad_plan_rejected():
     with pytest.raises(ValueError):
         oracle.plan_run([dict(kind="copy", rank=0, dst=2, srcs=[0, 1], cbeg=0, cend=1)],
                         ins, _sentinel_outs(2, 10, "bf16"), DT_CODE["bf16"], 1)
+
+
+def _python_plan(steps, ins, outs, dtype, nchunks):
+    """The plain meaning of a plan, restated with numpy and torch: steps one
+    after another; chunk c is elements [c*C, min((c+1)*C, n)) with
+    C = ceil(n / nchunks) rounded up to a whole 16-byte vector; a copy moves
+    bits; a reduce is a binary32 left fold of its sources in the listed order,
+    narrowed once by torch's cast."""
+    import torch
+    R, n = len(ins), ins[0].size
+    per_vec = 16 // {"bf16": 2, "fp16": 2, "fp32": 4}[dtype]
+    C = -(-(-(-n // nchunks)) // per_vec) * per_vec
+    bufs = [a.copy() for a in ins] + [a.copy() for a in outs]
+    for st in steps:
+        for c in range(st["cbeg"], st["cend"]):
+            lo, hi = min(c * C, n), min((c + 1) * C, n)
+            if lo >= hi:
+                continue
+            if st["kind"] == "copy":
+                bufs[st["dst"]][lo:hi] = bufs[st["srcs"][0]][lo:hi]
+                continue
+            with np.errstate(over="ignore"):
+                acc = decode64(bufs[st["srcs"][0]][lo:hi], dtype).astype(np.float32)
+                for b in st["srcs"][1:]:
+                    acc = acc + decode64(bufs[b][lo:hi], dtype).astype(np.float32)
+            y = wl.bits(torch.from_numpy(acc.copy()).to(wl.TORCH_DTYPE[dtype]))
+            bufs[st["dst"]][lo:hi] = y
+    return bufs[:R], bufs[R:]
+
+
+@pytest.mark.parametrize("dtype", DTYPES)
+@pytest.mark.parametrize("seed", range(6))
+def test_random_programs_match_a_python_restatement(dtype, seed):
+    """Random copy/reduce programs (writes into inputs included): the oracle's
+    plan interpreter against an independent restatement of the plan's
+    meaning, bit for bit, on every buffer."""
+    import random
+    rng = random.Random(seed)
+    R, n, nch = 4, 101 + seed * 37, 5
+    steps = []
+    for _ in range(16):
+        cb = rng.randrange(nch)
+        ce = rng.randrange(cb + 1, nch + 1)
+        kind = rng.choice(["copy", "reduce"])
+        sk = rng.choice([0, 1])
+        srcs = [sk * R + rng.randrange(R)] if kind == "copy" else \
+            [sk * R + rng.randrange(R) for _ in range(rng.randint(1, R))]
+        steps.append(dict(kind=kind, rank=rng.randrange(R), dst=rng.randrange(2 * R),
+                          srcs=srcs, cbeg=cb, cend=ce))
+    ins = _ins(R, n, dtype, config=81, dist="normal")
+    outs = [wl.bits(t) for t in wl.make_inputs(82, R, n, dtype, "normal")]
+    want_in, want_out = _python_plan(steps, ins, outs, dtype, nch)
+    got_in, got_out = [a.copy() for a in ins], [a.copy() for a in outs]
+    oracle.plan_run(steps, got_in, got_out, DT_CODE[dtype], nch)
+    for r in range(R):
+        assert np.array_equal(as_uint(got_in[r], dtype), as_uint(want_in[r], dtype))
+        assert np.array_equal(as_uint(got_out[r], dtype), as_uint(want_out[r], dtype))
