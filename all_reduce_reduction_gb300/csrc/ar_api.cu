@@ -33,7 +33,7 @@ struct ar_handle {
     uint64_t ppad;          // packets per slot
     uint64_t shard;         // two-shot shard S, elements
     int ll_cap[2][2];       // co-resident LL CTAs [vec][two_shot]
-    int ll_staged_cap;      // co-resident CTAs of the staged one-shot LL kernel
+    int ll_staged_cap[2];   // co-resident CTAs of the staged LL kernels [two_shot]
     int one_shot_warps;     // warps per CTA of the one-shot HB kernel
     int one_shot_cap;       // CTAs of the one-shot HB kernel per launch
     int reg_cap;            // CTAs of the 256-thread kernels per launch
@@ -227,18 +227,18 @@ int ll(ar_handle *h, const Call &c, bool two) {
     a.R = h->R;
     a.c = h->ctl;
     const uint64_t nbytes = c.n * h->esz;
-    if (!two && c.vec8) {
-        // one-shot, aligned: CTAs serving all R ranks a block of units each,
-        // the receivers of a unit sharing its packets' polls
+    if (c.vec8) {
+        // aligned: CTAs serving all R ranks a block of units each, the
+        // receivers of a unit sharing its packets' polls
         const uint64_t ub = kLlStagedThreads / h->R;
-        int cap = h->ll_staged_cap;
+        int cap = h->ll_staged_cap[two ? 1 : 0];
         if (cap > kEpochWords)
             cap = kEpochWords;
         if (cap < 1)
             return AR_ERR_UNSUPPORTED;
         a.G = 0;
         const int ctas = clamp_grid(ceil_div(nbytes / 8, ub), cap);
-        return from_cuda(launch_ll_staged(a, h->dtype, ctas, c.s, h->pdl));
+        return from_cuda(launch_ll_staged(a, h->dtype, two, ctas, c.s, h->pdl));
     }
     const uint64_t work = c.vec8 ? nbytes / 8 + 1 : (nbytes + 3) / 4;   // units per rank
     const int cap = h->ll_cap[c.vec8 ? 1 : 0][two ? 1 : 0];
@@ -392,10 +392,10 @@ int ar_create(int R, size_t N, int dtype, ar_handle_t *out) {
             err |= ll_occupancy(dtype, v != 0, t != 0, &per_sm) != cudaSuccess;
             h->ll_cap[v][t] = per_sm * h->num_sms;
         }
-    {
+    for (int t = 0; t < 2; ++t) {
         int per_sm = 0;
-        err |= ll_staged_occupancy(dtype, &per_sm) != cudaSuccess;
-        h->ll_staged_cap = per_sm * h->num_sms;
+        err |= ll_staged_occupancy(dtype, t != 0, &per_sm) != cudaSuccess;
+        h->ll_staged_cap[t] = per_sm * h->num_sms;
     }
     h->one_shot_warps = R <= 8 ? R * ((8 + R - 1) / R) : R;
     h->one_shot_cap = h->num_sms * (2048 / (32 * h->one_shot_warps));

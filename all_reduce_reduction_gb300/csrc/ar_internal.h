@@ -163,8 +163,8 @@ cudaError_t launch_two_shot_tma(const TmaArgs &a, int dtype, int grid, cudaStrea
 cudaError_t ll_occupancy(int dtype, bool vec, bool two_shot, int *blocks_per_sm);
 cudaError_t launch_ll(const LlArgs &a, int dtype, bool vec, bool two_shot, cudaStream_t s,
                       bool pdl = false);
-cudaError_t ll_staged_occupancy(int dtype, int *blocks_per_sm);
-cudaError_t launch_ll_staged(const LlArgs &a, int dtype, int ctas, cudaStream_t s,
+cudaError_t ll_staged_occupancy(int dtype, bool two_shot, int *blocks_per_sm);
+cudaError_t launch_ll_staged(const LlArgs &a, int dtype, bool two_shot, int ctas, cudaStream_t s,
                              bool pdl = false);
 cudaError_t launch_pack(const PackArgs &a, int dtype, bool vec, int grid, cudaStream_t s,
                         bool pdl = false);

@@ -9,11 +9,11 @@
 // all-gather all-reduce algorithms of "SGLang 中的 MSCCL++ All-Reduce 基准测试与
 // 推理集成指南", section 4.4.
 //
-// Two kernels.  k_ll_staged runs the one-shot schedule when every buffer is
-// 8-byte aligned: its CTAs serve all R ranks for a block of units, and the R
-// receivers of a unit share one poll of each packet (see its comment).
-// k_ll runs the two-shot schedule and the unaligned one-shot with per-rank
-// CTAs, as follows.
+// Kernels.  When every buffer is 8-byte aligned, k_ll_staged (one-shot) and
+// k_ll2_staged (two-shot) run: their CTAs serve all R ranks for a block of
+// units, and the R receivers of a unit share one poll of each packet (see
+// their comments).  Otherwise k_ll runs either schedule with per-rank CTAs,
+// as follows.
 //
 // Virtual peers.  The R ranks' kernels are emulated as one kernel over all
 // ranks' data: CTA b works for virtual rank r = b % R (CTA gi = b / R of its
@@ -338,25 +338,167 @@ __global__ void __launch_bounds__(kLlStagedThreads) k_ll_staged(const __grid_con
     publish_epoch(a.c, flag);
 }
 
+// ---------------------------------------------------------------------------
+// Two-shot LL with shared staging (every buffer 8-byte aligned), on the same
+// blocks and thread roles as k_ll_staged:
+//   put:            as k_ll_staged (block b + 1 of every rank);
+//   reduce-scatter: for each of its blocks, thread (k, j) polls sender k's
+//                   pair of unit j once and stages it; after a barrier the
+//                   thread of the unit's shard owner folds the R payloads in
+//                   rank order and writes the reduced pair as a result
+//                   packet (slot R);
+//   all-gather:     for the block after each of its blocks (whose results
+//                   another CTA reduced), one thread per unit polls the
+//                   result pair once and stages it; after a barrier thread
+//                   (k, j) stores it to out[k].
+// Every wait depends only on work each CTA finishes before its own waits
+// (puts before reductions, reductions before gathers), so the cooperative
+// grid makes progress.  In place: out[k]'s units of block b + 1 are written
+// by the CTA that read in[k]'s units of that block in its put.  The last
+// (< 8) message bytes travel as single packets: put by the last CTA,
+// reduced by CTA 0, gathered by the last CTA.
+// ---------------------------------------------------------------------------
+template <int DT>
+__global__ void __launch_bounds__(kLlStagedThreads) k_ll2_staged(const __grid_constant__ LlArgs a) {
+    constexpr int ESZ = Elem<DT>::kSize;
+    __shared__ uint2 stage[kLlStagedThreads];
+    __shared__ uint32_t stage1[2 * AR_MAX_RANKS];        // single packets: [rank][0..1]
+    __shared__ uint32_t gather1[2];                      // their reduced values
+    kernel_prologue();
+    const uint32_t flag = call_flag(a.c);
+    Poller w{&a.c, flag, 0};
+    const int R = a.R;
+    const uint32_t tid = threadIdx.x;
+    const uint32_t UB = blockDim.x / (uint32_t)R;         // units per block
+    const uint32_t k = tid / UB, j = tid - k * UB;
+    const bool member = k < (uint32_t)R;                  // tid < R * UB
+    const uint32_t nbytes = (uint32_t)a.n * ESZ;
+    const uint32_t U = nbytes / 8;                        // packet pairs per rank
+    const uint32_t ntail = (nbytes + 3) / 4 - 2 * U;      // 0, 1 or 2 single packets
+    const uint32_t nblk = (U + UB - 1) / UB;
+    const uint32_t G = gridDim.x;
+    const uint32_t ppad = (uint32_t)a.ppad;
+    const uint32_t shard_pk = (uint32_t)(a.shard * ESZ / 4);   // packets per shard (even)
+    uint64_t *const slot_k = a.slots + (member ? k : 0) * ppad;
+    uint64_t *const res = a.slots + (uint32_t)R * ppad;         // result packets
+    auto owner = [&](uint32_t q) {                        // shard owner of packet q
+        const uint32_t o = q / shard_pk;
+        return o < (uint32_t)R ? o : (uint32_t)R - 1u;
+    };
+
+    // ---- put -----------------------------------------------------------------
+    if (member && a.c.drop_rank != (int)k) {
+        const uint2 *src = reinterpret_cast<const uint2 *>(a.p.in[k]);
+        for (uint32_t b = blockIdx.x; b < nblk; b += G) {
+            const uint32_t u = (b + 1 == nblk ? 0 : b + 1) * UB + j;
+            if (u < U) {
+                const uint2 v = ld_v2(src + u);
+                st_pkt2(slot_k + 2 * u, make_pkt(v.x, flag), make_pkt(v.y, flag));
+            }
+        }
+        if (blockIdx.x == G - 1 && j < ntail)
+            st_pkt(slot_k + 2 * U + j,
+                   make_pkt(load_payload<ESZ>(a.p.in[k], a.n, 2 * U + j), flag));
+    }
+
+    // ---- reduce-scatter: this CTA's blocks ----------------------------------
+    bool ok = true, aborted = false;
+    for (uint32_t b = blockIdx.x; b < nblk; b += G) {                // uniform per CTA
+        const uint32_t u = b * UB + j;
+        const bool live = member && u < U;
+        if (live && ok) {
+            uint64_t p0, p1;
+            ok = poll_pkt2(w, slot_k + 2 * u, p0, p1);
+            stage[tid] = make_uint2(pkt_payload(p0), pkt_payload(p1));
+        }
+        if (__syncthreads_or(!ok)) {
+            aborted = true;
+            break;
+        }
+        if (live && k == owner(2 * u)) {
+            WordAcc<DT> a0, a1;
+            a0.init(stage[j].x);
+            a1.init(stage[j].y);
+            for (int s = 1; s < R; ++s) {
+                const uint2 x = stage[(uint32_t)s * UB + j];
+                a0.add(x.x);
+                a1.add(x.y);
+            }
+            st_pkt2(res + 2 * u, make_pkt(a0.result(), flag), make_pkt(a1.result(), flag));
+        }
+        __syncthreads();                                  // the stage is refilled next block
+    }
+    if (!aborted && blockIdx.x == 0 && ntail > 0) {
+        const bool tl = member && j < ntail;
+        if (tl) {
+            uint64_t p = 0;
+            ok = poll_pkt(w, slot_k + 2 * U + j, p);
+            stage1[2 * k + j] = pkt_payload(p);
+        }
+        if (__syncthreads_or(!ok)) {
+            aborted = true;
+        } else if (tl && k == owner(2 * U + j)) {
+            WordAcc<DT> acc;
+            acc.init(stage1[j]);
+            for (int s = 1; s < R; ++s)
+                acc.add(stage1[2 * s + j]);
+            st_pkt(res + 2 * U + j, make_pkt(acc.result(), flag));
+        }
+    }
+
+    // ---- all-gather: the block after each of this CTA's blocks ---------------
+    for (uint32_t b = blockIdx.x; !aborted && b < nblk; b += G) {    // uniform per CTA
+        const uint32_t u = (b + 1 == nblk ? 0 : b + 1) * UB + j;
+        if (k == 0 && u < U && ok) {
+            uint64_t p0, p1;
+            ok = poll_pkt2(w, res + 2 * u, p0, p1);
+            stage[j] = make_uint2(pkt_payload(p0), pkt_payload(p1));
+        }
+        if (__syncthreads_or(!ok)) {
+            aborted = true;
+            break;
+        }
+        if (member && u < U)
+            st_v2(reinterpret_cast<uint2 *>(a.p.out[k]) + u, stage[j]);
+        __syncthreads();
+    }
+    if (!aborted && blockIdx.x == G - 1 && ntail > 0) {
+        if (k == 0 && j < ntail) {
+            uint64_t p = 0;
+            ok = poll_pkt(w, res + 2 * U + j, p);
+            gather1[j] = pkt_payload(p);
+        }
+        if (!__syncthreads_or(!ok) && member && j < ntail)
+            store_payload<ESZ>(a.p.out[k], a.n, 2 * U + j, gather1[j]);
+    }
+
+    publish_epoch(a.c, flag);
+}
+
+template <int DT> static const void *ll2_staged_kernel() {
+    return reinterpret_cast<const void *>(&k_ll2_staged<DT>);
+}
+
 template <int DT> static const void *ll_staged_kernel() {
     return reinterpret_cast<const void *>(&k_ll_staged<DT>);
 }
 
-static const void *ll_staged_for(int dtype) {
+static const void *ll_staged_for(int dtype, bool two) {
     switch (dtype) {
-    case AR_BF16: return ll_staged_kernel<AR_BF16>();
-    case AR_FP16: return ll_staged_kernel<AR_FP16>();
-    default: return ll_staged_kernel<AR_FP32>();
+    case AR_BF16: return two ? ll2_staged_kernel<AR_BF16>() : ll_staged_kernel<AR_BF16>();
+    case AR_FP16: return two ? ll2_staged_kernel<AR_FP16>() : ll_staged_kernel<AR_FP16>();
+    default: return two ? ll2_staged_kernel<AR_FP32>() : ll_staged_kernel<AR_FP32>();
     }
 }
 
-cudaError_t ll_staged_occupancy(int dtype, int *blocks_per_sm) {
-    return cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks_per_sm, ll_staged_for(dtype),
-                                                         kLlStagedThreads, 0);
+cudaError_t ll_staged_occupancy(int dtype, bool two_shot, int *blocks_per_sm) {
+    return cudaOccupancyMaxActiveBlocksPerMultiprocessor(
+        blocks_per_sm, ll_staged_for(dtype, two_shot), kLlStagedThreads, 0);
 }
 
 // gridDim = ctas, each serving all R ranks (a.G is not used).
-cudaError_t launch_ll_staged(const LlArgs &a, int dtype, int ctas, cudaStream_t s, bool pdl) {
+cudaError_t launch_ll_staged(const LlArgs &a, int dtype, bool two_shot, int ctas, cudaStream_t s,
+                             bool pdl) {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)ctas);
     cfg.blockDim = dim3(kLlStagedThreads);
@@ -373,7 +515,7 @@ cudaError_t launch_ll_staged(const LlArgs &a, int dtype, int ctas, cudaStream_t 
     }
     cfg.attrs = attr;
     void *args[] = {const_cast<LlArgs *>(&a)};
-    return cudaLaunchKernelExC(&cfg, ll_staged_for(dtype), args);
+    return cudaLaunchKernelExC(&cfg, ll_staged_for(dtype, two_shot), args);
 }
 
 template <int DT, bool VEC, bool TWO> static const void *ll_kernel() {

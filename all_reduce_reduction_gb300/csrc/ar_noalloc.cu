@@ -72,7 +72,7 @@ int setup(int dev, DeviceState **out) {
             }
         for (int dt = 0; dt < 3; ++dt) {
             int per_sm = 0;
-            if (ar::ll_staged_occupancy(dt, &per_sm) != cudaSuccess) {
+            if (ar::ll_staged_occupancy(dt, false, &per_sm) != cudaSuccess) {
                 (void)cudaGetLastError();
                 return AR_ERR_CUDA;
             }
@@ -160,7 +160,7 @@ extern "C" int ar_allreduce_ll_static(int R, size_t N, int dtype, const void *co
         if (ctas > (uint64_t)cap)
             ctas = (uint64_t)cap;
         a.G = 0;
-        if (ar::launch_ll_staged(a, dtype, (int)ctas, stream) != cudaSuccess) {
+        if (ar::launch_ll_staged(a, dtype, false, (int)ctas, stream) != cudaSuccess) {
             (void)cudaGetLastError();
             return AR_ERR_CUDA;
         }
