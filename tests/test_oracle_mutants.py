@@ -41,6 +41,12 @@ MUTANTS = {
     "combine_weights_transposed": ("float p = w[t * (size_t)K + (size_t)k]", "float p = w[(size_t)k * T + t]"),
     "flag_in_low_half": ("pkts[p] = ((uint64_t)flag << 32) | (uint64_t)payload;",
                          "pkts[p] = ((uint64_t)payload << 32) | (uint64_t)flag;"),
+    "plan_chunks_not_whole_vectors": ("C = (C + per_vec - 1) / per_vec * per_vec;", "C = C + 0 * per_vec;"),
+    "plan_last_chunk_dropped": ("for (c = cbeg[k]; c < cend[k]; ++c) {",
+                                "for (c = cbeg[k]; c < cend[k] - 1; ++c) {"),
+    "plan_in_and_out_swapped": ("d = dst[k] < R ? (void *)in[dst[k]] : out[dst[k] - R];",
+                                "d = dst[k] < R ? out[dst[k]] : (void *)in[dst[k] - R];"),
+    "plan_steps_reversed": ("for (k = 0; k < nsteps; ++k) {", "for (k = nsteps - 1; k >= 0; --k) {"),
 }
 
 
@@ -100,6 +106,24 @@ def _pins_pass(lib) -> bool:
     got = oracle.combine(ys, np.ldexp(1.0, e).astype(np.float32).reshape(-1), 4, 8, DT_CODE["fp32"], lib=lib)
     if not np.array_equal(got.view(np.uint32), want.view(np.uint32)):
         return False
+    # plans: a built-in two-shot plan is the all-reduce, and random programs
+    # equal a pure-Python restatement of a plan's meaning
+    from plan_helpers import builtin_steps
+    from test_oracle_plan import _python_plan, random_program
+    ins = [wl.bits(t) for t in wl.make_inputs(89, 5, 203, "bf16", "normal")]
+    outs = [np.zeros(203, np.uint16) for _ in range(5)]
+    got = oracle.plan_run(builtin_steps(5, "two_shot", 2), [a.copy() for a in ins], outs,
+                          DT_CODE["bf16"], 10, lib=lib)
+    want = oracle.allreduce(ins, DT_CODE["bf16"], lib=lib)
+    if any(not np.array_equal(got[r], want[r]) for r in range(5)):
+        return False
+    for seed in range(3):
+        steps, ins, outs, nch = random_program("bf16", seed)
+        w_in, w_out = _python_plan(steps, ins, outs, "bf16", nch)
+        g_in, g_out = [a.copy() for a in ins], [a.copy() for a in outs]
+        oracle.plan_run(steps, g_in, g_out, DT_CODE["bf16"], nch, lib=lib)
+        if any(not np.array_equal(a, b) for a, b in zip(g_in + g_out, w_in + w_out)):
+            return False
     # packets
     for case in golden("ll_packets.json")["cases"]:
         dt = case["dtype"]

@@ -117,12 +117,9 @@ def _python_plan(steps, ins, outs, dtype, nchunks):
     return bufs[:R], bufs[R:]
 
 
-@pytest.mark.parametrize("dtype", DTYPES)
-@pytest.mark.parametrize("seed", range(6))
-def test_random_programs_match_a_python_restatement(dtype, seed):
-    """Random copy/reduce programs (writes into inputs included): the oracle's
-    plan interpreter against an independent restatement of the plan's
-    meaning, bit for bit, on every buffer."""
+def random_program(dtype, seed):
+    """(steps, ins, outs, nchunks): 16 random copy/reduce steps over 4 ranks,
+    writes into inputs included, on seeded inputs."""
     import random
     rng = random.Random(seed)
     R, n, nch = 4, 101 + seed * 37, 5
@@ -138,6 +135,17 @@ def test_random_programs_match_a_python_restatement(dtype, seed):
                           srcs=srcs, cbeg=cb, cend=ce))
     ins = _ins(R, n, dtype, config=81, dist="normal")
     outs = [wl.bits(t) for t in wl.make_inputs(82, R, n, dtype, "normal")]
+    return steps, ins, outs, nch
+
+
+@pytest.mark.parametrize("dtype", DTYPES)
+@pytest.mark.parametrize("seed", range(6))
+def test_random_programs_match_a_python_restatement(dtype, seed):
+    """Random copy/reduce programs (writes into inputs included): the oracle's
+    plan interpreter against an independent restatement of the plan's
+    meaning, bit for bit, on every buffer."""
+    steps, ins, outs, nch = random_program(dtype, seed)
+    R = len(ins)
     want_in, want_out = _python_plan(steps, ins, outs, dtype, nch)
     got_in, got_out = [a.copy() for a in ins], [a.copy() for a in outs]
     oracle.plan_run(steps, got_in, got_out, DT_CODE[dtype], nch)
