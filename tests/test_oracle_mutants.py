@@ -47,6 +47,9 @@ MUTANTS = {
     "plan_in_and_out_swapped": ("d = dst[k] < R ? (void *)in[dst[k]] : out[dst[k] - R];",
                                 "d = dst[k] < R ? out[dst[k]] : (void *)in[dst[k] - R];"),
     "plan_steps_reversed": ("for (k = 0; k < nsteps; ++k) {", "for (k = nsteps - 1; k >= 0; --k) {"),
+    "shards_not_whole_vectors": ("    S = (S + per_vec - 1) / per_vec * per_vec;\n    a = (size_t)j * S;",
+                                 "    S = S + 0 * per_vec;\n    a = (size_t)j * S;"),
+    "shards_floor_division": ("size_t S = (N + (size_t)R - 1) / (size_t)R;", "size_t S = N / (size_t)R;"),
 }
 
 
@@ -124,6 +127,33 @@ def _pins_pass(lib) -> bool:
         oracle.plan_run(steps, g_in, g_out, DT_CODE["bf16"], nch, lib=lib)
         if any(not np.array_equal(a, b) for a, b in zip(g_in + g_out, w_in + w_out)):
             return False
+    # shards: a partition of [0, N) into R ranges, every boundary on a whole
+    # 16-byte vector (or at N), at most one vector of difference in length
+    # between consecutive full shards; the reduce-scatter writes only shard j
+    # (33 = 4 * 8 + 1: floor(n / R) is already a whole vector, so a floor in
+    # place of the ceiling would leave the last element in no shard)
+    for dt, R, n in (("bf16", 4, 4097 * 3 + 3), ("fp32", 5, 9), ("fp16", 16, 1001),
+                     ("bf16", 4, 33)):
+        per_vec = 16 // wl.ELEM_SIZE[dt]
+        bounds = [oracle.shard_bounds(R, n, DT_CODE[dt], j, lib=lib) for j in range(R)]
+        if bounds[0][0] != 0 or bounds[-1][1] != n:
+            return False
+        if any(bounds[j][1] != bounds[j + 1][0] for j in range(R - 1)):
+            return False
+        if any(lo % per_vec and lo != n for lo, _ in bounds):
+            return False
+        if bounds[0][1] - bounds[0][0] < -(-n // R):     # the first shard holds ceil(n/R) or more
+            return False
+        ins = [wl.bits(t) for t in wl.make_inputs(87, R, n, dt, "normal")]
+        full = oracle.allreduce(ins, DT_CODE[dt], lib=lib)[0]
+        outs = [np.zeros(n, ins[0].dtype) for _ in range(R)]
+        oracle.reduce_scatter(ins, DT_CODE[dt], outs, lib=lib)
+        for j, (lo, hi) in enumerate(bounds):
+            if not np.array_equal(as_uint(outs[j][lo:hi], dt), as_uint(full[lo:hi], dt)):
+                return False
+            rest = np.concatenate([as_uint(outs[j][:lo], dt), as_uint(outs[j][hi:], dt)])
+            if rest.any():
+                return False
     # packets
     for case in golden("ll_packets.json")["cases"]:
         dt = case["dtype"]
