@@ -50,6 +50,11 @@ MUTANTS = {
     "shards_not_whole_vectors": ("    S = (S + per_vec - 1) / per_vec * per_vec;\n    a = (size_t)j * S;",
                                  "    S = S + 0 * per_vec;\n    a = (size_t)j * S;"),
     "shards_floor_division": ("size_t S = (N + (size_t)R - 1) / (size_t)R;", "size_t S = N / (size_t)R;"),
+    "combine_starts_at_positive_zero": (
+        "float acc = w[t * (size_t)K] * load_widened(dtype, y[0], i);\n            for (k = 1; k < K; ++k) {",
+        "float acc = 0.0f;\n            for (k = 0; k < K; ++k) {"),
+    "unpack_accepts_any_flag": ("        if (f != flag) {\n            ++bad;\n            continue;\n        }",
+                                "        if (f != flag)\n            ++bad;"),
 }
 
 
@@ -154,12 +159,19 @@ def _pins_pass(lib) -> bool:
             rest = np.concatenate([as_uint(outs[j][:lo], dt), as_uint(outs[j][hi:], dt)])
             if rest.any():
                 return False
-    # packets
+    # packets, and an unpack that must leave the destination alone where the
+    # flag does not match
     for case in golden("ll_packets.json")["cases"]:
         dt = case["dtype"]
         x = hex_array(case["elements"], dt)
         pk = oracle.ll_pack(x, DT_CODE[dt], int(case["flag"], 16), lib=lib)
         if [int(p) for p in pk] != [int(h, 16) for h in case["packets"]]:
+            return False
+        keep = np.full(x.size, 0x5A5A, np.uint32 if dt == "fp32" else np.uint16)
+        keep = keep.view(np.float32) if dt == "fp32" else keep
+        dst, bad = oracle.ll_unpack(pk, DT_CODE[dt], x.size, int(case["flag"], 16) ^ 1,
+                                    dst=keep.copy(), lib=lib)
+        if bad != len(pk) or not np.array_equal(as_uint(dst, dt), as_uint(keep, dt)):
             return False
     return True
 
