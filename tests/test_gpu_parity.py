@@ -283,6 +283,14 @@ def test_ll_rejected_above_cap():
         ar.ar_allreduce(h.h, x, x, ar.AR_TWO_SHOT, ar.AR_HB)   # HB still serves it
 
 
+@pytest.mark.parametrize("algo", [ar.AR_ONE_SHOT, ar.AR_TWO_SHOT], ids=["one_shot", "two_shot"])
+def test_ll_at_the_cap(algo):
+    """The largest message LL accepts: exactly AR_LL_MAX_BYTES per rank."""
+    need_gpu()
+    R, n = 2, ar.AR_LL_MAX_BYTES // 2
+    run_case(R, n, "bf16", algo, ar.AR_LL, dist="normal", config=44)
+
+
 def test_too_few_buffers_rejected():
     """The binding pads pointer arrays with NULL: fewer buffers than ranks is
     an argument error, never a read past the array."""
