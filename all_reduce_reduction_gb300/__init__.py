@@ -66,6 +66,7 @@ class ar_info(ctypes.Structure):
         ("ll_cluster_units", ctypes.c_int),
         ("ll_cluster_max", ctypes.c_int),
         ("pdl", ctypes.c_int),
+        ("ll_staged_ctas_max", ctypes.c_int),
     ]
 
     def as_dict(self) -> dict:

@@ -32,7 +32,7 @@ struct ar_handle {
     uint64_t *slots;        // LL scratch, NULL if the handle is not LL capable
     uint64_t ppad;          // packets per slot
     uint64_t shard;         // two-shot shard S, elements
-    int ll_cap[2][2];       // co-resident LL CTAs [vec][two_shot]
+    int ll_cap[2];          // co-resident CTAs of the per-rank LL kernel [two_shot]
     int ll_staged_cap[2];   // co-resident CTAs of the staged LL kernels [two_shot]
     int one_shot_warps;     // warps per CTA of the one-shot HB kernel
     int one_shot_cap;       // CTAs of the one-shot HB kernel per launch
@@ -211,8 +211,8 @@ int ll_cluster(ar_handle *h, const Call &c) {
     return from_cuda(launch_ll_cluster(a, h->dtype, clamp_grid(nchunks, cap), c.s, h->pdl));
 }
 
-// LL: the global-memory kernel's vector path needs 8-byte alignment, the
-// cluster kernel 16-byte alignment.
+// LL: the staged kernels need every buffer 8-byte aligned, the cluster
+// kernel 16-byte aligned; other buffers take the per-rank kernel.
 int ll(ar_handle *h, const Call &c, bool two) {
     if (!h->slots)
         return AR_ERR_UNSUPPORTED;
@@ -240,15 +240,15 @@ int ll(ar_handle *h, const Call &c, bool two) {
         const int ctas = clamp_grid(ceil_div(nbytes / 8, ub), cap);
         return from_cuda(launch_ll_staged(a, h->dtype, two, ctas, c.s, h->pdl));
     }
-    const uint64_t work = c.vec8 ? nbytes / 8 + 1 : (nbytes + 3) / 4;   // units per rank
-    const int cap = h->ll_cap[c.vec8 ? 1 : 0][two ? 1 : 0];
-    int gmax = cap / h->R;
+    // not 8-byte aligned: per-rank CTAs, one packet per unit
+    const uint64_t work = (nbytes + 3) / 4;
+    int gmax = h->ll_cap[two ? 1 : 0] / h->R;
     if (gmax > kEpochWords / h->R)
         gmax = kEpochWords / h->R;
     if (gmax < 1)
         return AR_ERR_UNSUPPORTED;                 // cannot keep R CTAs resident
     a.G = clamp_grid(ceil_div(work, kLlThreads), gmax);
-    return from_cuda(launch_ll(a, h->dtype, c.vec8, two, c.s, h->pdl));
+    return from_cuda(launch_ll(a, h->dtype, two, c.s, h->pdl));
 }
 
 int run_path(ar_handle *h, const Call &c, int algo, int proto) {
@@ -386,14 +386,10 @@ int ar_create(int R, size_t N, int dtype, ar_handle_t *out) {
 
     // launch shapes
     int err = 0;
-    for (int v = 0; v < 2; ++v)
-        for (int t = 0; t < 2; ++t) {
-            int per_sm = 0;
-            err |= ll_occupancy(dtype, v != 0, t != 0, &per_sm) != cudaSuccess;
-            h->ll_cap[v][t] = per_sm * h->num_sms;
-        }
     for (int t = 0; t < 2; ++t) {
         int per_sm = 0;
+        err |= ll_occupancy(dtype, t != 0, &per_sm) != cudaSuccess;
+        h->ll_cap[t] = per_sm * h->num_sms;
         err |= ll_staged_occupancy(dtype, t != 0, &per_sm) != cudaSuccess;
         h->ll_staged_cap[t] = per_sm * h->num_sms;
     }
@@ -797,7 +793,7 @@ int ar_get_info(ar_handle_t h, ar_info *info) {
     info->ll_packets_per_rank = (h->N * h->esz + 3) / 4;
     info->scratch_bytes = h->dev_bytes;
     info->num_sms = h->num_sms;
-    info->ll_ctas_per_rank_max = h->ll_cap[1][0] / h->R;
+    info->ll_ctas_per_rank_max = h->ll_cap[0] / h->R;
     info->tma_tile_bytes = h->tma_tile;
     info->tma_stages = h->tma_stages;
     info->timeout_ns = h->ctl.timeout_ns;
@@ -806,6 +802,7 @@ int ar_get_info(ar_handle_t h, ar_info *info) {
     info->ll_cluster_ok = h->cluster_ok ? 1 : 0;
     info->ll_cluster_units = h->cluster_ok ? (int)h->cluster_uc : 0;
     info->ll_cluster_max = h->cluster_ok ? h->cluster_max : 0;
+    info->ll_staged_ctas_max = h->ll_staged_cap[0] < kEpochWords ? h->ll_staged_cap[0] : kEpochWords;
     return AR_OK;
 }
 

@@ -160,9 +160,10 @@ cudaError_t launch_two_shot_tma(const TmaArgs &a, int dtype, int grid, cudaStrea
                                 bool pdl = false);
 
 // ar_ll.cu
-cudaError_t ll_occupancy(int dtype, bool vec, bool two_shot, int *blocks_per_sm);
-cudaError_t launch_ll(const LlArgs &a, int dtype, bool vec, bool two_shot, cudaStream_t s,
-                      bool pdl = false);
+// the per-rank kernel (buffers not all 8-byte aligned)
+cudaError_t ll_occupancy(int dtype, bool two_shot, int *blocks_per_sm);
+cudaError_t launch_ll(const LlArgs &a, int dtype, bool two_shot, cudaStream_t s, bool pdl = false);
+// the staged kernels (every buffer 8-byte aligned)
 cudaError_t ll_staged_occupancy(int dtype, bool two_shot, int *blocks_per_sm);
 cudaError_t launch_ll_staged(const LlArgs &a, int dtype, bool two_shot, int ctas, cudaStream_t s,
                              bool pdl = false);

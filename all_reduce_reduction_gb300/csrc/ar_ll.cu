@@ -12,8 +12,8 @@
 // Kernels.  When every buffer is 8-byte aligned, k_ll_staged (one-shot) and
 // k_ll2_staged (two-shot) run: their CTAs serve all R ranks for a block of
 // units, and the R receivers of a unit share one poll of each packet (see
-// their comments).  Otherwise k_ll runs either schedule with per-rank CTAs,
-// as follows.
+// their comments).  Otherwise k_ll runs either schedule with per-rank CTAs
+// and one packet per unit, as follows.
 //
 // Virtual peers.  The R ranks' kernels are emulated as one kernel over all
 // ranks' data: CTA b works for virtual rank r = b % R (CTA gi = b / R of its
@@ -46,42 +46,9 @@ __device__ __forceinline__ void st_v2(void *p, uint2 v) {
     asm volatile("st.global.v2.u32 [%0], {%1, %2};" :: "l"(p), "r"(v.x), "r"(v.y) : "memory");
 }
 
-// Fold the packet pair at `base` (packet offset inside a slot) of slots
-// 0..R-1, in rank order.  Loads of eight ranks are issued before any flag is
+// Fold the packet at `base` (packet offset inside a slot) of slots 0..R-1,
+// in rank order.  Loads of eight ranks are issued before any flag is
 // checked, so a ready message costs one round trip per eight ranks.
-template <int DT>
-__device__ __forceinline__ bool fold_pair(Poller &w, const uint64_t *base, uint32_t ppad, int R,
-                                          uint2 &out) {
-    WordAcc<DT> a0, a1;
-#pragma unroll 1
-    for (int k0 = 0; k0 < R; k0 += 8) {
-        uint64_t p0[8], p1[8];
-#pragma unroll
-        for (int j = 0; j < 8; ++j)
-            if (k0 + j < R)
-                ld_pkt2(base + (uint32_t)(k0 + j) * ppad, p0[j], p1[j]);
-#pragma unroll
-        for (int j = 0; j < 8; ++j) {
-            if (k0 + j < R) {
-                if (pkt_flag(p0[j]) != w.flag || pkt_flag(p1[j]) != w.flag) {
-                    if (!poll_pkt2(w, base + (uint32_t)(k0 + j) * ppad, p0[j], p1[j]))
-                        return false;
-                }
-                if (k0 + j == 0) {
-                    a0.init(pkt_payload(p0[j]));
-                    a1.init(pkt_payload(p1[j]));
-                } else {
-                    a0.add(pkt_payload(p0[j]));
-                    a1.add(pkt_payload(p1[j]));
-                }
-            }
-        }
-    }
-    out = make_uint2(a0.result(), a1.result());
-    return true;
-}
-
-// Same for a single packet.
 template <int DT>
 __device__ __forceinline__ bool fold_one(Poller &w, const uint64_t *base, uint32_t ppad, int R,
                                          uint32_t &out) {
@@ -109,10 +76,9 @@ __device__ __forceinline__ bool fold_one(Poller &w, const uint64_t *base, uint32
     return true;
 }
 
-// Units: with VEC every in/out buffer is 8-byte aligned and a unit is 8
-// message bytes = two packets; the last (< 8) bytes travel as single packets
-// handled by CTA gi == 0 of each rank.  Without VEC every packet is single.
-template <int DT, bool VEC, bool TWO>
+// Per-rank kernel for buffers that are not all 8-byte aligned: a unit is one
+// packet (4 message bytes; the last one may be partial).
+template <int DT, bool TWO>
 __global__ void __launch_bounds__(kLlThreads) k_ll(const __grid_constant__ LlArgs a) {
     constexpr int ESZ = Elem<DT>::kSize;
     const int R = a.R, G = a.G;
@@ -124,12 +90,8 @@ __global__ void __launch_bounds__(kLlThreads) k_ll(const __grid_constant__ LlArg
 
     const uint32_t nbytes = (uint32_t)a.n * ESZ;
     const uint32_t P = (nbytes + 3) / 4;                  // packets per rank
-    const uint32_t U = nbytes / 8;                        // packet pairs (VEC)
-    const uint32_t first1 = VEC ? 2 * U : 0;              // first single packet
-    // this thread's single packets (same set in every phase that uses them)
-    const uint32_t q0 = VEC ? (gi == 0 ? first1 + tid : P) : (uint32_t)gi * T + tid;
-    const uint32_t qstep = VEC ? T : (uint32_t)G * T;
-    const uint32_t ustart = (uint32_t)gi * T + tid, ustep = (uint32_t)G * T;
+    // this thread's packets (the same set in every phase that uses them)
+    const uint32_t q0 = (uint32_t)gi * T + tid, qstep = (uint32_t)G * T;
 
     const uint32_t ppad = (uint32_t)a.ppad;
     uint64_t *const slot_r = a.slots + (uint32_t)r * ppad;
@@ -138,39 +100,12 @@ __global__ void __launch_bounds__(kLlThreads) k_ll(const __grid_constant__ LlArg
 
     // ---- put: rank r's input -> slot r (one 8-byte store per packet) -------
     if (a.c.drop_rank != r) {
-        if constexpr (VEC) {
-            // four units' loads are in flight before the first packet store
-            constexpr int kPut = 4;
-            const uint2 *src = reinterpret_cast<const uint2 *>(a.p.in[r]);
-            for (uint32_t u0 = ustart; u0 < U; u0 += kPut * ustep) {
-                uint2 v[kPut];
-#pragma unroll
-                for (int j = 0; j < kPut; ++j)
-                    if (u0 + j * ustep < U)
-                        v[j] = ld_v2(src + u0 + j * ustep);
-#pragma unroll
-                for (int j = 0; j < kPut; ++j) {
-                    const uint32_t u = u0 + j * ustep;
-                    if (u < U)
-                        st_pkt2(slot_r + 2 * u, make_pkt(v[j].x, flag), make_pkt(v[j].y, flag));
-                }
-            }
-        }
         for (uint32_t q = q0; q < P; q += qstep)
             st_pkt(slot_r + q, make_pkt(load_payload<ESZ>(a.p.in[r], a.n, q), flag));
     }
 
     if (!TWO) {
         // ---- one-shot: out[r] = fold of every slot -------------------------
-        if constexpr (VEC) {
-            uint2 *dst = reinterpret_cast<uint2 *>(a.p.out[r]);
-            for (uint32_t u = ustart; ok && u < U; u += ustep) {
-                uint2 y;
-                ok = fold_pair<DT>(w, a.slots + 2 * u, ppad, R, y);
-                if (ok)
-                    st_v2(dst + u, y);
-            }
-        }
         for (uint32_t q = q0; ok && q < P; q += qstep) {
             uint32_t y;
             ok = fold_one<DT>(w, a.slots + q, ppad, R, y);
@@ -180,53 +115,17 @@ __global__ void __launch_bounds__(kLlThreads) k_ll(const __grid_constant__ LlArg
     } else {
         // ---- reduce-scatter: rank r folds shard r into result packets ------
         const uint32_t shard_pk = (uint32_t)(a.shard * ESZ / 4);   // packets per shard
-        if constexpr (VEC) {
-            const uint32_t lo = (uint32_t)r * (shard_pk / 2);
-            uint32_t hi = lo + shard_pk / 2;
-            if (hi > U)
-                hi = U;
-            for (uint32_t u = lo + ustart; ok && u < hi; u += ustep) {
-                uint2 y;
-                ok = fold_pair<DT>(w, a.slots + 2 * u, ppad, R, y);
-                if (ok)
-                    st_pkt2(res + 2 * u, make_pkt(y.x, flag), make_pkt(y.y, flag));
-            }
-            // single packets belong to the shard that holds them
-            if (gi == 0) {
-                for (uint32_t q = first1 + tid; ok && q < P; q += T) {
-                    int owner = (int)(q / shard_pk);
-                    if (owner > R - 1)
-                        owner = R - 1;
-                    if (owner != r)
-                        continue;
-                    uint32_t y;
-                    ok = fold_one<DT>(w, a.slots + q, ppad, R, y);
-                    if (ok)
-                        st_pkt(res + q, make_pkt(y, flag));
-                }
-            }
-        } else {
-            const uint32_t lo = (uint32_t)r * shard_pk;
-            uint32_t hi = lo + shard_pk;
-            if (hi > P)
-                hi = P;
-            for (uint32_t q = lo + ustart; ok && q < hi; q += ustep) {
-                uint32_t y;
-                ok = fold_one<DT>(w, a.slots + q, ppad, R, y);
-                if (ok)
-                    st_pkt(res + q, make_pkt(y, flag));
-            }
+        const uint32_t lo = (uint32_t)r * shard_pk;
+        uint32_t hi = lo + shard_pk;
+        if (hi > P)
+            hi = P;
+        for (uint32_t q = lo + q0; ok && q < hi; q += qstep) {
+            uint32_t y;
+            ok = fold_one<DT>(w, a.slots + q, ppad, R, y);
+            if (ok)
+                st_pkt(res + q, make_pkt(y, flag));
         }
         // ---- all-gather: out[r] <- result packets (same units as the put) --
-        if constexpr (VEC) {
-            uint2 *dst = reinterpret_cast<uint2 *>(a.p.out[r]);
-            for (uint32_t u = ustart; ok && u < U; u += ustep) {
-                uint64_t p0, p1;
-                ok = poll_pkt2(w, res + 2 * u, p0, p1);
-                if (ok)
-                    st_v2(dst + u, make_uint2(pkt_payload(p0), pkt_payload(p1)));
-            }
-        }
         for (uint32_t q = q0; ok && q < P; q += qstep) {
             uint64_t p;
             ok = poll_pkt(w, res + q, p);
@@ -518,30 +417,25 @@ cudaError_t launch_ll_staged(const LlArgs &a, int dtype, bool two_shot, int ctas
     return cudaLaunchKernelExC(&cfg, ll_staged_for(dtype, two_shot), args);
 }
 
-template <int DT, bool VEC, bool TWO> static const void *ll_kernel() {
-    return reinterpret_cast<const void *>(&k_ll<DT, VEC, TWO>);
+template <int DT, bool TWO> static const void *ll_kernel() {
+    return reinterpret_cast<const void *>(&k_ll<DT, TWO>);
 }
 
-static const void *ll_kernel_for(int dtype, bool vec, bool two) {
-#define AR_LL_PICK(DT)                                                                  \
-    return vec ? (two ? ll_kernel<DT, true, true>() : ll_kernel<DT, true, false>())     \
-               : (two ? ll_kernel<DT, false, true>() : ll_kernel<DT, false, false>());
+static const void *ll_kernel_for(int dtype, bool two) {
     switch (dtype) {
-    case AR_BF16: AR_LL_PICK(AR_BF16)
-    case AR_FP16: AR_LL_PICK(AR_FP16)
-    default: AR_LL_PICK(AR_FP32)
+    case AR_BF16: return two ? ll_kernel<AR_BF16, true>() : ll_kernel<AR_BF16, false>();
+    case AR_FP16: return two ? ll_kernel<AR_FP16, true>() : ll_kernel<AR_FP16, false>();
+    default: return two ? ll_kernel<AR_FP32, true>() : ll_kernel<AR_FP32, false>();
     }
-#undef AR_LL_PICK
 }
 
-cudaError_t ll_occupancy(int dtype, bool vec, bool two_shot, int *blocks_per_sm) {
+cudaError_t ll_occupancy(int dtype, bool two_shot, int *blocks_per_sm) {
     return cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks_per_sm,
-                                                         ll_kernel_for(dtype, vec, two_shot),
+                                                         ll_kernel_for(dtype, two_shot),
                                                          kLlThreads, 0);
 }
 
-cudaError_t launch_ll(const LlArgs &a, int dtype, bool vec, bool two_shot, cudaStream_t s,
-                      bool pdl) {
+cudaError_t launch_ll(const LlArgs &a, int dtype, bool two_shot, cudaStream_t s, bool pdl) {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)(a.R * a.G));
     cfg.blockDim = dim3(kLlThreads);
@@ -558,7 +452,7 @@ cudaError_t launch_ll(const LlArgs &a, int dtype, bool vec, bool two_shot, cudaS
     }
     cfg.attrs = attr;
     void *args[] = {const_cast<LlArgs *>(&a)};
-    return cudaLaunchKernelExC(&cfg, ll_kernel_for(dtype, vec, two_shot), args);
+    return cudaLaunchKernelExC(&cfg, ll_kernel_for(dtype, two_shot), args);
 }
 
 // ---------------------------------------------------------------------------

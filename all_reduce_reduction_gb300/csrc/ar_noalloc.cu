@@ -33,7 +33,7 @@ struct DeviceState {
     bool ready;
     uint8_t *base;          // device address of g_noalloc_scratch on this device
     int num_sms;
-    int cap[3][2];          // co-resident per-rank one-shot LL CTAs [dtype][vec]
+    int cap[3];             // co-resident per-rank one-shot LL CTAs [dtype]
     int staged_cap[3];      // co-resident CTAs of the staged one-shot LL [dtype]
 };
 
@@ -61,22 +61,15 @@ int setup(int dev, DeviceState **out) {
             (void)cudaGetLastError();
             return AR_ERR_CUDA;
         }
-        for (int dt = 0; dt < 3; ++dt)
-            for (int v = 0; v < 2; ++v) {
-                int per_sm = 0;
-                if (ar::ll_occupancy(dt, v != 0, false, &per_sm) != cudaSuccess) {
-                    (void)cudaGetLastError();
-                    return AR_ERR_CUDA;
-                }
-                s.cap[dt][v] = per_sm * s.num_sms;
-            }
         for (int dt = 0; dt < 3; ++dt) {
-            int per_sm = 0;
-            if (ar::ll_staged_occupancy(dt, false, &per_sm) != cudaSuccess) {
+            int per_sm = 0, staged_per_sm = 0;
+            if (ar::ll_occupancy(dt, false, &per_sm) != cudaSuccess ||
+                ar::ll_staged_occupancy(dt, false, &staged_per_sm) != cudaSuccess) {
                 (void)cudaGetLastError();
                 return AR_ERR_CUDA;
             }
-            s.staged_cap[dt] = per_sm * s.num_sms;
+            s.cap[dt] = per_sm * s.num_sms;
+            s.staged_cap[dt] = staged_per_sm * s.num_sms;
         }
         s.base = static_cast<uint8_t *>(ptr);
         s.ready = true;
@@ -166,19 +159,20 @@ extern "C" int ar_allreduce_ll_static(int R, size_t N, int dtype, const void *co
         }
         return AR_OK;
     }
-    int gmax = s->cap[dtype][vec ? 1 : 0] / R;
+    // not 8-byte aligned: per-rank CTAs, one packet per unit
+    int gmax = s->cap[dtype] / R;
     if (gmax > ar::kEpochWords / R)
         gmax = ar::kEpochWords / R;
     if (gmax < 1)
         return AR_ERR_UNSUPPORTED;
-    const uint64_t work = vec ? N * esz / 8 + 1 : (N * esz + 3) / 4;
+    const uint64_t work = (N * esz + 3) / 4;
     uint64_t G = (work + ar::kLlThreads - 1) / ar::kLlThreads;
     if (G < 1)
         G = 1;
     if (G > (uint64_t)gmax)
         G = (uint64_t)gmax;
     a.G = (int)G;
-    if (ar::launch_ll(a, dtype, vec, false, stream) != cudaSuccess) {
+    if (ar::launch_ll(a, dtype, false, stream) != cudaSuccess) {
         (void)cudaGetLastError();
         return AR_ERR_CUDA;
     }

@@ -145,7 +145,8 @@ typedef struct ar_info {
     size_t ll_packets_per_rank;/* ceil(N * elem_size / 4)                      */
     size_t scratch_bytes;      /* device bytes the handle owns                 */
     int num_sms;               /* SMs of the handle's device                   */
-    int ll_ctas_per_rank_max;  /* co-resident CTAs per rank for LL kernels     */
+    int ll_ctas_per_rank_max;  /* co-resident CTAs per rank of the per-rank LL
+                                  kernel (buffers not all 8-byte aligned)     */
     int tma_tile_bytes;        /* per-rank tile of the two-shot TMA kernel     */
     int tma_stages;            /* pipeline stages of the two-shot TMA kernel   */
     uint64_t timeout_ns;       /* current device-side wait limit               */
@@ -154,6 +155,9 @@ typedef struct ar_info {
     int ll_cluster_units;      /* its 16-byte units per rank per chunk         */
     int ll_cluster_max;        /* its co-resident clusters                     */
     int pdl;                   /* 1 if launches use programmatic dependent launch */
+    int ll_staged_ctas_max;    /* CTAs of the staged one-shot LL kernel (every
+                                  buffer 8-byte aligned), each serving all R
+                                  ranks                                       */
 } ar_info;
 
 /* Create a handle for R virtual ranks of N elements of `dtype` each, on the

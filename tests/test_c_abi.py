@@ -92,3 +92,52 @@ int main() {
            "-L" + os.path.dirname(lib), "-lar_gb300", "-Wl,-rpath," + os.path.dirname(lib)]
     res = subprocess.run(cmd, capture_output=True, text=True)
     assert res.returncode == 0, res.stderr
+
+
+def _layout_program():
+    from all_reduce_reduction_gb300 import ar_info, ar_op
+    lines = ['#include "ar.h"', "#include <stddef.h>", "#include <stdio.h>", "int main(void) {"]
+    for cls in (ar_info, ar_op):
+        name = cls.__name__
+        lines.append('    printf("%s size %%zu\\n", sizeof(%s));' % (name, name))
+        for field, _ in cls._fields_:
+            lines.append('    printf("%s.%s %%zu\\n", offsetof(%s, %s));' % (name, field, name, field))
+    lines += ["    return 0;", "}"]
+    return "\n".join(lines) + "\n"
+
+
+@pytest.mark.skipif(shutil.which("gcc") is None, reason="no C compiler")
+def test_binding_structs_match_the_header_layout(tmp_path):
+    """Every field of the ctypes ar_info and ar_op sits at the offset the C
+    compiler gives it from include/ar.h, and the sizes agree (a field added
+    to one side only, or declared with another width, fails here)."""
+    import ctypes
+    from all_reduce_reduction_gb300 import ar_info, ar_op
+    src = tmp_path / "layout.c"
+    src.write_text(_layout_program())
+    exe = tmp_path / "layout"
+    cmd = ["gcc", "-std=c11", "-Wall", "-Wextra", "-Werror", "-I" + os.path.join(ROOT, "include"),
+           "-I" + CUDA_INC, str(src), "-o", str(exe)]
+    res = subprocess.run(cmd, capture_output=True, text=True)
+    assert res.returncode == 0, res.stderr
+    out = subprocess.run([str(exe)], capture_output=True, text=True, check=True).stdout.split("\n")
+    got = dict(line.rsplit(" ", 1) for line in out if line)
+    for cls in (ar_info, ar_op):
+        name = cls.__name__
+        assert int(got.pop("%s size" % name)) == ctypes.sizeof(cls), name
+        for field, _ in cls._fields_:
+            assert int(got.pop("%s.%s" % (name, field))) == getattr(cls, field).offset, (name, field)
+    assert not got
+    # and the header declares exactly the binding's fields, in order
+    import re
+    header = open(os.path.join(ROOT, "include", "ar.h")).read()
+    header = re.sub(r"/\*.*?\*/", "", header, flags=re.S)
+    for cls in (ar_info, ar_op):
+        body = re.search(r"typedef struct %s \{(.*?)\} %s;" % (cls.__name__, cls.__name__),
+                         header, re.S).group(1)
+        names = []
+        for decl in body.split(";"):
+            decl = re.sub(r"\[[^\]]*\]", "", decl).strip()
+            if decl:
+                names += [part.split()[-1] for part in decl.split(",")]
+        assert names == [f for f, _ in cls._fields_], cls.__name__
