@@ -76,6 +76,18 @@ def test_cluster_transport_available_up_to_eight_ranks():
             assert info["ll_cluster_ok"] == 1 and info["ll_cluster_max"] > 0, (R, info)
 
 
+def test_info_reports_launch_capacities():
+    need_gpu()
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    for R in (1, 8, 32):
+        with ar.Handle(R, 4096, "fp32") as h:
+            info = ar.ar_get_info(h.h)
+            assert info["num_sms"] == sms
+            # the staged kernel: at least one CTA per SM, at most one epoch word each
+            assert sms <= info["ll_staged_ctas_max"] <= 8192, info
+            assert info["ll_ctas_per_rank_max"] >= 1, info
+
+
 @pytest.mark.parametrize("transport", TRANSPORTS, ids=TRANSPORT_IDS)
 @pytest.mark.parametrize("offset", [0, 1])
 def test_ll_transports_in_place(transport, offset):

@@ -3,7 +3,9 @@ R in 1..32 and every dtype, through one-shot/two-shot x HB/LL, checked bit
 for bit against the oracle with canary zones on both sides of each output.
 These sizes cover every split of a message into whole 16-byte vectors, LL
 packet pairs, single packets and element tails, and every shard layout of
-the two-shot schedule with empty and short shards."""
+the two-shot schedule with empty and short shards.  Each size runs with
+every buffer 16-byte aligned, 8-byte aligned only (the staged LL kernels,
+element-wise HB) and element aligned only (the per-rank LL kernel)."""
 import numpy as np
 import pytest
 import torch
@@ -17,13 +19,16 @@ pytestmark = pytest.mark.gpu
 
 NMAX = 67
 # each rank's output row: GUARD canaries, a 72-element slot (a whole number of
-# 16-byte vectors, so every rank's output stays 16-byte aligned and the vector
-# paths run), GUARD canaries
+# 16-byte vectors, so every row starts 16-byte aligned), GUARD canaries
 ROW = GUARD + 72 + GUARD
+# byte offset of every input and output from a 16-byte boundary (None: one
+# element)
+ALIGNMENTS = {"a16": 0, "a8": 8, "elem": None}
 
 
+@pytest.mark.parametrize("align", list(ALIGNMENTS))
 @pytest.mark.parametrize("dtype", ["bf16", "fp16", "fp32"])
-def test_every_tiny_size_every_rank_count(dtype):
+def test_every_tiny_size_every_rank_count(dtype, align):
     need_gpu()
     u = np.uint32 if dtype == "fp32" else np.uint16
     cv = canary_value(dtype)
@@ -34,10 +39,15 @@ def test_every_tiny_size_every_rank_count(dtype):
         # prefix of the result for all NMAX elements
         want = np.ascontiguousarray(oracle.allreduce([wl.bits(t) for t in cpu],
                                                      wl.DTYPE_CODE[dtype])[0]).view(u)
-        ins = device_inputs(cpu)
+        esz = wl.ELEM_SIZE[dtype]
+        off = 1 if ALIGNMENTS[align] is None else ALIGNMENTS[align] // esz
+        ins = device_inputs(cpu, off)
         block = torch.empty((R, ROW), dtype=wl.TORCH_DTYPE[dtype], device="cuda")
-        outs = [block[r, GUARD:GUARD + NMAX] for r in range(R)]
-        assert all(o.data_ptr() % 16 == 0 for o in outs)
+        outs = [block[r, GUARD + off:GUARD + off + NMAX] for r in range(R)]
+        want_align = {"a16": 16, "a8": 8, "elem": esz}[align]
+        for t in ins + outs:
+            assert t.data_ptr() % want_align == 0
+            assert want_align == 16 or t.data_ptr() % (2 * want_align) != 0
         with ar.Handle(R, NMAX, dtype) as h:
             for n in range(1, NMAX + 1):
                 for algo, proto in ALL_PATHS:
@@ -49,10 +59,11 @@ def test_every_tiny_size_every_rank_count(dtype):
                         failures.append((R, n, algo, proto, "status " + ar.ar_strerror(st)))
                         continue
                     canary = np.array(cv, dtype=np.int64).astype(u)
-                    body = got[:, GUARD:GUARD + n]
+                    body = got[:, GUARD + off:GUARD + off + n]
                     if not (body == want[:n]).all():
                         r, i = np.argwhere(body != want[:n])[0]
                         failures.append((R, n, algo, proto, "rank %d element %d" % (r, i)))
-                    if not ((got[:, :GUARD] == canary).all() and (got[:, GUARD + n:] == canary).all()):
+                    if not ((got[:, :GUARD + off] == canary).all()
+                            and (got[:, GUARD + off + n:] == canary).all()):
                         failures.append((R, n, algo, proto, "write outside the message"))
     assert not failures, "%d failures, first: %s" % (len(failures), failures[:5])
