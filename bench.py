@@ -25,6 +25,7 @@ import argparse
 import hashlib
 import json
 import os
+import platform
 import statistics
 import subprocess
 import sys
@@ -36,6 +37,7 @@ sys.path.insert(0, ROOT)
 METRIC = ("all-reduce µs/call and GB/s vs msg size (R=8 bf16, 1 GB300), "
           "% of HBM roofline")
 FALLBACK_HBM_GBS = 6800.0
+NOMINAL_HBM_GBS = 7900.0        # GB300 HBM3e, nominal (context beside the measured peak)
 TRANSPORTS = {"auto": 0, "global": 1, "cluster": 2}   # enum ar_ll_transport
 L2_FLUSH_BYTES = 256 << 20
 
@@ -211,6 +213,24 @@ def clocks_rejected(c: dict | None) -> bool:
 # ---------------------------------------------------------------------------
 # peaks and committed ncu traffic
 # ---------------------------------------------------------------------------
+def ll_wire_bytes(r):
+    """Bytes the one-shot LL call moves through L2 with its packets counted
+    (8-byte packets carry 4 payload bytes): every input read, every packet
+    stored and loaded once, every output written.  None for other paths,
+    whose bytes are the minimal ones."""
+    import all_reduce_reduction_gb300 as ar
+    from all_reduce_reduction_gb300 import workload as wl
+    if r.c.get("plan") or r.c.get("combine"):
+        return None
+    if (r.choice or "%s_%s" % (r.c["algo"], r.c["proto"])) != "one_shot_ll":
+        return None
+    if r.c.get("transport", ar.AR_LL_AUTO) == ar.AR_LL_CLUSTER:
+        return None                     # its packets travel through shared memory
+    nb = r.w.n * wl.ELEM_SIZE[r.w.dtype]
+    packets = 8 * -(-nb // 4)
+    return r.w.R * (2 * nb + 2 * packets)
+
+
 def hbm_peak():
     try:
         with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
@@ -470,7 +490,9 @@ def run_ours(args, dist: Dist):
     roofline = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                 "frac": round(achieved / peak, 4), "traffic": committed_traffic(kkey),
                 "kernel": kkey, "peak_source": peak_kind + " (MEASURED_PEAKS.json hbm_gbs)"
-                if peak_kind == "measured" else "fallback 6800 GB/s"}
+                if peak_kind == "measured" else "fallback 6800 GB/s",
+                "nominal_peak": NOMINAL_HBM_GBS,
+                "frac_of_nominal": round(achieved / NOMINAL_HBM_GBS, 4)}
 
     sweep = {}
     for i, r in enumerate(runners):
@@ -484,6 +506,10 @@ def run_ours(args, dist: Dist):
             "frac_of_hbm_peak": round(r.bytes / us / 1e3 / peak, 4),
             "l2_resident": 2 * r.bytes <= 100 << 20,
         }
+        wire = ll_wire_bytes(r)
+        if wire is not None:
+            sweep[str(r.w.n)]["wire_bytes_per_call"] = wire
+            sweep[str(r.w.n)]["wire_GBps"] = round(wire / us / 1e3, 1)
         if r.choice:
             sweep[str(r.w.n)]["auto_choice"] = r.choice
 
@@ -648,6 +674,26 @@ def host_threads() -> int:
         return os.cpu_count() or 1
 
 
+def cpu_model() -> str:
+    """The host CPU's name: /proc/cpuinfo's model name where it has one (x86),
+    else lscpu's (Arm cores list only part numbers in /proc/cpuinfo)."""
+    try:
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                if line.lower().startswith("model name"):
+                    return line.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.startswith("Model name:"):
+                return line.split(":", 1)[1].strip()
+    except (OSError, subprocess.SubprocessError):
+        pass
+    return platform.machine() or "unknown"
+
+
 def split_range(n: int, parts: int, align: int):
     """At most `parts` [lo, hi) ranges covering 0..n, each a multiple of
     `align` long except the last."""
@@ -730,6 +776,7 @@ def cpu_baseline(runners, seconds: float):
     one, passes1, dt1 = time_oracle(lib, sample, seconds / 2, 1)
     sliced = ", first 2^22 elements per rank" if any(r.w.n > (1 << 22) for r in runners) else ""
     return {"value": round(value, 4), "unit": "GB/s", "cores": threads, "kind": "oracle",
+            "cpu_model": cpu_model(),
             "sample": "%d passes over the step's %d cases, one call each%s, every call split "
                       "by element range over %d threads (%.1f s)" % (
                           passes, len(sample), sliced, threads, dt),
@@ -786,7 +833,7 @@ def run_reference(args, world: int):
                    "sizes_elems_per_rank": [c["w"].n for c in cases],
                    "algo": cases[0]["algo"], "proto": cases[0]["proto"]},
         "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": threads,
-                         "kind": "oracle", "sample": sample_desc},
+                         "kind": "oracle", "cpu_model": cpu_model(), "sample": sample_desc},
         "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
     }

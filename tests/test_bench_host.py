@@ -136,3 +136,26 @@ def test_digest_ignores_comments_but_not_code():
     assert bench.strip_comments(src) == bench.strip_comments(src.replace("note", "other words"))
     assert "// not a comment" in bench.strip_comments(src)
     assert bench.strip_comments(src) != bench.strip_comments(src.replace("a = 1", "a = 2"))
+
+
+def test_ll_wire_bytes_count_packets():
+    import types
+    import all_reduce_reduction_gb300 as ar
+
+    def runner(algo, proto, n, dtype="bf16", R=8, **extra):
+        w = types.SimpleNamespace(R=R, n=n, dtype=dtype)
+        return types.SimpleNamespace(c=dict(algo=algo, proto=proto, **extra), choice=None, w=w)
+    # whole packets: inputs + outputs 2RNs, packets stored and loaded 2 x 2RNs
+    assert bench.ll_wire_bytes(runner("one_shot", "ll", 1 << 18)) == 6 * 8 * (1 << 19)
+    # a partial last packet still travels as 8 bytes
+    assert bench.ll_wire_bytes(runner("one_shot", "ll", 513)) == 8 * (2 * 1026 + 2 * 8 * 257)
+    assert bench.ll_wire_bytes(runner("one_shot", "ll", 3, "fp32", 2)) == 2 * (2 * 12 + 2 * 24)
+    # other paths report only the minimal bytes
+    assert bench.ll_wire_bytes(runner("two_shot", "ll", 1024)) is None
+    assert bench.ll_wire_bytes(runner("one_shot", "hb", 1024)) is None
+    assert bench.ll_wire_bytes(runner("one_shot", "ll", 1024, transport=ar.AR_LL_CLUSTER)) is None
+
+
+def test_cpu_model_is_named():
+    name = bench.cpu_model()
+    assert isinstance(name, str) and name.strip()
