@@ -455,7 +455,8 @@ int ar_destroy(ar_handle_t h) {
     if (!h)
         return AR_OK;
     int rc = AR_OK;
-    if (cudaDeviceSynchronize() != cudaSuccess)
+    DeviceScope on(h->device);
+    if (!on.ok() || cudaDeviceSynchronize() != cudaSuccess)
         rc = AR_ERR_CUDA;
     if (cudaFree(h->dev_mem) != cudaSuccess)
         rc = AR_ERR_CUDA;

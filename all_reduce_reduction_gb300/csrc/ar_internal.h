@@ -31,6 +31,29 @@ constexpr int kTmaMaxStages = 4;
 
 inline size_t elem_size(int dtype) { return dtype == AR_FP32 ? 4 : 2; }
 
+// Makes `device` current for the scope and restores the caller's device.
+class DeviceScope {
+  public:
+    explicit DeviceScope(int device) {
+        ok_ = cudaGetDevice(&prev_) == cudaSuccess &&
+              (prev_ == device || cudaSetDevice(device) == cudaSuccess);
+        if (!ok_)
+            prev_ = -1;
+    }
+    ~DeviceScope() {
+        int cur = -1;
+        if (prev_ >= 0 && cudaGetDevice(&cur) == cudaSuccess && cur != prev_)
+            (void)cudaSetDevice(prev_);
+    }
+    bool ok() const { return ok_; }
+    DeviceScope(const DeviceScope &) = delete;
+    DeviceScope &operator=(const DeviceScope &) = delete;
+
+  private:
+    int prev_ = -1;
+    bool ok_ = false;
+};
+
 // Launch kernel(args...) on stream s.  With `pdl` the launch allows
 // programmatic dependent launch: it may start while the previous kernel in
 // the stream drains, and every kernel of this library waits (griddepcontrol

@@ -688,7 +688,8 @@ extern "C" int ar_plan_destroy(ar_plan_t p) {
     if (!p)
         return AR_OK;
     int rc = AR_OK;
-    if (cudaDeviceSynchronize() != cudaSuccess || cudaFree(p->dev) != cudaSuccess)
+    DeviceScope on(p->device);
+    if (!on.ok() || cudaDeviceSynchronize() != cudaSuccess || cudaFree(p->dev) != cudaSuccess)
         rc = AR_ERR_CUDA;
     delete p;
     return rc;

@@ -41,7 +41,11 @@
  *     streams joined by events): the handle's scratch and its epoch words are
  *     shared by all its calls.
  *   - Call with the device that was current at ar_create current; otherwise
- *     AR_ERR_INVALID.
+ *     AR_ERR_INVALID.  ar_destroy and ar_plan_destroy make that device
+ *     current themselves for the call, and restore the caller's.
+ *   - A handle holds host state (its tuning table and settings) without
+ *     locks: calls on one handle come from one host thread at a time.
+ *     Distinct handles are independent.
  *   - Errors detected on the host are returned immediately and nothing is
  *     enqueued.  Errors detected on the device (a timed-out wait, a packet
  *     with the wrong flag) are recorded in the handle's status word and
@@ -173,8 +177,9 @@ typedef struct ar_info {
  * bad dtype, out == NULL), AR_ERR_NOMEM, AR_ERR_CUDA. */
 int ar_create(int R, size_t N, int dtype, ar_handle_t *out);
 
-/* Free the handle and its device memory.  Waits for the device first.
- * NULL is accepted and ignored. */
+/* Free the handle and its device memory.  Waits for the handle's device
+ * first (whichever device is current; the caller's is restored).  NULL is
+ * accepted and ignored. */
 int ar_destroy(ar_handle_t h);
 
 /* Sum all-reduce: for every rank r and element i < N,
