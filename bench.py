@@ -239,10 +239,12 @@ def hbm_peak():
         return FALLBACK_HBM_GBS, "fallback"
 
 
-# device sources of each kernel family (the key's leading words)
+# device sources of each kernel family (the key's leading words): whole
+# files, or, where a file holds several kernels, (file, functions): the
+# file's helpers before its first kernel plus those functions alone
 KERNEL_SOURCES = {
-    "one_shot_ll_global": ["ar_ll.cu"],
-    "two_shot_ll": ["ar_ll.cu"],
+    "one_shot_ll_global": [("ar_ll.cu", ["k_ll_staged", "launch_ll_staged"])],
+    "two_shot_ll": [("ar_ll.cu", ["k_ll2_staged", "launch_ll_staged"])],
     "one_shot_ll_cluster": ["ar_ll_cluster.cu"],
     "one_shot_hb": ["ar_hb.cu"],
     "two_shot_hb": ["ar_tma.cu"],
@@ -276,10 +278,50 @@ def strip_comments(src: str) -> str:
     return " ".join("".join(out).split())
 
 
+def function_source(src: str, name: str) -> str:
+    """The definition of function `name` in comment-stripped source: from its
+    name to the brace that closes its body (the first occurrence whose
+    parameter list is followed by a body, not a call or a declaration)."""
+    i = 0
+    while True:
+        i = src.find(name + "(", i)
+        if i < 0:
+            raise KeyError(name)
+        if i > 0 and (src[i - 1].isalnum() or src[i - 1] == "_"):
+            i += 1
+            continue
+        depth, j = 0, i + len(name)
+        while j < len(src):                 # the parameter list's closing parenthesis
+            if src[j] == "(":
+                depth += 1
+            elif src[j] == ")":
+                depth -= 1
+                if depth == 0:
+                    break
+            j += 1
+        k = j + 1
+        while k < len(src) and src[k].isspace():
+            k += 1
+        if k >= len(src) or src[k] != "{":
+            i += 1
+            continue
+        depth = 0
+        while k < len(src):                 # the body's closing brace
+            if src[k] == "{":
+                depth += 1
+            elif src[k] == "}":
+                depth -= 1
+                if depth == 0:
+                    return src[i:k + 1]
+            k += 1
+        raise KeyError(name)
+
+
 def kernel_source_digest(kernel_key: str) -> str:
-    """Digest of the device code a kernel key names: its .cu file plus the
-    shared device header, comments and layout aside.  Any change to the code
-    invalidates recorded counters."""
+    """Digest of the device code a kernel key names: its .cu file (or, for a
+    file holding several kernels, the file's helpers and the named functions)
+    plus the shared device header, comments and layout aside.  Any change to
+    that code invalidates recorded counters."""
     files = None
     for prefix, fs in KERNEL_SOURCES.items():
         if kernel_key.startswith(prefix):
@@ -288,8 +330,16 @@ def kernel_source_digest(kernel_key: str) -> str:
         return "unknown"
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "all_reduce_reduction_gb300", "csrc")
-    for fn in files + ["ar_device.cuh"]:
-        h.update(strip_comments(open(os.path.join(csrc, fn)).read()).encode())
+    for entry in files + ["ar_device.cuh"]:
+        fn, funcs = entry if isinstance(entry, tuple) else (entry, None)
+        text = strip_comments(open(os.path.join(csrc, fn)).read())
+        if funcs is None:
+            h.update(text.encode())
+            continue
+        first = text.find("__global__")
+        h.update(text[:first if first >= 0 else len(text)].encode())
+        for f in funcs:
+            h.update(function_source(text, f).encode())
     return h.hexdigest()[:16]
 
 

@@ -159,3 +159,37 @@ def test_ll_wire_bytes_count_packets():
 def test_cpu_model_is_named():
     name = bench.cpu_model()
     assert isinstance(name, str) and name.strip()
+
+
+def test_function_source_takes_definitions_not_calls():
+    src = bench.strip_comments(
+        "int g(int x); int h() { return g(1); }\n"
+        "int g(int x) { if (x) { return 1; } return 0; }  // done\n"
+        "int gg(int x) { return x; }")
+    assert bench.function_source(src, "g") == "g(int x) { if (x) { return 1; } return 0; }"
+    assert bench.function_source(src, "gg") == "gg(int x) { return x; }"
+    with pytest.raises(KeyError):
+        bench.function_source(src, "missing")
+
+
+def test_digest_follows_only_the_named_kernels(tmp_path, monkeypatch):
+    import shutil
+    csrc = os.path.join(bench.ROOT, "all_reduce_reduction_gb300", "csrc")
+    copy = tmp_path / "all_reduce_reduction_gb300" / "csrc"
+    shutil.copytree(csrc, copy)
+    one = bench.kernel_source_digest("one_shot_ll_global_r8_n1_bf16")
+    two = bench.kernel_source_digest("two_shot_ll_r8_n1_bf16")
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    assert bench.kernel_source_digest("one_shot_ll_global_r8_n1_bf16") == one
+    src = (copy / "ar_ll.cu").read_text()
+    # a change inside the two-shot kernel leaves the one-shot digest alone
+    i = src.index("k_ll2_staged(const __grid_constant__")
+    j = src.index("const uint32_t tid = threadIdx.x;", i)
+    (copy / "ar_ll.cu").write_text(src[:j] + "const uint32_t tid = threadIdx.x + 0;" +
+                                   src[j + len("const uint32_t tid = threadIdx.x;"):])
+    assert bench.kernel_source_digest("one_shot_ll_global_r8_n1_bf16") == one
+    assert bench.kernel_source_digest("two_shot_ll_r8_n1_bf16") != two
+    # a change to a helper before the kernels reaches both
+    (copy / "ar_ll.cu").write_text(src.replace("ld.global.L1::no_allocate.v2.u32",
+                                               "ld.global.v2.u32", 1))
+    assert bench.kernel_source_digest("one_shot_ll_global_r8_n1_bf16") != one
