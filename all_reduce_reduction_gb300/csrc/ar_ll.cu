@@ -247,9 +247,10 @@ __global__ void __launch_bounds__(kLlStagedThreads) k_ll_staged(const __grid_con
 //                   rank order and writes the reduced pair as a result
 //                   packet (slot R);
 //   all-gather:     for the block after each of its blocks (whose results
-//                   another CTA reduced), one thread per unit polls the
-//                   result pair once and stages it; after a barrier thread
-//                   (k, j) stores it to out[k].
+//                   another CTA reduced), R blocks per pass: thread (k, j)
+//                   polls the result pair of unit j of the pass's k-th block
+//                   once and stages it; after a barrier thread (k, j) stores
+//                   unit j of every block of the pass to out[k].
 // Every wait depends only on work each CTA finishes before its own waits
 // (puts before reductions, reductions before gathers), so the cooperative
 // grid makes progress.  In place: out[k]'s units of block b + 1 are written
@@ -345,21 +346,37 @@ __global__ void __launch_bounds__(kLlStagedThreads) k_ll2_staged(const __grid_co
         }
     }
 
-    // ---- all-gather: the block after each of this CTA's blocks ---------------
-    for (uint32_t b = blockIdx.x; !aborted && b < nblk; b += G) {    // uniform per CTA
-        const uint32_t u = (b + 1 == nblk ? 0 : b + 1) * UB + j;
-        if (k == 0 && u < U && ok) {
-            uint64_t p0, p1;
-            ok = poll_pkt2(w, res + 2 * u, p0, p1);
-            stage[j] = make_uint2(pkt_payload(p0), pkt_payload(p1));
+    // ---- all-gather: the block after each of this CTA's blocks, R blocks per
+    // pass: thread (k, j) polls the result pair of unit j of the pass's k-th
+    // block once and stages it; after a barrier it stores unit j of every
+    // block of the pass to out[k] --------------------------------------------
+    const uint32_t mine = blockIdx.x < nblk ? (nblk - 1 - blockIdx.x) / G + 1 : 0;
+    auto gather_unit = [&](uint32_t i) {                  // unit j of gather block i
+        const uint32_t b = blockIdx.x + i * G;            // this CTA's i-th block
+        return (b + 1 == nblk ? 0 : b + 1) * UB + j;
+    };
+    for (uint32_t i0 = 0; !aborted && i0 < mine; i0 += (uint32_t)R) {   // uniform per CTA
+        if (member && i0 + k < mine && ok) {
+            const uint32_t u = gather_unit(i0 + k);
+            if (u < U) {
+                uint64_t p0, p1;
+                ok = poll_pkt2(w, res + 2 * u, p0, p1);
+                stage[tid] = make_uint2(pkt_payload(p0), pkt_payload(p1));
+            }
         }
         if (__syncthreads_or(!ok)) {
             aborted = true;
             break;
         }
-        if (member && u < U)
-            st_v2(reinterpret_cast<uint2 *>(a.p.out[k]) + u, stage[j]);
-        __syncthreads();
+        if (member) {
+            uint2 *dst = reinterpret_cast<uint2 *>(a.p.out[k]);
+            for (uint32_t s = 0; s < (uint32_t)R && i0 + s < mine; ++s) {
+                const uint32_t u = gather_unit(i0 + s);
+                if (u < U)
+                    st_v2(dst + u, stage[s * UB + j]);
+            }
+        }
+        __syncthreads();                                  // the stage is refilled next pass
     }
     if (!aborted && blockIdx.x == G - 1 && ntail > 0) {
         if (k == 0 && j < ntail) {
