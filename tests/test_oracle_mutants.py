@@ -53,6 +53,15 @@ MUTANTS = {
     "combine_starts_at_positive_zero": (
         "float acc = w[t * (size_t)K] * load_widened(dtype, y[0], i);\n            for (k = 1; k < K; ++k) {",
         "float acc = 0.0f;\n            for (k = 0; k < K; ++k) {"),
+    "bf16_overflow_saturates": ("        K += 1u;\n    return (uint16_t)((sign >> 16) | K);",
+                                "        K += 1u;\n    if (K > 0x7F7Fu)\n        K = 0x7F7Fu;\n"
+                                "    return (uint16_t)((sign >> 16) | K);"),
+    "fp16_overflow_saturates": ("    if (field >= 31)\n        return (uint16_t)(sign | 0x7C00u);",
+                                "    if (field >= 31)\n        return (uint16_t)(sign | 0x7BFFu);"),
+    "fp16_subnormal_widen_scale": ("mag = ldexpf((float)m, -24);", "mag = ldexpf((float)m, -25);"),
+    "packet_tail_padded_with_ones": ("uint32_t byte = at < bytes ? (uint32_t)b[at] : 0u;",
+                                     "uint32_t byte = at < bytes ? (uint32_t)b[at] : 0xFFu;"),
+    "packet_count_rounds_down": ("    return (bytes + 3) / 4;", "    return bytes / 4;"),
     "unpack_accepts_any_flag": ("        if (f != flag) {\n            ++bad;\n            continue;\n        }",
                                 "        if (f != flag)\n            ++bad;"),
 }
