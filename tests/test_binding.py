@@ -1,0 +1,57 @@
+"""The Python binding's argument marshalling, on the CPU: pointer arrays,
+plan steps and errors (no device call)."""
+import ctypes
+
+import pytest
+
+import all_reduce_reduction_gb300 as ar
+
+
+class FakeTensor:
+    def __init__(self, ptr):
+        self.ptr = ptr
+
+    def data_ptr(self):
+        return self.ptr
+
+
+def test_pointer_array_is_padded_with_nulls():
+    arr = ar._ptr_array([FakeTensor(0x1000), 0x2000, None])
+    assert len(arr) == ar.AR_MAX_RANKS
+    assert [arr[i] for i in range(3)] == [0x1000, 0x2000, None]
+    assert all(arr[i] is None for i in range(3, ar.AR_MAX_RANKS))   # NULL
+    full = ar._ptr_array([FakeTensor(16 * (i + 1)) for i in range(ar.AR_MAX_RANKS)])
+    assert [full[i] for i in range(ar.AR_MAX_RANKS)] == [16 * (i + 1)
+                                                          for i in range(ar.AR_MAX_RANKS)]
+    with pytest.raises(ValueError):
+        ar._ptr_array([0x10] * (ar.AR_MAX_RANKS + 1))
+
+
+def test_stream_handles():
+    assert ar._stream(0) == 0
+    assert ar._stream(0xABC) == 0xABC
+
+    class S:
+        cuda_stream = 0x1234
+    assert ar._stream(S()) == 0x1234
+
+
+def test_make_op_fields():
+    o = ar.make_op(ar.AR_OP_REDUCE, 3, (ar.AR_BUF_OUT, 2),
+                   [(ar.AR_BUF_IN, 5), (ar.AR_BUF_IN, 0), (ar.AR_BUF_IN, 7)], 4, 9)
+    assert (o.kind, o.rank, o.dst_buf, o.dst_rank) == (ar.AR_OP_REDUCE, 3, ar.AR_BUF_OUT, 2)
+    assert (o.src_buf, o.nsrc) == (ar.AR_BUF_IN, 3)
+    assert list(o.src_rank)[:3] == [5, 0, 7] and not any(list(o.src_rank)[3:])
+    assert (o.chunk_begin, o.chunk_end) == (4, 9)
+    with pytest.raises(ValueError):
+        ar.make_op(ar.AR_OP_REDUCE, 0, (ar.AR_BUF_OUT, 0),
+                   [(ar.AR_BUF_IN, 0), (ar.AR_BUF_OUT, 1)], 0, 1)
+    # a step array as the library receives it
+    arr = (ar.ar_op * 2)(o, o)
+    assert ctypes.sizeof(arr) == 2 * ctypes.sizeof(ar.ar_op)
+
+
+def test_error_carries_its_code():
+    e = ar.ArError(ar.AR_ERR_UNSUPPORTED, "ar_allreduce")
+    assert e.code == ar.AR_ERR_UNSUPPORTED
+    assert str(e).startswith("ar_allreduce: AR_ERR_UNSUPPORTED")
