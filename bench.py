@@ -249,7 +249,8 @@ KERNEL_SOURCES = {
     "one_shot_hb": ["ar_hb.cu"],
     "two_shot_hb": ["ar_tma.cu"],
     "combine": ["ar_combine.cu"],
-    "plan_": ["ar_plan.cu"],
+    # a plan's traffic follows its compiled tasks: the compiler counts too
+    "plan_": [("ar_plan.cu", ["k_plan", "compile_plan", "builtin_plan", "ar_plan_execute"])],
 }
 
 
@@ -889,7 +890,7 @@ def run_reference(args, world: int):
     }
 
 
-def main():
+def make_parser() -> argparse.ArgumentParser:
     p = argparse.ArgumentParser()
     p.add_argument("--gpus", type=int, default=1)
     p.add_argument("--steps", type=int, default=1000)
@@ -916,7 +917,11 @@ def main():
                    help="run only the workload's case with this many elements per rank")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-variants", action="store_true")
-    args = p.parse_args()
+    return p
+
+
+def main():
+    args = make_parser().parse_args()
     if args.warmup < 3:
         raise SystemExit("--warmup must be >= 3")
 
