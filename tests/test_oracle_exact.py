@@ -10,7 +10,8 @@ binary32; binary16: 11 bits, exponents -14..15).  Signed zeros follow IEEE
 other exact zero sum is +0 under round-to-nearest, and a nonzero result that
 rounds to zero keeps its sign.  Inputs are drawn from the edge-of-format
 pools (zeros, subnormals, smallest normals, ones, values near the largest
-finite) and from the log-uniform workload recipe."""
+finite) and from the log-uniform workload recipe.  The weighted combine is
+checked the same way, with IEEE binary32 multiplication in the model."""
 from fractions import Fraction
 
 import numpy as np
@@ -142,3 +143,52 @@ def test_fold_equals_exact_model_on_edge_values(dtype, R):
 def test_fold_equals_exact_model_on_loguniform(dtype, R):
     n = 96
     _case(dtype, R, n, wl.make_inputs(310 + R, R, n, dtype, "loguniform"))
+
+
+def _mul32(x, y):
+    """IEEE binary32 multiplication, round to nearest even."""
+    neg = x[1] != y[1]
+    if x[0] == NAN or y[0] == NAN:
+        return (NAN, False, None)
+    if x[0] == INF or y[0] == INF:
+        other = y if x[0] == INF else x
+        if other[0] == FIN and other[2] == 0:
+            return (NAN, False, None)                    # infinity times zero
+        return (INF, neg, None)
+    return _round(x[2] * y[2], neg, "fp32")
+
+
+def _combine_model(weights, columns, fmt):
+    acc = _mul32(_decode(weights[0], "fp32"), _decode(columns[0], fmt))
+    for wb, b in zip(weights[1:], columns[1:]):
+        acc = _add32(acc, _mul32(_decode(wb, "fp32"), _decode(b, fmt)))
+    if fmt == "fp32" or acc[0] != FIN:
+        return acc
+    return _round(acc[2], acc[1], fmt)
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "fp16", "fp32"])
+@pytest.mark.parametrize("K", [1, 3, 8])
+@pytest.mark.parametrize("special", [True, False])
+def test_combine_equals_exact_model(dtype, K, special):
+    """The weighted combine: every product w[t,k] * y_k[t,h] rounded to
+    binary32 on its own, folded left to right from k = 0, rounded once."""
+    T, H = 6, 24
+    u = np.uint32 if dtype == "fp32" else np.uint16
+    if special:
+        ys = wl.special_inputs(320 + K, K, T * H, dtype)
+        w = wl.special_weights(330 + K, T, K)
+    else:
+        ys = wl.make_inputs(340 + K, K, T * H, dtype, "loguniform")
+        w = wl.gate_weights(350 + K, T, K)
+    bits = [np.ascontiguousarray(wl.bits(t)).view(u) for t in ys]
+    wbits = np.ascontiguousarray(w, dtype=np.float32).view(np.uint32)
+    out = np.ascontiguousarray(oracle.combine([wl.bits(t) for t in ys], w, T, H,
+                                              wl.DTYPE_CODE[dtype])).view(u)
+    for t in range(T):
+        for h in range(H):
+            i = t * H + h
+            want = _combine_model([int(wbits[t * K + k]) for k in range(K)],
+                                  [int(b[i]) for b in bits], dtype)
+            got = _decode(int(out[i]), dtype)
+            assert _same(got, want), (dtype, K, t, h, got, want)
