@@ -55,3 +55,35 @@ def test_error_carries_its_code():
     e = ar.ArError(ar.AR_ERR_UNSUPPORTED, "ar_allreduce")
     assert e.code == ar.AR_ERR_UNSUPPORTED
     assert str(e).startswith("ar_allreduce: AR_ERR_UNSUPPORTED")
+
+
+def _header_constants():
+    import os
+    import re
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    text = open(os.path.join(root, "include", "ar.h")).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    consts = {}
+    for body in re.findall(r"enum\s+\w+\s*\{(.*?)\}", text, re.S):
+        for name, value in re.findall(r"(AR_\w+)\s*=\s*(\d+)", body):
+            consts[name] = int(value)
+    for name, expr in re.findall(r"^#define\s+(AR_\w+)\s+(.+)$", text, re.M):
+        expr = re.sub(r"(\d+)u?l?l?", r"\1", expr.strip())
+        if re.fullmatch(r"[\d\s()<]+", expr):
+            consts[name] = eval(expr)                 # digits, shifts, parentheses only
+    return consts
+
+
+def test_binding_constants_match_the_header():
+    consts = _header_constants()
+    assert {"AR_MAX_RANKS", "AR_LL_MAX_BYTES", "AR_NOALLOC_SCRATCH_BYTES", "AR_OK",
+            "AR_ERR_FLAG_MISMATCH", "AR_LL_CLUSTER", "AR_BUF_OUT"} <= set(consts)
+    for name, value in consts.items():
+        if hasattr(ar, name):
+            assert getattr(ar, name) == value, name
+    # every enumerator the calls take or return is exposed by the binding
+    for name in consts:
+        if name.startswith(("AR_ERR_", "AR_OK", "AR_BF16", "AR_FP", "AR_ONE", "AR_TWO",
+                            "AR_ALGO", "AR_PROTO", "AR_LL", "AR_HB", "AR_OP_", "AR_BUF_")):
+            if name != "AR_LL_MAX_BYTES":
+                assert hasattr(ar, name), name
