@@ -193,3 +193,30 @@ def test_digest_follows_only_the_named_kernels(tmp_path, monkeypatch):
     (copy / "ar_ll.cu").write_text(src.replace("ld.global.L1::no_allocate.v2.u32",
                                                "ld.global.v2.u32", 1))
     assert bench.kernel_source_digest("one_shot_ll_global_r8_n1_bf16") != one
+
+
+def test_workloads_match_the_configurations():
+    """The bench's workloads have the sizes, dtypes and value recipes of the
+    configurations they stand for, and the algorithmic bytes 2*R*N*s."""
+    _, sweep = bench.workload_cases("sweep")
+    assert [(c["w"].R, c["w"].n, c["w"].dtype, c["w"].dist) for c in sweep] == \
+        [(8, 1 << i, "bf16", "uniform") for i in range(9, 19)]
+    assert all(c["algo"] == "one_shot" and c["proto"] == "ll" and c["calls"] == 10 and c["flush"]
+               for c in sweep)
+    assert [bench.case_bytes(c) for c in sweep] == [2 * 8 * (1 << i) * 2 for i in range(9, 19)]
+    _, decode = bench.workload_cases("decode")
+    assert [(c["w"].R, c["w"].n, c["w"].dist) for c in decode] == \
+        [(8, 8192 * b, "normal") for b in (1, 8, 32, 128, 256)]
+    _, prefill = bench.workload_cases("prefill")
+    (p,) = prefill
+    assert (p["w"].R, p["w"].n, p["w"].dtype, p["algo"], p["proto"], p["flush"]) == \
+        (16, 8192 * 8192, "bf16", "two_shot", "hb", False)
+    assert bench.case_bytes(p) == 4 << 30                  # 4 GiB per call, far above L2
+    _, edge = bench.workload_cases("edge")
+    (e,) = edge
+    assert (e["w"].R, e["w"].n, e["w"].dtype, e["w"].dist) == (32, 4097 * 4096 + 3, "fp32",
+                                                               "loguniform")
+    assert bench.case_bytes(e) == 2 * 32 * (4097 * 4096 + 3) * 4
+    _, comb = bench.workload_cases("combine")
+    assert [(c["w"].K, c["w"].T, c["w"].H) for c in comb] == [(8, t, 8192) for t in (1, 16, 128, 4096)]
+    assert bench.case_bytes(comb[-1]) == 9 * 4096 * 8192 * 2 + 4 * 4096 * 8
