@@ -283,10 +283,13 @@ def ar_get_info(h: int) -> dict:
 
 def ar_allreduce_ll_static(R: int, N: int, dtype, ins, outs, stream=None) -> None:
     """One-shot LL all-reduce with no handle and no allocation, for callers
-    that may not allocate device memory where they run it (see include/ar.h:
-    library-static scratch, at most AR_NOALLOC_SCRATCH_BYTES of packets;
-    the first call on a device must precede any stream capture; calls that
-    overlap on the GPU race)."""
+    that may not allocate device memory where they run it: an engine whose
+    own pool holds nearly all of the GPU's memory, or a latency-critical
+    hook that cannot pay for cudaMalloc's device-wide synchronisation.  The
+    packet scratch is a static array inside the library (at most
+    AR_NOALLOC_SCRATCH_BYTES of packets, else AR_ERR_UNSUPPORTED); the first
+    call on a device sets it up and must precede any stream capture; calls
+    that overlap on the GPU race on the shared array."""
     dt = DTYPES[dtype] if isinstance(dtype, str) else dtype
     _check(load_library().ar_allreduce_ll_static(R, N, dt, _ptr_array(ins), _ptr_array(outs),
                                                  _stream(stream)), "ar_allreduce_ll_static")

@@ -2,13 +2,13 @@
 // without any allocation.
 //
 // Some callers cannot allocate device memory at the point where they need
-// the collective: a plugin's enqueue hook that an inference engine calls
-// while it captures its stream into a CUDA graph (an allocation there is an
-// illegal call during capture), or an engine that hands out every byte of
-// device memory from its own pool and forbids side allocations, so that its
-// memory plan stays exact.  ar_create allocates the packet scratch and the
-// control words such callers cannot create; this entry point takes them from
-// a fixed array compiled into the library instead.
+// the collective: an inference engine that reserves nearly all of the GPU's
+// memory up front for its own pool and accounts for every byte (a side
+// allocation would fail, or break its memory plan), or a hook on a
+// latency-critical path that must not pay for cudaMalloc/cudaFree, which can
+// synchronise the whole device.  ar_create allocates the packet scratch and
+// the control words such callers cannot create; this entry point takes them
+// from a fixed array compiled into the library instead.
 //
 // The array below is static device storage: every GPU that loads the library
 // holds AR_NOALLOC_SCRATCH_BYTES of it (plus the control words) until the

@@ -150,14 +150,14 @@ class ClockSampler:
 
     def start(self):
         q = ("pci.bus_id,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
-             + ",".join("clocks_event_reasons." + r for r in REASONS))
+             + ",".join("clocks_event_reasons." + r for r in REASONS) + ",timestamp")
         try:
             import tempfile
             fd, self.path = tempfile.mkstemp(prefix="clocks_", suffix=".csv")
             os.close(fd)
             self.out = open(self.path, "w")
             self.proc = subprocess.Popen(
-                ["nvidia-smi", "--query-gpu=" + q, "--format=csv,noheader,nounits", "-lms", "100"],
+                ["nvidia-smi", "--query-gpu=" + q, "--format=csv,noheader,nounits", "-lms", "50"],
                 stdout=self.out, stderr=subprocess.DEVNULL)
         except Exception:
             self.proc = None
@@ -177,10 +177,24 @@ class ClockSampler:
         return parse_clock_rows(lines, self.bus_id)
 
 
+def parse_smi_time(text: str) -> float | None:
+    """Seconds since the epoch of an nvidia-smi timestamp such as
+    "2026/12/03 05:29:26.123" (the host's local time, as time.time() counts)."""
+    import datetime
+    for fmt in ("%Y/%m/%d %H:%M:%S.%f", "%Y/%m/%d %H:%M:%S"):
+        try:
+            return datetime.datetime.strptime(text.strip(), fmt).timestamp()
+        except ValueError:
+            pass
+    return None
+
+
 def parse_clock_rows(lines, bus_id: str | None) -> dict | None:
     """Summarise nvidia-smi CSV rows (pci.bus_id, clocks.sm, clocks.max.sm,
     power.draw, reasons.active, then one Active/Not Active column per REASONS
-    entry) of the GPU whose bus id ends with `bus_id`."""
+    entry, then an optional timestamp) of the GPU whose bus id ends with
+    `bus_id`.  `series` lists (seconds since the epoch, SM MHz) of the rows
+    that carry both."""
     rows = []
     for line in lines:
         f = [x.strip() for x in line.split(",")]
@@ -195,9 +209,44 @@ def parse_clock_rows(lines, bus_id: str | None) -> dict | None:
     mx = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
     seen = sorted({REASONS[i] for r in rows for i in range(len(REASONS))
                    if r[5 + i].lower().startswith("active")})
+    series = []
+    for r in rows:
+        if len(r) > 5 + len(REASONS) and r[1].replace(".", "").isdigit():
+            t = parse_smi_time(r[5 + len(REASONS)])
+            if t is not None:
+                series.append((t, float(r[1])))
     return {"sm_mhz": statistics.median(sm) if sm else None,
             "sm_max_mhz": max(mx) if mx else None,
-            "reasons": seen, "samples": len(rows)}
+            "reasons": seen, "samples": len(rows), "series": series}
+
+
+def clocks_for_windows(series, windows, reach: float = 0.06) -> dict:
+    """The SM clock seen by a set of replays: for every replay window
+    (start, end) in seconds since the epoch, the clock sample nearest to the
+    window's middle, if one lies within `reach` seconds; returns the median
+    of those samples and how many replays had one."""
+    if not series:
+        return {"sm_mhz_median": None, "replays_with_sample": 0}
+    ts = sorted(series)
+    got = []
+    for lo, hi in windows:
+        mid = 0.5 * (lo + hi)
+        t, mhz = min(ts, key=lambda x: abs(x[0] - mid))
+        if abs(t - mid) <= reach + 0.5 * (hi - lo):
+            got.append(mhz)
+    return {"sm_mhz_median": statistics.median(got) if got else None,
+            "replays_with_sample": len(got)}
+
+
+def replay_stats(times_ms, calls: int) -> dict:
+    """µs per call of individual graph replays (each `calls` calls): median,
+    90th percentile (nearest rank), minimum and maximum."""
+    us = sorted(t * 1e3 / calls for t in times_ms)
+    if not us:
+        return {}
+    p90 = us[min(len(us) - 1, max(0, -(-9 * len(us) // 10) - 1))]
+    return {"us_p50": round(statistics.median(us), 3), "us_p90": round(p90, 3),
+            "us_min": round(us[0], 3), "us_max": round(us[-1], 3), "replays": len(us)}
 
 
 def clocks_rejected(c: dict | None) -> bool:
@@ -371,7 +420,7 @@ def rank_stride(n: int, elem_size: int) -> int:
 class CaseRunner:
     """Handle, device inputs/outputs and a captured graph for one case."""
 
-    def __init__(self, c, stream):
+    def __init__(self, c, stream, host_buffers: bool = True):
         import torch
         import all_reduce_reduction_gb300 as ar
         from all_reduce_reduction_gb300 import workload as wl
@@ -438,6 +487,10 @@ class CaseRunner:
         torch.cuda.synchronize()
         if ar.ar_status(self.h.h) != ar.AR_OK:
             raise RuntimeError("device status after warm-up: " + ar.ar_strerror(ar.ar_status(self.h.h)))
+        self.pinned_in = self.pinned_out = None
+        if not host_buffers:
+            self.cpu_inputs = None
+            return
         self.pinned_in = torch.zeros(in_block.shape, dtype=in_block.dtype).pin_memory()
         for r, t in enumerate(self.cpu_inputs):
             self.pinned_in[r * self.stride:r * self.stride + n].copy_(t)
@@ -482,17 +535,30 @@ def run_ours(args, dist: Dist):
             events.append((i, e0, e1))
 
     def timed(K):
+        """Sum of event time per case, each replay's time per case, and each
+        replay's (start, end) in host seconds since the epoch (the GPU's
+        event clock anchored at an event recorded on an idle stream)."""
         events = []
         dist.barrier()
         torch.cuda.synchronize()
+        anchor = torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(stream):
+            anchor.record(stream)
+        t_anchor = time.time()
         for _ in range(K):
             one_step(events)
         torch.cuda.synchronize()
         dist.barrier()
         per_case = [0.0] * len(runners)
+        replays = [[] for _ in runners]
+        windows = [[] for _ in runners]
         for i, e0, e1 in events:
-            per_case[i] += e0.elapsed_time(e1)
-        return per_case
+            ms = e0.elapsed_time(e1)
+            per_case[i] += ms
+            replays[i].append(ms)
+            t0 = t_anchor + anchor.elapsed_time(e0) * 1e-3
+            windows[i].append((t0, t0 + ms * 1e-3))
+        return per_case, replays, windows
 
     for _ in range(args.warmup):
         one_step([])
@@ -504,15 +570,20 @@ def run_ours(args, dist: Dist):
         bus = "%02X:%02X.0" % (props.pci_bus_id, props.pci_device_id)
     sampler = ClockSampler(bus)
     sampler.start()
-    per_case = timed(args.steps)
+    time.sleep(0.2)                     # the sampler's first rows precede the timed region
+    per_case, replays, windows = timed(args.steps)
+    time.sleep(0.1)
     clocks = sampler.stop()
     remeasured = False
     if clocks_rejected(clocks):
         sampler = ClockSampler(bus)
         sampler.start()
-        per_case = timed(args.steps)
+        time.sleep(0.2)
+        per_case, replays, windows = timed(args.steps)
+        time.sleep(0.1)
         clocks = sampler.stop()
         remeasured = True
+    series = clocks.pop("series", []) if clocks else []
 
     total_ms = sum(per_case)
     for r in runners:
@@ -557,6 +628,8 @@ def run_ours(args, dist: Dist):
             "frac_of_hbm_peak": round(r.bytes / us / 1e3 / peak, 4),
             "l2_resident": 2 * r.bytes <= 100 << 20,
         }
+        sweep[str(r.w.n)].update(replay_stats(replays[i], r.c["calls"]))
+        sweep[str(r.w.n)]["clock"] = clocks_for_windows(series, windows[i])
         wire = ll_wire_bytes(r)
         if wire is not None:
             sweep[str(r.w.n)]["wire_bytes_per_call"] = wire
@@ -564,12 +637,42 @@ def run_ours(args, dist: Dist):
         if r.choice:
             sweep[str(r.w.n)]["auto_choice"] = r.choice
 
-    # end to end: pinned host inputs -> device, the same graph, outputs -> host
+    # end to end, one host round trip per all-reduce: every step, each case's
+    # R inputs are copied in from pinned host memory, one all-reduce is
+    # launched through the library's public call (no graph), and all R
+    # outputs are copied back to pinned host memory; events on the stream
+    # bracket the three
     e2e_steps = max(3, min(args.steps, 50))
-    e2e_ms = 0.0
+    for r in runners:                   # warm the eager path of every case first
+        with torch.cuda.stream(stream):
+            r.in_block.copy_(r.pinned_in, non_blocking=True)
+            r.call()
+            r.pinned_out.copy_(r.out_block, non_blocking=True)
+    torch.cuda.synchronize()
     h2d = sum(r.pinned_in.numel() * r.pinned_in.element_size() for r in runners)
     d2h = sum(r.pinned_out.numel() * r.pinned_out.element_size() for r in runners)
+    e2e_bytes = sum(r.bytes for r in runners)          # one call per case per step
+    e2e_ms = 0.0
     dist.barrier()
+    torch.cuda.synchronize()
+    for _ in range(e2e_steps):
+        for r in runners:
+            with torch.cuda.stream(stream):
+                e0 = torch.cuda.Event(enable_timing=True)
+                e1 = torch.cuda.Event(enable_timing=True)
+                e0.record(stream)
+                r.in_block.copy_(r.pinned_in, non_blocking=True)
+                r.call()
+                r.pinned_out.copy_(r.out_block, non_blocking=True)
+                e1.record(stream)
+            e1.synchronize()
+            e2e_ms += e0.elapsed_time(e1)
+    e2e_ms = dist.max(e2e_ms / e2e_steps)
+    e2e_value = dist.sum(e2e_bytes) / (e2e_ms * 1e-3) / 1e9
+
+    # the earlier form, for comparison: one host round trip per case around
+    # the case's whole graph (`calls` all-reduces)
+    batched_ms = 0.0
     torch.cuda.synchronize()
     for _ in range(e2e_steps):
         for r in runners:
@@ -582,13 +685,23 @@ def run_ours(args, dist: Dist):
                 r.pinned_out.copy_(r.out_block, non_blocking=True)
                 e1.record(stream)
             e1.synchronize()
-            e2e_ms += e0.elapsed_time(e1)
-    e2e_ms = dist.max(e2e_ms / e2e_steps)
-    e2e_value = dist.sum(bytes_step) / (e2e_ms * 1e-3) / 1e9
+            batched_ms += e0.elapsed_time(e1)
+    batched_ms = dist.max(batched_ms / e2e_steps)
+    batched_value = dist.sum(bytes_step) / (batched_ms * 1e-3) / 1e9
+
+    hbm = None
+    if args.workload == "sweep" and not args.no_hbm:
+        for r in runners:               # release the sweep's pinned host buffers first
+            r.pinned_in = r.pinned_out = None
+        hbm = measure_hbm_workloads(stream, bus, peak, dist)
 
     variants = None
     if args.workload in ("sweep", "decode") and not args.no_variants:
         variants = measure_variants(runners, stream, flush, max(20, args.steps // 10))
+
+    eager = None
+    if args.workload in ("sweep", "decode"):
+        eager = measure_eager(runners, stream, flush)
 
     cpu = None
     if dist.world == 1 and not args.no_cpu_baseline:
@@ -616,17 +729,26 @@ def run_ours(args, dist: Dist):
         "roofline": roofline,
         "cpu_baseline": cpu,
         "e2e": {"value": round(e2e_value, 2), "unit": "GB/s", "h2d_bytes_per_step": h2d,
-                "d2h_bytes_per_step": d2h,
-                "note": "per case: the R inputs copied in from one pinned host block, the "
-                        "case's graph, all outputs copied back to one pinned host block"},
+                "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms, 5),
+                "calls_per_step": len(runners),
+                "note": "one all-reduce per case per step, each with its own host round trip: "
+                        "the case's R inputs copied in from pinned host memory, one eager "
+                        "ar_allreduce call, all R outputs copied back to pinned host memory; "
+                        "CUDA events on the stream around the three; minimal bytes of the "
+                        "step's calls / that time",
+                "graph_batched": {"value": round(batched_value, 2), "unit": "GB/s",
+                                  "note": "the earlier form: one host round trip per case "
+                                          "around the case's whole %d-call graph"
+                                          % cases[0]["calls"]}},
         "gpu_launches": launches,
         "clocks": clocks, "clocks_remeasured": remeasured,
         "sweep": sweep,
     }
+    if hbm is not None:
+        line["hbm_workloads"] = hbm
     if variants is not None:
         line["variants_us_per_call"] = variants
-    if args.workload in ("sweep", "decode"):
-        eager = measure_eager(runners, stream, flush)
+    if eager is not None:
         line["eager_us_per_call"] = eager
         if dist.rank == 0:
             print_table(runners, sweep, eager)
@@ -635,16 +757,88 @@ def run_ours(args, dist: Dist):
     return line
 
 
+# the bandwidth-bound workloads timed after the default sweep: the prefill
+# all-reduce (R=16, 128 MiB per rank, bf16, two-shot HB with TMA staging) and
+# the R=32 binary32 edge case (two-shot HB)
+HBM_WORKLOADS = ("prefill", "edge")
+
+
+def measure_hbm_workloads(stream, bus, peak, dist, replays=20, warmup=3) -> dict:
+    """µs/call and minimal-bytes GB/s of the HBM_WORKLOADS, one at a time:
+    the case's single-call graph replayed `warmup` times, then `replays`
+    times with a CUDA event pair around each replay, under its own clock
+    sampler.  Inputs and outputs (4.3 GB per call) are far larger than L2,
+    so no flush is needed.  Each case's buffers are freed before the next."""
+    import torch
+    import all_reduce_reduction_gb300 as ar
+    out = {}
+    for name in HBM_WORKLOADS:
+        desc, cases = workload_cases(name)
+        c = cases[0]
+        r = CaseRunner(c, stream, host_buffers=False)
+        for _ in range(warmup):
+            r.graph.replay()
+        torch.cuda.synchronize()
+        sampler = ClockSampler(bus)
+        sampler.start()
+        time.sleep(0.2)
+        evs = []
+        dist.barrier()
+        torch.cuda.synchronize()
+        for _ in range(replays):
+            with torch.cuda.stream(stream):
+                e0 = torch.cuda.Event(enable_timing=True)
+                e1 = torch.cuda.Event(enable_timing=True)
+                e0.record(stream)
+                r.graph.replay()
+                e1.record(stream)
+            evs.append((e0, e1))
+        torch.cuda.synchronize()
+        dist.barrier()
+        time.sleep(0.1)
+        clocks = sampler.stop()
+        if clocks:
+            clocks.pop("series", None)
+        st = ar.ar_status(r.h.h, stream)
+        if st != ar.AR_OK:
+            raise RuntimeError("device status after the %s workload: %s" % (name, ar.ar_strerror(st)))
+        times = [e0.elapsed_time(e1) for e0, e1 in evs]
+        calls = c["calls"]
+        us = dist.max(sum(times) * 1e3 / (replays * calls))
+        gbs = r.bytes / us / 1e3
+        key = "%s_%s_r%d_n%d_%s" % (c["algo"], c["proto"], r.w.R, r.w.n, r.w.dtype)
+        out[name] = {
+            "workload": desc, "R": r.w.R, "n": r.w.n, "dtype": r.w.dtype,
+            "algo": c["algo"], "proto": c["proto"],
+            "warmup_calls": warmup * calls, "timed_calls": replays * calls,
+            "us_per_call": round(us, 3), **replay_stats(times, calls),
+            "min_bytes_per_call": r.bytes, "min_bytes_GBps": round(gbs, 1),
+            "peak": peak, "frac_of_hbm_peak": round(gbs / peak, 4),
+            "frac_of_nominal": round(gbs / NOMINAL_HBM_GBS, 4),
+            "traffic": committed_traffic(key), "kernel": key,
+            "l2": "inputs and outputs far larger than L2 (no flush)",
+            "clocks": clocks, "clocks_rejected": clocks_rejected(clocks),
+        }
+        r.close()
+        del r
+        torch.cuda.empty_cache()
+    return out
+
+
 def measure_eager(runners, stream, flush, warmup=2, calls=10):
-    """µs/call of the same calls launched one by one, without a graph: two
-    warm-up calls, then the mean of `calls` calls after an L2 flush
-    (informative; not part of `value`)."""
+    """µs/call of the same calls launched one by one, without a graph: every
+    case warmed first (`warmup` calls each, so no case pays for the idle
+    time before this pass), then per case the mean of `calls` calls after
+    an L2 flush (informative; not part of `value`)."""
     import torch
     out = {}
-    for r in runners:
-        with torch.cuda.stream(stream):
+    with torch.cuda.stream(stream):
+        for r in runners:
             for _ in range(warmup):
                 r.call()
+    torch.cuda.synchronize()
+    for r in runners:
+        with torch.cuda.stream(stream):
             flush.fill_(3)
             e0 = torch.cuda.Event(enable_timing=True)
             e1 = torch.cuda.Event(enable_timing=True)
@@ -917,6 +1111,8 @@ def make_parser() -> argparse.ArgumentParser:
                    help="run only the workload's case with this many elements per rank")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-variants", action="store_true")
+    p.add_argument("--no-hbm", action="store_true",
+                   help="default workload: skip the prefill and edge cases timed after the sweep")
     return p
 
 

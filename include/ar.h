@@ -165,7 +165,12 @@ typedef struct ar_info {
 } ar_info;
 
 /* Create a handle for R virtual ranks of N elements of `dtype` each, on the
- * current device.
+ * current device.  Source: the communication objects are set up once, on the
+ * host, before device code uses them ("microsoft/mscclpp" project page, "How
+ * it works": channels are defined on the host and called from kernels; SGLang
+ * guide, section 4.4: the communicator is built once at start-up).  What it
+ * allocates (packet scratch, epoch and status words) is this library's own
+ * design; the pages size no such buffers.
  *   R:     1 .. AR_MAX_RANKS.
  *   N:     >= 1 elements per rank.
  *   dtype: enum ar_dtype.
@@ -179,7 +184,8 @@ int ar_create(int R, size_t N, int dtype, ar_handle_t *out);
 
 /* Free the handle and its device memory.  Waits for the handle's device
  * first (whichever device is current; the caller's is restored).  NULL is
- * accepted and ignored. */
+ * accepted and ignored.  The pages define no teardown call: library
+ * plumbing. */
 int ar_destroy(ar_handle_t h);
 
 /* Sum all-reduce: for every rank r and element i < N,
@@ -202,7 +208,9 @@ int ar_allreduce(ar_handle_t h, const void *const in[], void *const out[],
                  int algo, int proto, cudaStream_t stream);
 
 /* ar_allreduce on the first n elements of every buffer, 1 <= n <= N (the
- * handle's N is the largest message it serves; n has its own shards, S =
+ * handle's N is the largest message it serves, as one SGLang communicator
+ * serves every message size it was tuned for: SGLang guide, section 4.4;
+ * n has its own shards, S =
  * ceil(n/R) rounded up to a 16-byte vector).  Buffers need n elements.
  * With AR_ALGO_AUTO and/or AR_PROTO_AUTO the library picks the half left
  * open, per message size: the tuned fastest choice after ar_tune, else a
@@ -227,7 +235,9 @@ int ar_tune(ar_handle_t h, cudaStream_t stream);
 
 /* The AUTO choice for a message of `bytes` per rank (*algo, *proto) and,
  * if `us` is not NULL, the tuned µs per call of the four pairs in the order
- * one-shot LL, one-shot HB, two-shot LL, two-shot HB (0 = not timed). */
+ * one-shot LL, one-shot HB, two-shot LL, two-shot HB (0 = not timed).  The
+ * lookup follows the tuned-configuration cache of the SGLang guide, section
+ * 4.4 (size rounded up to a power of two, clamped to [512 B, 256 MiB]). */
 int ar_get_tuning(ar_handle_t h, size_t bytes, int *algo, int *proto, float us[4]);
 
 /* Weighted per-token combine ("NCCL EP统一MoE通信生态", section 3.1 and
@@ -245,21 +255,24 @@ int ar_get_tuning(ar_handle_t h, size_t bytes, int *algo, int *proto, float us[4
 int ar_combine(ar_handle_t h, const void *const y[], const float *w, void *out, size_t T,
                size_t H, cudaStream_t stream);
 
-/* Reduce-scatter step of the two-shot schedule (HB): for every shard j,
+/* Reduce-scatter step of the two-shot schedule (the "rsag" algorithm of the
+ * SGLang guide, section 4.4), HB: for every shard j,
  *   out[j][i] = round_dtype(fold of in[0..R-1][i])  for i in shard j,
  * and nothing else is written.  Shards as in enum ar_algo.  Arguments,
  * alignment and aliasing rules as in ar_allreduce. */
 int ar_reduce_scatter(ar_handle_t h, const void *const in[], void *const out[],
                       cudaStream_t stream);
 
-/* All-gather step of the two-shot schedule: for every shard j and rank
+/* All-gather step of the two-shot schedule (SGLang guide, section 4.4,
+ * "rsag"): for every shard j and rank
  * r != j, copies out[j]'s shard j into out[r]'s shard j (bits unchanged).
  *   out: host array of R device pointers, N elements each, not overlapping.
  * ar_reduce_scatter followed by ar_all_gather on the same outputs equals
  * ar_allreduce. */
 int ar_all_gather(ar_handle_t h, void *const out[], cudaStream_t stream);
 
-/* LL encode of one message of n elements of the handle's dtype.
+/* LL encode of one message of n elements of the handle's dtype (the LL
+ * protocol of the MSCCL++ summary, section "MemoryChannel", protocol table).
  *   src:  device pointer, n elements.
  *   pkts: device pointer, ceil(n * elem_size / 4) 8-byte packets, 8-byte
  *         aligned.  Packet p = ((uint64_t)flag << 32) | payload, payload =
@@ -273,7 +286,8 @@ int ar_all_gather(ar_handle_t h, void *const out[], cudaStream_t stream);
 int ar_ll_pack(ar_handle_t h, const void *src, uint64_t *pkts, size_t n,
                uint32_t flag, cudaStream_t stream);
 
-/* LL decode: the inverse of ar_ll_pack.  A packet whose flag differs from
+/* LL decode (MSCCL++ summary, section "MemoryChannel", LL protocol): the
+ * inverse of ar_ll_pack.  A packet whose flag differs from
  * `flag` leaves its bytes of dst unwritten and records AR_ERR_FLAG_MISMATCH
  * in the handle's status word (read it with ar_status).  No waiting. */
 int ar_ll_unpack(ar_handle_t h, const uint64_t *pkts, void *dst, size_t n,
@@ -282,13 +296,15 @@ int ar_ll_unpack(ar_handle_t h, const uint64_t *pkts, void *dst, size_t n,
 /* Wait for `stream`, then return and clear the handle's device status word:
  * AR_OK, AR_ERR_TIMEOUT or AR_ERR_FLAG_MISMATCH (the first error recorded
  * since the last ar_status), or AR_ERR_CUDA if the stream reports a CUDA
- * error. */
+ * error.  The pages define no device-side error reporting (their waits are
+ * unbounded): library plumbing for this library's bounded waits. */
 int ar_status(ar_handle_t h, cudaStream_t stream);
 
 /* Limit, in nanoseconds, of every device-side wait (LL packet polls, TMA
  * barrier waits) of later calls.  Default 1e9 (one second); 0 restores the
  * default.  A wait past the limit records AR_ERR_TIMEOUT, makes the other
- * waiters of the same call give up, and the kernel returns normally. */
+ * waiters of the same call give up, and the kernel returns normally.  The
+ * pages define no such limit: library plumbing. */
 int ar_set_timeout(ar_handle_t h, uint64_t ns);
 
 /* Programmatic dependent launch for the handle's later calls (1 = on, the
@@ -309,19 +325,24 @@ int ar_set_ll_transport(ar_handle_t h, int transport);
 
 /* Fault injection for tests: virtual rank `rank` (0..R-1) writes no LL
  * packets in later LL calls, so its peers' polls time out (AR_ERR_TIMEOUT
- * from ar_status) and the kernel returns.  -1 turns it off. */
+ * from ar_status) and the kernel returns.  -1 turns it off.  The pages
+ * define no such call: test plumbing. */
 int ar_debug_drop_rank(ar_handle_t h, int rank);
 
 /* The final rounding step on its own: dst[i] = round_dtype(src[i]) for n
  * binary32 values, with the same conversion the all-reduce kernels use
  * (round to nearest even, no flush to zero).  src, dst: device pointers.
- * Errors: AR_ERR_INVALID. */
+ * Errors: AR_ERR_INVALID.  The pages print no rounding rule; this exposes
+ * the library's reading (one round-to-nearest-even narrowing) so that it can
+ * be checked exhaustively. */
 int ar_round(int dtype, const float *src, void *dst, size_t n, cudaStream_t stream);
 
-/* Fill *info (host pointer) with the handle's description. */
+/* Fill *info (host pointer) with the handle's description.  The pages define
+ * no such call: library plumbing. */
 int ar_get_info(ar_handle_t h, ar_info *info);
 
-/* Static string naming an ar_status_code. */
+/* Static string naming an ar_status_code.  The pages define no such call:
+ * library plumbing. */
 const char *ar_strerror(int code);
 
 /* ---------------------------------------------------------------------------
@@ -384,7 +405,8 @@ int ar_plan_compile(ar_handle_t h, const ar_op *ops, int nops, int nchunks,
 /* (ctas_per_rank == 0: as many as can be resident together, R * that <= the
  * device's capacity for the interpreter kernel.) */
 
-/* The two all-reduce algorithms as plans, with chunks_per_rank * R chunks:
+/* The two all-reduce algorithms of the SGLang guide, section 4.4 (one-shot
+ * packet and "rsag"), as plans with chunks_per_rank * R chunks:
  *   AR_ONE_SHOT: rank r reduces every input into out[r];
  *   AR_TWO_SHOT: rank j reduces shard j (chunks [j*K, (j+1)*K)) into out[j],
  *                then every rank copies every other shard into its output.
@@ -394,7 +416,8 @@ int ar_plan_compile(ar_handle_t h, const ar_op *ops, int nops, int nchunks,
 int ar_plan_builtin(ar_handle_t h, int algo, int chunks_per_rank, int ctas_per_rank,
                     ar_plan_t *out);
 
-/* Run the plan once on these buffers (host arrays of R device pointers, N
+/* Run the plan once (the runtime that interprets an execution plan, section
+ * "第二层：DSL API" above) on these buffers (host arrays of R device pointers, N
  * elements each; the 2R buffers must not overlap).  Capturable in a CUDA
  * graph: the run index comes from device-side epoch words.  Waits are
  * bounded by the handle's timeout; a timed-out run reports AR_ERR_TIMEOUT
@@ -402,10 +425,12 @@ int ar_plan_builtin(ar_handle_t h, int algo, int chunks_per_rank, int ctas_per_r
 int ar_plan_execute(ar_plan_t p, const void *const in[], void *const out[], cudaStream_t stream);
 
 /* Tasks (after fusion), inserted waits and signalling tasks of a compiled
- * plan (any pointer may be NULL). */
+ * plan (any pointer may be NULL).  The pages define no such call: library
+ * plumbing that exposes what the compiler of section "第二层：DSL API" did. */
 int ar_plan_stats(ar_plan_t p, int *tasks, int *waits, int *signals);
 
-/* Free a plan (waits for the device first).  NULL is accepted. */
+/* Free a plan (waits for the device first).  NULL is accepted.  The pages
+ * define no teardown call: library plumbing. */
 int ar_plan_destroy(ar_plan_t p);
 
 /* Bytes of packet scratch compiled into the library for
@@ -416,12 +441,13 @@ int ar_plan_destroy(ar_plan_t p);
 
 /* One-shot LL all-reduce that allocates nothing.  The pages have no
  * counterpart of this call; it exists for callers that cannot allocate
- * device memory where they run the collective: a plugin hook that an
- * inference engine calls while capturing its stream into a CUDA graph (an
- * allocation there is an illegal call during capture), or an engine that
- * serves all device memory from its own pool and forbids side allocations.
- * ar_create's scratch is unavailable to them; this call uses a fixed array
- * of static device memory inside the library instead.
+ * device memory where they run the collective: an inference engine that
+ * reserves nearly all of the GPU's memory up front for its own pool (KV
+ * cache, activations) and accounts for every byte, so a side allocation
+ * would fail or break its memory plan; or a hook on a latency-critical path
+ * that must not pay for cudaMalloc/cudaFree, which can synchronise the whole
+ * device.  ar_create's scratch is unavailable to them; this call uses a
+ * fixed array of static device memory inside the library instead.
  *   R, N, dtype: as in ar_create.   in, out, stream: as in ar_allreduce
  *   (same alignment and aliasing rules).
  * Computes exactly what ar_allreduce(h, in, out, AR_ONE_SHOT, AR_LL, stream)

@@ -78,7 +78,8 @@ def test_clock_rows():
     lines = [hdr.format(sm=s, a="Not Active", b="Not Active") for s in (1965, 1980, 1995)]
     lines.append("00000000:2C:00.0, 300, 2070, 100, 0x0, Active, Not Active, Not Active, Not Active")
     c = bench.parse_clock_rows(lines, "1B:00.0")
-    assert c == {"sm_mhz": 1980.0, "sm_max_mhz": 2070.0, "reasons": [], "samples": 3}
+    assert c == {"sm_mhz": 1980.0, "sm_max_mhz": 2070.0, "reasons": [], "samples": 3,
+                 "series": []}
     assert not bench.clocks_rejected(c)
     lines.append(hdr.format(sm=1900, a="Active", b="Active"))
     c = bench.parse_clock_rows(lines, "1B:00.0")
@@ -220,3 +221,36 @@ def test_workloads_match_the_configurations():
     _, comb = bench.workload_cases("combine")
     assert [(c["w"].K, c["w"].T, c["w"].H) for c in comb] == [(8, t, 8192) for t in (1, 16, 128, 4096)]
     assert bench.case_bytes(comb[-1]) == 9 * 4096 * 8192 * 2 + 4 * 4096 * 8
+
+
+def test_clock_rows_with_timestamps_bin_by_replay_window():
+    """Rows carrying nvidia-smi's timestamp give a (time, MHz) series; each
+    replay window takes the sample nearest its middle, if one is close."""
+    row = ("00000000:1B:00.0, {sm}, 2070, 900.5, 0x0, Not Active, Not Active, Not Active, "
+           "Not Active, 2026/12/03 05:29:{sec}")
+    lines = [row.format(sm=m, sec=t) for m, t in ((2070, "26.000"), (1800, "26.050"),
+                                                   (1500, "26.100"), (2070, "27.500"))]
+    c = bench.parse_clock_rows(lines, "1B:00.0")
+    t0 = bench.parse_smi_time("2026/12/03 05:29:26.000")
+    assert [round(t - t0, 3) for t, _ in c["series"]] == [0.0, 0.05, 0.1, 1.5]
+    assert [m for _, m in c["series"]] == [2070.0, 1800.0, 1500.0, 2070.0]
+    win = [(t0 + 0.045, t0 + 0.055), (t0 + 0.095, t0 + 0.101), (t0 + 0.8, t0 + 0.801)]
+    got = bench.clocks_for_windows(c["series"], win)
+    assert got == {"sm_mhz_median": 1650.0, "replays_with_sample": 2}
+    assert bench.clocks_for_windows([], win) == {"sm_mhz_median": None, "replays_with_sample": 0}
+    assert bench.parse_smi_time("not a time") is None
+
+
+def test_replay_stats():
+    # replays of 10 calls: 30..39 us per replay -> 3.0..3.9 us per call
+    st = bench.replay_stats([(30 + i) * 1e-3 for i in (9, 0, 5, 1, 8, 2, 7, 3, 6, 4)], 10)
+    assert st == {"us_p50": 3.45, "us_p90": 3.8, "us_min": 3.0, "us_max": 3.9, "replays": 10}
+    assert bench.replay_stats([0.005], 1) == {"us_p50": 5.0, "us_p90": 5.0, "us_min": 5.0,
+                                              "us_max": 5.0, "replays": 1}
+    assert bench.replay_stats([], 10) == {}
+
+
+def test_bench_options_parse():
+    a = bench.make_parser().parse_args(["--no-hbm", "--steps", "3", "--warmup", "3"])
+    assert a.no_hbm and a.workload == "sweep"
+    assert bench.HBM_WORKLOADS == ("prefill", "edge")
