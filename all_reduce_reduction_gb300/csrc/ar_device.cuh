@@ -317,23 +317,34 @@ __device__ __forceinline__ bool poll_vec(Poller &w, const uint64_t *p, uint4 &v)
 //
 // The handle keeps kEpochWords words, all equal to the last call's flag E
 // between calls.  CTA b of a launch with g CTAs reads word b at its start and
-// uses flag E + 1 (0 is skipped: zeroed scratch means "empty").  At its end
-// CTA b writes the new flag to words b, b + g, b + 2g, ...  Those sets are
-// disjoint and together cover every word, so each word is written exactly
-// once per call, no CTA writes a word another CTA of the same call reads,
-// and all words are equal again when the kernel ends.  No atomics, no
+// uses flag E + 1 (0 is skipped: zeroed scratch means "empty").  CTA b writes
+// the new flag to words b, b + g, b + 2g, ...  Those sets are disjoint and
+// together cover every word, so each word is written exactly once per call
+// and all words are equal again when the kernel ends; no atomics, no
 // last-block detection, whatever the grid size of each call.
+//
+// No CTA of a call reads any word but its own, so the words b + g, b + 2g,
+// ... are written as soon as the CTA has its flag (publish_epoch_others,
+// early in the kernel, overlapping the rest of its work); word b itself is
+// written last, once every thread of the CTA has read it
+// (publish_epoch_own).  The next call reads the words only after this grid
+// has completed (griddepcontrol.wait, or plain stream order).
 // ---------------------------------------------------------------------------
 __device__ __forceinline__ uint32_t call_flag(const Ctl &c) {
     uint32_t f = ld_u32_relaxed(c.epoch + blockIdx.x) + 1u;
     return f == 0u ? 1u : f;
 }
 
-__device__ __forceinline__ void publish_epoch(const Ctl &c, uint32_t flag) {
-    __syncthreads();   // every thread of this CTA has read word blockIdx.x
-    for (uint32_t w = blockIdx.x + threadIdx.x * gridDim.x; w < (uint32_t)kEpochWords;
+__device__ __forceinline__ void publish_epoch_others(const Ctl &c, uint32_t flag) {
+    for (uint32_t w = blockIdx.x + (threadIdx.x + 1) * gridDim.x; w < (uint32_t)kEpochWords;
          w += blockDim.x * gridDim.x)
         st_u32_relaxed(c.epoch + w, flag);
+}
+
+__device__ __forceinline__ void publish_epoch_own(const Ctl &c, uint32_t flag) {
+    __syncthreads();   // every thread of this CTA has read word blockIdx.x
+    if (threadIdx.x == 0)
+        st_u32_relaxed(c.epoch + blockIdx.x, flag);
 }
 
 }  // namespace ar

@@ -13,8 +13,10 @@
 namespace ar {
 
 // Words in a handle's epoch array.  Every LL kernel launch uses at most this
-// many CTAs (see the epoch scheme in ar_device.cuh).
-constexpr int kEpochWords = 8192;
+// many CTAs (see the epoch scheme in ar_device.cuh).  Every call rewrites all
+// of them, so the array is kept just above the largest grid the LL kernels
+// use on GB300 (1216 co-resident CTAs of the staged kernel: 152 SMs x 8).
+constexpr int kEpochWords = 2048;
 
 // Threads per CTA of the register (non-TMA) kernels and the LL kernels.
 constexpr int kRegThreads = 256;

@@ -104,6 +104,8 @@ __global__ void __launch_bounds__(kLlThreads) k_ll(const __grid_constant__ LlArg
             st_pkt(slot_r + q, make_pkt(load_payload<ESZ>(a.p.in[r], a.n, q), flag));
     }
 
+    publish_epoch_others(a.c, flag);
+
     if (!TWO) {
         // ---- one-shot: out[r] = fold of every slot -------------------------
         for (uint32_t q = q0; ok && q < P; q += qstep) {
@@ -134,7 +136,7 @@ __global__ void __launch_bounds__(kLlThreads) k_ll(const __grid_constant__ LlArg
         }
     }
 
-    publish_epoch(a.c, flag);
+    publish_epoch_own(a.c, flag);
 }
 
 // ---------------------------------------------------------------------------
@@ -191,6 +193,8 @@ __global__ void __launch_bounds__(kLlStagedThreads) k_ll_staged(const __grid_con
                    make_pkt(load_payload<ESZ>(a.p.in[k], a.n, 2 * U + j), flag));
     }
 
+    publish_epoch_others(a.c, flag);
+
     // ---- receive -----------------------------------------------------------------
     bool ok = true, aborted = false;
     for (uint32_t b = blockIdx.x; b < nblk; b += gridDim.x) {        // uniform per CTA
@@ -234,7 +238,7 @@ __global__ void __launch_bounds__(kLlStagedThreads) k_ll_staged(const __grid_con
         }
     }
 
-    publish_epoch(a.c, flag);
+    publish_epoch_own(a.c, flag);
 }
 
 // ---------------------------------------------------------------------------
@@ -300,6 +304,8 @@ __global__ void __launch_bounds__(kLlStagedThreads) k_ll2_staged(const __grid_co
             st_pkt(slot_k + 2 * U + j,
                    make_pkt(load_payload<ESZ>(a.p.in[k], a.n, 2 * U + j), flag));
     }
+
+    publish_epoch_others(a.c, flag);
 
     // ---- reduce-scatter: this CTA's blocks ----------------------------------
     bool ok = true, aborted = false;
@@ -388,7 +394,7 @@ __global__ void __launch_bounds__(kLlStagedThreads) k_ll2_staged(const __grid_co
             store_payload<ESZ>(a.p.out[k], a.n, 2 * U + j, gather1[j]);
     }
 
-    publish_epoch(a.c, flag);
+    publish_epoch_own(a.c, flag);
 }
 
 template <int DT> static const void *ll2_staged_kernel() {

@@ -99,6 +99,7 @@ __global__ void __launch_bounds__(kLlThreads) k_ll_cluster(const __grid_constant
     kernel_prologue();
     const uint32_t call = call_flag(a.c);                // names this call for the abort word
     Poller w{&a.c, call, 0};
+    publish_epoch_others(a.c, call);
 
     const uint64_t nbytes = a.n * ESZ;
     const uint64_t P = (nbytes + 3) / 4;
@@ -196,7 +197,7 @@ __global__ void __launch_bounds__(kLlThreads) k_ll_cluster(const __grid_constant
     // call gave up); the final barrier also keeps peers' smem alive while
     // remote stores of a given-up call may still be in flight.
     cluster_sync();
-    publish_epoch(a.c, call);
+    publish_epoch_own(a.c, call);
 }
 
 template <int DT> static const void *cluster_kernel() {

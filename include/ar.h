@@ -435,7 +435,7 @@ int ar_plan_destroy(ar_plan_t p);
 
 /* Bytes of packet scratch compiled into the library for
  * ar_allreduce_ll_static (every GPU that loads the library holds this much
- * static device memory, plus 33 KiB of control words, until the process
+ * static device memory, plus 8.25 KiB of control words, until the process
  * exits). */
 #define AR_NOALLOC_SCRATCH_BYTES (8u << 20)
 
