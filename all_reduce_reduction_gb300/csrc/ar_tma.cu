@@ -13,16 +13,21 @@
 //     item's tile of every input into one pipeline stage, completing on the
 //     stage's "full" mbarrier (expect_tx = R * len);
 //   consumers (8 warps): fold the R staged tiles in rank order (binary32),
-//     round, write the reduced tile to one of two shared output tiles, and
-//     release the input stage ("empty" mbarrier);
+//     round, write the reduced tile to one of four shared output tiles, and
+//     release the input stage ("empty" mbarrier); for R = 8, 16 and 32 the
+//     fold is instantiated with R fixed, fully unrolled, its shared-memory
+//     reads issued eight at a time;
 //   one consumer thread: R bulk copies shared -> global of the reduced tile,
 //     one per output (the all-gather step fed from shared memory, so the
 //     reduced shard is never re-read from HBM).
+// One named barrier among the consumers per item, after the fold: the four
+// output tiles give the bulk stores of an item three items' time to read
+// their tile before it is written again.
 // No multicast.  Minimal traffic: R reads + R writes of every byte.
 //
 // Every wait is bounded by the handle's timeout; a timed-out wait records
 // AR_ERR_TIMEOUT and raises a shared abort flag that all consumer threads
-// read after the same named barrier, so they leave together.  Before the CTA
+// read at the same named barrier, so they leave together.  Before the CTA
 // exits, bulk copies still in flight are waited for.
 #include "ar_device.cuh"
 
@@ -64,8 +69,8 @@ __device__ __forceinline__ void bulk_s2g(void *dst, uint32_t src, uint32_t bytes
 __device__ __forceinline__ void bulk_commit() {
     asm volatile("cp.async.bulk.commit_group;" ::: "memory");
 }
-__device__ __forceinline__ void bulk_wait_read_1() {
-    asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
+template <int N> __device__ __forceinline__ void bulk_wait_read() {
+    asm volatile("cp.async.bulk.wait_group.read %0;" :: "n"(N) : "memory");
 }
 __device__ __forceinline__ void bulk_wait_all() {
     asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
@@ -76,13 +81,18 @@ __device__ __forceinline__ void fence_async_shared() {
 __device__ __forceinline__ void fence_mbar_init() {
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
 }
-// Barrier 1 among the consumer warps only (the producer warp never joins it).
-// Non-aligned forms: the warps may arrive diverged.
-__device__ __forceinline__ void consumer_sync() {
-    asm volatile("barrier.sync 1, %0;" :: "n"(32 * kTmaConsumerWarps) : "memory");
-}
-// The same barrier, returning the OR of every consumer's `v`: one uniform
-// decision, whatever each thread saw on its own.
+// Threads that take part in the consumers' named barrier: every thread of
+// the consumer warps, and no other (the producer warp never joins it).  A
+// count that differed from the threads arriving would never complete.
+constexpr int kConsumerThreads = 32 * kTmaConsumerWarps;
+static_assert(kTmaThreads == 32 + kConsumerThreads,
+              "the block is one producer warp plus the consumer warps");
+static_assert(kConsumerThreads % 32 == 0 && kConsumerThreads <= 1024 - 32,
+              "a named barrier counts whole warps");
+
+// Barrier 1 among the consumer warps, returning the OR of every consumer's
+// `v`: one uniform decision, whatever each thread saw on its own.
+// Non-aligned form: the warps may arrive diverged.
 __device__ __forceinline__ bool consumer_sync_or(bool v) {
     uint32_t r;
     asm volatile(
@@ -90,7 +100,7 @@ __device__ __forceinline__ bool consumer_sync_or(bool v) {
         "setp.ne.u32 q, %1, 0;\n\t"
         "barrier.red.or.pred p, 1, %2, q;\n\t"
         "selp.u32 %0, 1, 0, p;\n\t}"
-        : "=r"(r) : "r"((uint32_t)v), "n"(32 * kTmaConsumerWarps) : "memory");
+        : "=r"(r) : "r"((uint32_t)v), "n"(kConsumerThreads) : "memory");
     return r != 0;
 }
 
@@ -130,16 +140,25 @@ __device__ __forceinline__ bool item_range(const TmaArgs &a, uint64_t i, uint64_
     return true;
 }
 
-template <int DT>
+// Output tiles: the reduced tile of item i goes to out tile i % kOutTiles.
+// With four, the bulk stores of an item have three items' time to finish
+// reading their tile before it is written again, so one consumer barrier per
+// item suffices: before it, the elected thread waits until the stores of
+// item i - 3 have read their tile (the tile item i + 1 writes).
+constexpr int kOutTiles = 4;
+static_assert(kOutTiles >= 2, "an item's tile must not be the previous item's");
+
+template <int DT, int RC>
 __global__ void __launch_bounds__(kTmaThreads, 1) k_two_shot_tma(const __grid_constant__ TmaArgs a) {
     extern __shared__ __align__(128) uint8_t smem[];
     __shared__ int abort_flag;
     __shared__ uint64_t consumed_items;
 
-    const int R = a.R, T = a.tile_bytes, S = a.stages;
+    const int R = RC ? RC : a.R;
+    const int T = a.tile_bytes, S = a.stages;
     uint8_t *in_tiles = smem;                                   // [S][R][T]
-    uint8_t *out_tiles = smem + (size_t)S * R * T;              // [2][T]
-    uint64_t *bars = reinterpret_cast<uint64_t *>(out_tiles + 2 * (size_t)T);
+    uint8_t *out_tiles = smem + (size_t)S * R * T;              // [kOutTiles][T]
+    uint64_t *bars = reinterpret_cast<uint64_t *>(out_tiles + kOutTiles * (size_t)T);
     const uint32_t full0 = smem_u32(bars), empty0 = smem_u32(bars + S);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const uint64_t items = a.tiles_per_shard * (uint64_t)R;
@@ -185,7 +204,6 @@ __global__ void __launch_bounds__(kTmaThreads, 1) k_two_shot_tma(const __grid_co
         const int ct = threadIdx.x - 32;
         const bool elected = ct == 0;
         uint64_t done = 0;
-        int ob = 0;
         for (uint64_t i = blockIdx.x; i < items; i += gridDim.x) {
             uint64_t off;
             uint32_t len;
@@ -194,33 +212,47 @@ __global__ void __launch_bounds__(kTmaThreads, 1) k_two_shot_tma(const __grid_co
             const int stage = (int)(done % S);
             const uint32_t parity = (uint32_t)((done / S) & 1u);
             const bool ok = mbar_wait(full0 + 8 * stage, parity, a.c, abortp);
-            if (elected)
-                bulk_wait_read_1();   // output tile `ob` is no longer being stored
-            if (consumer_sync_or(!ok || *abortp))
-                break;                // every consumer leaves at the same item
-
-            const uint8_t *tile = in_tiles + (size_t)stage * R * T;
-            uint8_t *otile = out_tiles + (size_t)ob * T;
-            for (uint32_t p = (uint32_t)ct * 16u; p < len; p += 16u * 32u * kTmaConsumerWarps) {
-                VecAcc<DT> acc;
-                acc.init(*reinterpret_cast<const uint4 *>(tile + p));
+            uint8_t *otile = out_tiles + (size_t)(done % kOutTiles) * T;
+            if (ok) {
+                const uint8_t *tile = in_tiles + (size_t)stage * R * T;
+                for (uint32_t p = (uint32_t)ct * 16u; p < len; p += 16u * kConsumerThreads) {
+                    VecAcc<DT> acc;
+                    acc.init(*reinterpret_cast<const uint4 *>(tile + p));
+                    if constexpr (RC > 0) {
+#pragma unroll
+                        for (int k0 = 1; k0 < RC; k0 += 8) {
+                            uint4 x[8];
+#pragma unroll
+                            for (int j = 0; j < 8; ++j)
+                                if (k0 + j < RC)
+                                    x[j] = *reinterpret_cast<const uint4 *>(tile + (size_t)(k0 + j) * T + p);
+#pragma unroll
+                            for (int j = 0; j < 8; ++j)
+                                if (k0 + j < RC)
+                                    acc.add(x[j]);
+                        }
+                    } else {
 #pragma unroll 4
-                for (int k = 1; k < R; ++k)
-                    acc.add(*reinterpret_cast<const uint4 *>(tile + (size_t)k * T + p));
-                *reinterpret_cast<uint4 *>(otile + p) = acc.result();
+                        for (int k = 1; k < R; ++k)
+                            acc.add(*reinterpret_cast<const uint4 *>(tile + (size_t)k * T + p));
+                    }
+                    *reinterpret_cast<uint4 *>(otile + p) = acc.result();
+                }
             }
             __syncwarp();
             if (lane == 0)
                 mbar_arrive(empty0 + 8 * stage);
             fence_async_shared();
-            consumer_sync();
+            if (elected)
+                bulk_wait_read<kOutTiles - 2>();   // item done - 3 has read its tile
+            if (consumer_sync_or(!ok || *abortp))
+                break;                             // every consumer leaves at the same item
             if (elected) {
                 const uint32_t src = smem_u32(otile);
                 for (int r = 0; r < R; ++r)
                     bulk_s2g(static_cast<uint8_t *>(a.p.out[r]) + off, src, len);
                 bulk_commit();
             }
-            ob ^= 1;
             ++done;
         }
         if (elected) {
@@ -262,7 +294,19 @@ __global__ void __launch_bounds__(kTmaThreads, 1) k_two_shot_tma(const __grid_co
 }
 
 size_t tma_smem_bytes(int R, int tile_bytes, int stages) {
-    return (size_t)stages * R * tile_bytes + 2 * (size_t)tile_bytes + 2 * sizeof(uint64_t) * stages;
+    return (size_t)stages * R * tile_bytes + kOutTiles * (size_t)tile_bytes +
+           2 * sizeof(uint64_t) * stages;
+}
+
+// R fixed at compile time for the rank counts of the workloads (fold fully
+// unrolled, shared-memory reads eight at a time); other R loop.
+template <int DT> static void *tma_kernel_for(int R) {
+    switch (R) {
+    case 8: return reinterpret_cast<void *>(&k_two_shot_tma<DT, 8>);
+    case 16: return reinterpret_cast<void *>(&k_two_shot_tma<DT, 16>);
+    case 32: return reinterpret_cast<void *>(&k_two_shot_tma<DT, 32>);
+    default: return reinterpret_cast<void *>(&k_two_shot_tma<DT, 0>);
+    }
 }
 
 // Dynamic shared memory the kernel may opt in to: the device's per-block
@@ -274,12 +318,17 @@ template <int DT> static cudaError_t prepare_dt(int *limit) {
     if (e == cudaSuccess)
         e = cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
     if (e == cudaSuccess)
-        e = cudaFuncGetAttributes(&fa, k_two_shot_tma<DT>);
+        e = cudaFuncGetAttributes(&fa, tma_kernel_for<DT>(0));
     if (e != cudaSuccess)
         return e;
     *limit = optin - (int)fa.sharedSizeBytes;
-    return cudaFuncSetAttribute(k_two_shot_tma<DT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                *limit);
+    for (int R : {0, 8, 16, 32}) {
+        e = cudaFuncSetAttribute(tma_kernel_for<DT>(R), cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 *limit);
+        if (e != cudaSuccess)
+            return e;
+    }
+    return cudaSuccess;
 }
 
 cudaError_t tma_prepare(int dtype, int *max_dynamic_smem) {
@@ -292,11 +341,23 @@ cudaError_t tma_prepare(int dtype, int *max_dynamic_smem) {
 
 cudaError_t launch_two_shot_tma(const TmaArgs &a, int dtype, int grid, cudaStream_t s, bool pdl) {
     const size_t smem = tma_smem_bytes(a.R, a.tile_bytes, a.stages);
-    switch (dtype) {
-    case AR_BF16: return launch_kernel(k_two_shot_tma<AR_BF16>, grid, kTmaThreads, smem, s, pdl, a);
-    case AR_FP16: return launch_kernel(k_two_shot_tma<AR_FP16>, grid, kTmaThreads, smem, s, pdl, a);
-    default: return launch_kernel(k_two_shot_tma<AR_FP32>, grid, kTmaThreads, smem, s, pdl, a);
+    void *k = dtype == AR_BF16 ? tma_kernel_for<AR_BF16>(a.R)
+            : dtype == AR_FP16 ? tma_kernel_for<AR_FP16>(a.R) : tma_kernel_for<AR_FP32>(a.R);
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)grid);
+    cfg.blockDim = dim3(kTmaThreads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    cfg.numAttrs = 0;
+    if (pdl) {
+        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[0].val.programmaticStreamSerializationAllowed = 1;
+        cfg.numAttrs = 1;
     }
+    cfg.attrs = attr;
+    void *args[] = {const_cast<TmaArgs *>(&a)};
+    return cudaLaunchKernelExC(&cfg, k, args);
 }
 
 }  // namespace ar
