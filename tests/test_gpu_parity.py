@@ -104,6 +104,23 @@ def test_many_tiles_ragged_tail(path, dtype, R):
     run_case(R, (1 << 20) + 5, dtype, *path, dist="normal")
 
 
+@pytest.mark.parametrize("R,n,dtype", [(8, (4 << 20) + 3, "bf16"), (16, (2 << 20) + 5, "fp16"),
+                                       (32, (1 << 20) + 7, "fp32"), (3, 3 << 20, "bf16"),
+                                       (5, (2 << 20) + 1, "fp32")],
+                         ids=["r8_bf16", "r16_fp16", "r32_fp32", "r3_bf16", "r5_fp32"])
+def test_two_shot_tma_many_items_per_cta(R, n, dtype):
+    """Two-shot HB with every CTA folding 5 to 14 items, so each of the four
+    shared output tiles is reused while earlier bulk stores may still be
+    reading: R fixed at compile time (8, 16, 32) and a runtime R (3, 5),
+    each with a ragged tail."""
+    run_case(R, n, dtype, ar.AR_TWO_SHOT, ar.AR_HB, dist="normal")
+    with ar.Handle(R, n, dtype) as h:
+        info = ar.ar_get_info(h.h)
+    body = n * wl.ELEM_SIZE[dtype] // 16 * 16
+    items = -(-body // info["tma_tile_bytes"])
+    assert items >= 5 * info["num_sms"], (items, info["tma_tile_bytes"])
+
+
 @pytest.mark.parametrize("path", ALL_PATHS, ids=PATH_IDS)
 @pytest.mark.parametrize("dtype", DTYPES)
 @pytest.mark.parametrize("offset", [1, 2, 3])
