@@ -31,6 +31,7 @@ AR_ERR_NOMEM = 4
 AR_ERR_TIMEOUT = 5
 AR_ERR_FLAG_MISMATCH = 6
 AR_LL_AUTO, AR_LL_GLOBAL, AR_LL_CLUSTER = 0, 1, 2
+AR_HB_STAGING_AUTO, AR_HB_STAGING_TMA, AR_HB_STAGING_DIRECT = 0, 1, 2
 AR_MAX_RANKS = 32
 AR_LL_MAX_BYTES = 64 << 20
 
@@ -67,6 +68,7 @@ class ar_info(ctypes.Structure):
         ("ll_cluster_max", ctypes.c_int),
         ("pdl", ctypes.c_int),
         ("ll_staged_ctas_max", ctypes.c_int),
+        ("hb_staging", ctypes.c_int),
     ]
 
     def as_dict(self) -> dict:
@@ -114,6 +116,8 @@ SIGNATURES = {
     "ar_set_timeout": ([_VP, _U64], _I),
     "ar_debug_drop_rank": ([_VP, _I], _I),
     "ar_set_ll_transport": ([_VP, _I], _I),
+    "ar_set_hb_staging": ([_VP, _I], _I),
+    "ar_get_hb_staging": ([_VP, _SZ, ctypes.POINTER(_I)], _I),
     "ar_set_pdl": ([_VP, _I], _I),
     "ar_round": ([_I, _VP, _VP, _SZ, _VP], _I),
     "ar_get_info": ([_VP, ctypes.POINTER(ar_info)], _I),
@@ -264,6 +268,18 @@ def ar_set_pdl(h: int, enable: int) -> None:
 
 def ar_set_ll_transport(h: int, transport: int) -> None:
     _check(load_library().ar_set_ll_transport(h, transport), "ar_set_ll_transport")
+
+
+def ar_set_hb_staging(h: int, staging: int) -> None:
+    _check(load_library().ar_set_hb_staging(h, staging), "ar_set_hb_staging")
+
+
+def ar_get_hb_staging(h: int, nbytes: int) -> int:
+    """AR_HB_STAGING_TMA or AR_HB_STAGING_DIRECT: what a two-shot HB call of
+    `nbytes` per rank (16-byte-aligned buffers) would use now."""
+    out = ctypes.c_int(0)
+    _check(load_library().ar_get_hb_staging(h, nbytes, ctypes.byref(out)), "ar_get_hb_staging")
+    return out.value
 
 
 def ar_debug_drop_rank(h: int, rank: int) -> None:

@@ -18,6 +18,14 @@ constexpr int kMaxBucketLog2 = 28;
 constexpr int kBuckets = kMaxBucketLog2 - kMinBucketLog2 + 1;
 // ar_tune times 15 sizes, 2^9 .. 2^23 bytes per rank (the page's [2^9, 2^24)).
 constexpr int kTuneMaxLog2 = 23;
+// Two-shot HB with AR_HB_STAGING_AUTO before ar_tune (and above the tuned
+// sizes): TMA staging where it measured faster on GB300, direct staging
+// elsewhere.  T = bytes moved per call, 2 R n elem_size.
+static bool tma_band(int R, uint64_t T) {
+    const uint64_t MiB = (uint64_t)1 << 20;
+    return (R >= 8 && T >= 16 * MiB && T <= 64 * MiB) ||
+           (R >= 32 && T >= 256 * 1024 && T <= 64 * MiB);
+}
 
 struct ar_handle {
     int R;
@@ -43,8 +51,12 @@ struct ar_handle {
     // 2^(9+b) bytes per rank), timed by ar_tune; us[algo][proto], 0 = untimed
     float tuned_us[kBuckets][2][2];
     int tuned_max;          // largest tuned bucket, -1 before ar_tune
+    // two-shot HB staging per bucket, timed by ar_tune: enum ar_hb_staging,
+    // AR_HB_STAGING_AUTO = not timed
+    int tuned_hb2[kBuckets];
     int pdl;                // launch with programmatic dependent launch
     int ll_transport;       // enum ar_ll_transport
+    int hb_staging;         // enum ar_hb_staging
     bool cluster_ok;        // the cluster LL kernel can run for this R
     uint64_t cluster_uc;    // its 16-byte units per rank per chunk (largest)
     int cluster_max;        // co-resident clusters at that chunk size
@@ -170,9 +182,27 @@ int one_shot_hb(ar_handle *h, const Call &c) {
                                         32 * h->one_shot_warps, c.s, h->pdl));
 }
 
+int bucket_of(uint64_t bytes);
+
+// Staging of a two-shot HB call of n elements per rank whose buffers are all
+// 16-byte aligned: the handle's setting; with AR_HB_STAGING_AUTO the faster
+// one timed by ar_tune at the message's size bucket, else the fixed rule of
+// tma_band.
+int hb2_staging(const ar_handle *h, uint64_t n) {
+    if (h->hb_staging != AR_HB_STAGING_AUTO)
+        return h->hb_staging;
+    const uint64_t bytes = n * h->esz;
+    if (h->tuned_max >= 0) {
+        const int b = bucket_of(bytes);
+        if (b <= h->tuned_max && h->tuned_hb2[b] != AR_HB_STAGING_AUTO)
+            return h->tuned_hb2[b];
+    }
+    return tma_band(h->R, 2 * (uint64_t)h->R * bytes) ? AR_HB_STAGING_TMA : AR_HB_STAGING_DIRECT;
+}
+
 int two_shot_hb(ar_handle *h, const Call &c) {
     const uint64_t body = (c.n * h->esz) / 16 * 16;
-    if (c.vec16 && body > 0) {
+    if (c.vec16 && body > 0 && hb2_staging(h, c.n) == AR_HB_STAGING_TMA) {
         TmaArgs a;
         fill_ptrs(h, c.in, c.out, &a.p);
         a.n = c.n;
@@ -187,7 +217,8 @@ int two_shot_hb(ar_handle *h, const Call &c) {
         const int grid = clamp_grid(items, h->num_sms);
         return from_cuda(launch_two_shot_tma(a, h->dtype, grid, c.s, h->pdl));
     }
-    // unaligned buffers: one thread per element reduces once, stores R times
+    // direct staging, or unaligned buffers: one thread per 16-byte vector (or
+    // per element) folds the R inputs once and stores R copies
     const HbArgs a = hb_args(h, c);
     const uint64_t units = c.vec16 ? c.n / (16 / h->esz) : c.n;
     const int grid = clamp_grid(ceil_div(units, kRegThreads), h->reg_cap);
@@ -269,9 +300,10 @@ int bucket_of(uint64_t bytes) {
 // Resolve AR_ALGO_AUTO / AR_PROTO_AUTO for a message of `bytes` per rank:
 // the fastest tuned (algo, proto) allowed by the fixed half of the request,
 // or, before ar_tune, a fixed rule from GB300 measurements: one-shot HB up to
-// 2 MiB / R per rank (its fold work grows with R^2: the measured crossovers
-// are about 512 KiB at R = 4, 256 KiB at R = 8, 128 KiB at R = 16, 32-128
-// KiB at R = 32), two-shot HB above; with LL forced, one-shot up to 2 MiB.
+// max(64 KiB, 512 KiB / R) per rank, two-shot HB above (the one-shot's fold
+// work grows with R^2; against the two-shot with its AUTO staging the
+// measured crossovers are about 64 KiB at R = 8, 16 and 32 and 256-512 KiB
+// at R = 4); with LL forced, one-shot up to 2 MiB.
 void resolve(const ar_handle *h, uint64_t bytes, int *algo, int *proto) {
     const bool ll_ok = h->slots != nullptr;
     if (h->tuned_max >= 0) {
@@ -302,7 +334,11 @@ void resolve(const ar_handle *h, uint64_t bytes, int *algo, int *proto) {
     if (*proto == AR_PROTO_AUTO)
         *proto = AR_HB;
     if (*algo == AR_ALGO_AUTO) {
-        const uint64_t limit = *proto == AR_LL ? (2u << 20) : (2u << 20) / (uint64_t)h->R;
+        uint64_t limit = (512u << 10) / (uint64_t)h->R;
+        if (limit < (64u << 10))
+            limit = 64u << 10;
+        if (*proto == AR_LL)
+            limit = 2u << 20;
         *algo = bytes <= limit ? AR_ONE_SHOT : AR_TWO_SHOT;
     }
 }
@@ -415,12 +451,15 @@ int ar_create(int R, size_t N, int dtype, ar_handle_t *out) {
     h->tma_stages = stages;
 
     h->tuned_max = -1;                       // AUTO uses the fixed rule until ar_tune
-    for (int b = 0; b < kBuckets; ++b)
+    for (int b = 0; b < kBuckets; ++b) {
         for (int a = 0; a < 2; ++a)
             for (int p = 0; p < 2; ++p)
                 h->tuned_us[b][a][p] = 0.f;
+        h->tuned_hb2[b] = AR_HB_STAGING_AUTO;
+    }
     h->pdl = 1;
     h->ll_transport = AR_LL_AUTO;
+    h->hb_staging = AR_HB_STAGING_AUTO;
 
     // cluster LL: one CTA per virtual rank in a cluster (portable up to 8,
     // 16 with the non-portable size); receive buffers of ~64 KiB per CTA
@@ -611,46 +650,65 @@ int ar_tune(ar_handle_t h, cudaStream_t stream) {
         c.vec16 = c.vec8 = true;
         c.inplace = false;
         c.s = ts;
+        // µs per call of (a, p): a graph of 10 calls, 5 warm-up replays, 20
+        // timed replays; < 0 on a CUDA failure
+        auto time_path = [&](int a, int p) -> float {
+            cudaGraph_t g = nullptr;
+            cudaGraphExec_t ge = nullptr;
+            if (run_path(h, c, a, p) != AR_OK ||
+                cudaStreamBeginCapture(ts, cudaStreamCaptureModeThreadLocal) != cudaSuccess)
+                return -1.f;
+            int crc = AR_OK;
+            for (int k = 0; k < 10 && crc == AR_OK; ++k)
+                crc = run_path(h, c, a, p);
+            if (cudaStreamEndCapture(ts, &g) != cudaSuccess || crc != AR_OK ||
+                cudaGraphInstantiate(&ge, g, 0) != cudaSuccess) {
+                if (g)
+                    cudaGraphDestroy(g);
+                return -1.f;
+            }
+            float ms = 0.f;
+            bool okc = true;
+            for (int k = 0; k < 5 && okc; ++k)
+                okc = cudaGraphLaunch(ge, ts) == cudaSuccess;
+            okc = okc && cudaEventRecord(e0, ts) == cudaSuccess;
+            for (int k = 0; k < 20 && okc; ++k)
+                okc = cudaGraphLaunch(ge, ts) == cudaSuccess;
+            okc = okc && cudaEventRecord(e1, ts) == cudaSuccess &&
+                  cudaEventSynchronize(e1) == cudaSuccess &&
+                  cudaEventElapsedTime(&ms, e0, e1) == cudaSuccess;
+            cudaGraphExecDestroy(ge);
+            cudaGraphDestroy(g);
+            return okc ? ms * 1000.f / 200.f : -1.f;
+        };
         for (int a = 0; a < 2 && rc == AR_OK; ++a)
             for (int p = 0; p < 2 && rc == AR_OK; ++p) {
                 h->tuned_us[b][a][p] = 0.f;
                 if (p == AR_LL && !h->slots)
                     continue;
-                // 10 calls per graph, 5 warm-up replays, 20 timed replays
-                cudaGraph_t g = nullptr;
-                cudaGraphExec_t ge = nullptr;
-                if (run_path(h, c, a, p) != AR_OK ||
-                    cudaStreamBeginCapture(ts, cudaStreamCaptureModeThreadLocal) != cudaSuccess) {
+                if (a == AR_TWO_SHOT && p == AR_HB) {
+                    // both stagings (the buffers here are 16-byte aligned);
+                    // the faster is kept for this size
+                    const int user = h->hb_staging;
+                    h->hb_staging = AR_HB_STAGING_TMA;
+                    const float t_tma = time_path(a, p);
+                    h->hb_staging = AR_HB_STAGING_DIRECT;
+                    const float t_dir = t_tma < 0.f ? -1.f : time_path(a, p);
+                    h->hb_staging = user;
+                    if (t_tma < 0.f || t_dir < 0.f) {
+                        rc = AR_ERR_CUDA;
+                        break;
+                    }
+                    h->tuned_hb2[b] = t_dir < t_tma ? AR_HB_STAGING_DIRECT : AR_HB_STAGING_TMA;
+                    h->tuned_us[b][a][p] = t_dir < t_tma ? t_dir : t_tma;
+                    continue;
+                }
+                const float us = time_path(a, p);
+                if (us < 0.f) {
                     rc = AR_ERR_CUDA;
                     break;
                 }
-                int crc = AR_OK;
-                for (int k = 0; k < 10 && crc == AR_OK; ++k)
-                    crc = run_path(h, c, a, p);
-                if (cudaStreamEndCapture(ts, &g) != cudaSuccess || crc != AR_OK ||
-                    cudaGraphInstantiate(&ge, g, 0) != cudaSuccess) {
-                    if (g)
-                        cudaGraphDestroy(g);
-                    rc = AR_ERR_CUDA;
-                    break;
-                }
-                float ms = 0.f;
-                bool okc = true;
-                for (int k = 0; k < 5 && okc; ++k)
-                    okc = cudaGraphLaunch(ge, ts) == cudaSuccess;
-                okc = okc && cudaEventRecord(e0, ts) == cudaSuccess;
-                for (int k = 0; k < 20 && okc; ++k)
-                    okc = cudaGraphLaunch(ge, ts) == cudaSuccess;
-                okc = okc && cudaEventRecord(e1, ts) == cudaSuccess &&
-                      cudaEventSynchronize(e1) == cudaSuccess &&
-                      cudaEventElapsedTime(&ms, e0, e1) == cudaSuccess;
-                cudaGraphExecDestroy(ge);
-                cudaGraphDestroy(g);
-                if (!okc) {
-                    rc = AR_ERR_CUDA;
-                    break;
-                }
-                h->tuned_us[b][a][p] = ms * 1000.f / 200.f;
+                h->tuned_us[b][a][p] = us;
             }
         if (rc == AR_OK)
             last = b;
@@ -765,6 +823,21 @@ int ar_set_ll_transport(ar_handle_t h, int transport) {
     return AR_OK;
 }
 
+int ar_set_hb_staging(ar_handle_t h, int staging) {
+    if (!h || (staging != AR_HB_STAGING_AUTO && staging != AR_HB_STAGING_TMA &&
+               staging != AR_HB_STAGING_DIRECT))
+        return AR_ERR_INVALID;
+    h->hb_staging = staging;
+    return AR_OK;
+}
+
+int ar_get_hb_staging(ar_handle_t h, size_t bytes, int *staging) {
+    if (!h || !staging || bytes == 0 || bytes > h->N * h->esz)
+        return AR_ERR_INVALID;
+    *staging = hb2_staging(h, bytes / h->esz > 0 ? bytes / h->esz : 1);
+    return AR_OK;
+}
+
 int ar_debug_drop_rank(ar_handle_t h, int rank) {
     if (!h || rank < -1 || rank >= h->R)
         return AR_ERR_INVALID;
@@ -799,6 +872,7 @@ int ar_get_info(ar_handle_t h, ar_info *info) {
     info->tma_stages = h->tma_stages;
     info->timeout_ns = h->ctl.timeout_ns;
     info->ll_transport = h->ll_transport;
+    info->hb_staging = h->hb_staging;
     info->pdl = h->pdl;
     info->ll_cluster_ok = h->cluster_ok ? 1 : 0;
     info->ll_cluster_units = h->cluster_ok ? (int)h->cluster_uc : 0;

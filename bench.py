@@ -39,6 +39,7 @@ METRIC = ("all-reduce µs/call and GB/s vs msg size (R=8 bf16, 1 GB300), "
 FALLBACK_HBM_GBS = 6800.0
 NOMINAL_HBM_GBS = 7900.0        # GB300 HBM3e, nominal (context beside the measured peak)
 TRANSPORTS = {"auto": 0, "global": 1, "cluster": 2}   # enum ar_ll_transport
+STAGINGS = {"auto": 0, "tma": 1, "direct": 2}          # enum ar_hb_staging
 L2_FLUSH_BYTES = 256 << 20
 
 
@@ -60,6 +61,8 @@ def workload_cases(name: str, args=None):
             args.R, args.n, args.dtype,
             ("%s plan (%d chunks/rank, %d CTAs/rank)" % (args.plan, args.plan_chunks, args.plan_ctas))
             if args.plan else "%s %s" % (args.algo, args.proto), args.calls)
+        if args.staging != "auto":
+            desc += " (two-shot HB staging: %s)" % args.staging
     elif name == "sweep":
         cases = [dict(w=w, algo="one_shot", proto="ll", calls=10, flush=True) for w in wl.LL_SWEEP]
         desc = ("r8_bf16_ll_sweep: R=8 virtual ranks, bf16, N=2^9..2^18 elements per rank "
@@ -76,12 +79,12 @@ def workload_cases(name: str, args=None):
     elif name == "prefill":
         cases = [dict(w=wl.PREFILL, algo="two_shot", proto="hb", calls=1, flush=False)]
         desc = ("r16_bf16_prefill: R=16, bf16 [8192, 8192] per rank (128 MiB), N(0,1), "
-                "two-shot HB with TMA staging")
+                "two-shot HB (staging: %s)" % (args.staging if args else "auto"))
     elif name == "edge":
         w = [x for x in wl.EDGE if x.R == 32 and x.dtype == "fp32"][0]
         cases = [dict(w=w, algo="two_shot", proto="hb", calls=1, flush=False)]
         desc = ("r32_fp32_edge: R=32, fp32, N=4097*4096+3 per rank, log-uniform |x| in "
-                "[1e-4,1e4), two-shot HB")
+                "[1e-4,1e4), two-shot HB (staging: %s)" % (args.staging if args else "auto"))
     else:
         raise SystemExit("unknown workload " + name)
     return desc, cases
@@ -280,6 +283,16 @@ def ll_wire_bytes(r):
     return r.w.R * (2 * nb + 2 * packets)
 
 
+def staged_path(r, path: str) -> str:
+    """The kernel family of a case's path: two-shot HB is named with the
+    staging its calls use (its buffers are all 16-byte aligned here)."""
+    import all_reduce_reduction_gb300 as ar
+    if path != "two_shot_hb":
+        return path
+    st = ar.ar_get_hb_staging(r.h.h, r.w.n * {"bf16": 2, "fp16": 2, "fp32": 4}[r.w.dtype])
+    return "two_shot_hb_tma" if st == ar.AR_HB_STAGING_TMA else "two_shot_hb_direct"
+
+
 def hbm_peak():
     try:
         with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
@@ -296,7 +309,8 @@ KERNEL_SOURCES = {
     "two_shot_ll": [("ar_ll.cu", ["k_ll2_staged", "launch_ll_staged"])],
     "one_shot_ll_cluster": ["ar_ll_cluster.cu"],
     "one_shot_hb": ["ar_hb.cu"],
-    "two_shot_hb": ["ar_tma.cu"],
+    "two_shot_hb_tma": ["ar_tma.cu"],
+    "two_shot_hb_direct": [("ar_hb.cu", ["k_reduce", "reduce_dt", "launch_reduce"])],
     "combine": ["ar_combine.cu"],
     # a plan's traffic follows its compiled tasks: the compiler counts too
     "plan_": [("ar_plan.cu", ["k_plan", "compile_plan", "builtin_plan", "ar_plan_execute"])],
@@ -450,6 +464,7 @@ class CaseRunner:
         else:
             self.h = ar.Handle(w.R, w.n, w.dtype)
         ar.ar_set_ll_transport(self.h.h, c.get("transport", ar.AR_LL_AUTO))
+        ar.ar_set_hb_staging(self.h.h, c.get("staging", ar.AR_HB_STAGING_AUTO))
         ar.ar_set_pdl(self.h.h, c.get("pdl", 1))
         self.algo, self.proto = ar.ALGOS.get(c["algo"], 0), ar.PROTOS[c["proto"]]
         self.choice = "combine" if c.get("combine") else None
@@ -517,6 +532,7 @@ def run_ours(args, dist: Dist):
         desc += " (only the case of %d elements per rank)" % args.only
     for c in cases:
         c["transport"] = TRANSPORTS[args.ll_transport]
+        c["staging"] = STAGINGS[args.staging]
         c["pdl"] = 0 if args.no_pdl else 1
     stream = torch.cuda.Stream()
     runners = [CaseRunner(c, stream) for c in cases]
@@ -603,7 +619,7 @@ def run_ours(args, dist: Dist):
     achieved = dr.bytes / launch_s / 1e9
     path = dr.choice or ("plan_" + dr.c["plan"] if dr.c.get("plan") else
                          "%s_%s" % (dr.c["algo"], dr.c["proto"]))
-    kkey = "%s_r%d_n%d_%s" % (path, dr.w.R, dr.w.n, dr.w.dtype)
+    kkey = "%s_r%d_n%d_%s" % (staged_path(dr, path), dr.w.R, dr.w.n, dr.w.dtype)
     if path == "one_shot_ll":
         info = ar.ar_get_info(dr.h.h)
         tr = dr.c.get("transport", ar.AR_LL_AUTO)
@@ -758,67 +774,80 @@ def run_ours(args, dist: Dist):
 
 
 # the bandwidth-bound workloads timed after the default sweep: the prefill
-# all-reduce (R=16, 128 MiB per rank, bf16, two-shot HB with TMA staging) and
-# the R=32 binary32 edge case (two-shot HB)
+# all-reduce (R=16, 128 MiB per rank, bf16, two-shot HB) and the R=32 binary32
+# edge case (two-shot HB), each with both two-shot HB stagings
 HBM_WORKLOADS = ("prefill", "edge")
 
 
 def measure_hbm_workloads(stream, bus, peak, dist, replays=20, warmup=3) -> dict:
-    """µs/call and minimal-bytes GB/s of the HBM_WORKLOADS, one at a time:
-    the case's single-call graph replayed `warmup` times, then `replays`
-    times with a CUDA event pair around each replay, under its own clock
-    sampler.  Inputs and outputs (4.3 GB per call) are far larger than L2,
-    so no flush is needed.  Each case's buffers are freed before the next."""
+    """µs/call and minimal-bytes GB/s of the HBM_WORKLOADS, one at a time,
+    each with TMA staging and with direct staging (keys `<workload>_tma`,
+    `<workload>_direct`; `auto_staging` marks the one AUTO picks): the case's
+    single-call graph replayed `warmup` times, then `replays` times with a
+    CUDA event pair around each replay, under its own clock sampler.  Inputs
+    and outputs (4.3 GB per call) are far larger than L2, so no flush is
+    needed.  Each workload's buffers are freed before the next."""
     import torch
     import all_reduce_reduction_gb300 as ar
     out = {}
     for name in HBM_WORKLOADS:
         desc, cases = workload_cases(name)
-        c = cases[0]
+        c = dict(cases[0])
         r = CaseRunner(c, stream, host_buffers=False)
-        for _ in range(warmup):
-            r.graph.replay()
-        torch.cuda.synchronize()
-        sampler = ClockSampler(bus)
-        sampler.start()
-        time.sleep(0.2)
-        evs = []
-        dist.barrier()
-        torch.cuda.synchronize()
-        for _ in range(replays):
-            with torch.cuda.stream(stream):
-                e0 = torch.cuda.Event(enable_timing=True)
-                e1 = torch.cuda.Event(enable_timing=True)
-                e0.record(stream)
-                r.graph.replay()
-                e1.record(stream)
-            evs.append((e0, e1))
-        torch.cuda.synchronize()
-        dist.barrier()
-        time.sleep(0.1)
-        clocks = sampler.stop()
-        if clocks:
-            clocks.pop("series", None)
-        st = ar.ar_status(r.h.h, stream)
-        if st != ar.AR_OK:
-            raise RuntimeError("device status after the %s workload: %s" % (name, ar.ar_strerror(st)))
-        times = [e0.elapsed_time(e1) for e0, e1 in evs]
-        calls = c["calls"]
-        us = dist.max(sum(times) * 1e3 / (replays * calls))
-        gbs = r.bytes / us / 1e3
-        key = "%s_%s_r%d_n%d_%s" % (c["algo"], c["proto"], r.w.R, r.w.n, r.w.dtype)
-        out[name] = {
-            "workload": desc, "R": r.w.R, "n": r.w.n, "dtype": r.w.dtype,
-            "algo": c["algo"], "proto": c["proto"],
-            "warmup_calls": warmup * calls, "timed_calls": replays * calls,
-            "us_per_call": round(us, 3), **replay_stats(times, calls),
-            "min_bytes_per_call": r.bytes, "min_bytes_GBps": round(gbs, 1),
-            "peak": peak, "frac_of_hbm_peak": round(gbs / peak, 4),
-            "frac_of_nominal": round(gbs / NOMINAL_HBM_GBS, 4),
-            "traffic": committed_traffic(key), "kernel": key,
-            "l2": "inputs and outputs far larger than L2 (no flush)",
-            "clocks": clocks, "clocks_rejected": clocks_rejected(clocks),
-        }
+        auto = staged_path(r, "two_shot_hb")
+        for st_name, st in (("tma", ar.AR_HB_STAGING_TMA), ("direct", ar.AR_HB_STAGING_DIRECT)):
+            ar.ar_set_hb_staging(r.h.h, st)
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=stream):
+                for _ in range(c["calls"]):
+                    r.call()
+            for _ in range(warmup):
+                g.replay()
+            torch.cuda.synchronize()
+            sampler = ClockSampler(bus)
+            sampler.start()
+            time.sleep(0.2)
+            evs = []
+            dist.barrier()
+            torch.cuda.synchronize()
+            for _ in range(replays):
+                with torch.cuda.stream(stream):
+                    e0 = torch.cuda.Event(enable_timing=True)
+                    e1 = torch.cuda.Event(enable_timing=True)
+                    e0.record(stream)
+                    g.replay()
+                    e1.record(stream)
+                evs.append((e0, e1))
+            torch.cuda.synchronize()
+            dist.barrier()
+            time.sleep(0.1)
+            clocks = sampler.stop()
+            if clocks:
+                clocks.pop("series", None)
+            stc = ar.ar_status(r.h.h, stream)
+            if stc != ar.AR_OK:
+                raise RuntimeError("device status after the %s workload: %s"
+                                   % (name, ar.ar_strerror(stc)))
+            times = [e0.elapsed_time(e1) for e0, e1 in evs]
+            calls = c["calls"]
+            us = dist.max(sum(times) * 1e3 / (replays * calls))
+            gbs = r.bytes / us / 1e3
+            key = "two_shot_hb_%s_r%d_n%d_%s" % (st_name, r.w.R, r.w.n, r.w.dtype)
+            out["%s_%s" % (name, st_name)] = {
+                "workload": desc.replace("staging: auto", "staging: " + st_name),
+                "R": r.w.R, "n": r.w.n, "dtype": r.w.dtype,
+                "algo": "two_shot", "proto": "hb", "staging": st_name,
+                "auto_staging": auto == "two_shot_hb_" + st_name,
+                "warmup_calls": warmup * calls, "timed_calls": replays * calls,
+                "us_per_call": round(us, 3), **replay_stats(times, calls),
+                "min_bytes_per_call": r.bytes, "min_bytes_GBps": round(gbs, 1),
+                "peak": peak, "frac_of_hbm_peak": round(gbs / peak, 4),
+                "frac_of_nominal": round(gbs / NOMINAL_HBM_GBS, 4),
+                "traffic": committed_traffic(key), "kernel": key,
+                "l2": "inputs and outputs far larger than L2 (no flush)",
+                "clocks": clocks, "clocks_rejected": clocks_rejected(clocks),
+            }
+            del g
         r.close()
         del r
         torch.cuda.empty_cache()
@@ -874,15 +903,19 @@ def measure_variants(runners, stream, flush, K):
     import torch
     import all_reduce_reduction_gb300 as ar
     out = {}
-    for algo, proto, tr in (("one_shot", "hb", ar.AR_LL_AUTO), ("two_shot", "hb", ar.AR_LL_AUTO),
-                            ("two_shot", "ll", ar.AR_LL_AUTO),
-                            ("one_shot", "ll", ar.AR_LL_GLOBAL), ("one_shot", "ll", ar.AR_LL_CLUSTER),
-                            ("auto", "auto", ar.AR_LL_AUTO)):
+    for algo, proto, tr, st in (("one_shot", "hb", ar.AR_LL_AUTO, 0), ("two_shot", "hb", ar.AR_LL_AUTO, 0),
+                                ("two_shot", "hb", ar.AR_LL_AUTO, ar.AR_HB_STAGING_TMA),
+                                ("two_shot", "hb", ar.AR_LL_AUTO, ar.AR_HB_STAGING_DIRECT),
+                                ("two_shot", "ll", ar.AR_LL_AUTO, 0),
+                                ("one_shot", "ll", ar.AR_LL_GLOBAL, 0),
+                                ("one_shot", "ll", ar.AR_LL_CLUSTER, 0),
+                                ("auto", "auto", ar.AR_LL_AUTO, 0)):
         row = {}
         for r in runners:
             if algo == "auto" and r.choice is None:
                 ar.ar_tune(r.h.h, stream)
             ar.ar_set_ll_transport(r.h.h, tr)
+            ar.ar_set_hb_staging(r.h.h, st)
             g = torch.cuda.CUDAGraph()
             with torch.cuda.graph(g, stream=stream):
                 for _ in range(r.c["calls"]):
@@ -903,9 +936,12 @@ def measure_variants(runners, stream, flush, K):
                 tot += e0.elapsed_time(e1)
             row[str(r.w.n)] = round(tot * 1e3 / (K * r.c["calls"]), 3)
             ar.ar_set_ll_transport(r.h.h, r.c.get("transport", ar.AR_LL_AUTO))
+            ar.ar_set_hb_staging(r.h.h, r.c.get("staging", ar.AR_HB_STAGING_AUTO))
         key = "%s_%s" % (algo, proto) if algo != "auto" else "auto_tuned"
         if proto == "ll" and algo == "one_shot":
             key += "_" + {ar.AR_LL_GLOBAL: "global", ar.AR_LL_CLUSTER: "cluster"}[tr]
+        if st:
+            key += "_" + {ar.AR_HB_STAGING_TMA: "tma", ar.AR_HB_STAGING_DIRECT: "direct"}[st]
         out[key] = row
     torch.cuda.synchronize()
     return out
@@ -1103,6 +1139,8 @@ def make_parser() -> argparse.ArgumentParser:
     p.add_argument("--plan-chunks", type=int, default=0, help="0: one chunk per CTA")
     p.add_argument("--plan-ctas", type=int, default=0, help="0: fill the resident capacity")
     p.add_argument("--ll-transport", default="auto", choices=["auto", "global", "cluster"])
+    p.add_argument("--staging", default="auto", choices=["auto", "tma", "direct"],
+                   help="two-shot HB staging (enum ar_hb_staging)")
     p.add_argument("--no-pdl", action="store_true",
                    help="launch without programmatic dependent launch")
     p.add_argument("--impl", default="ours", choices=["ours", "reference"])

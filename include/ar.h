@@ -128,6 +128,35 @@ enum ar_ll_transport {
     AR_LL_CLUSTER = 2
 };
 
+/* How two-shot HB calls move their data when every buffer is 16-byte aligned
+ * (other buffers always take the direct form, element by element).
+ *   AR_HB_STAGING_TMA:    bulk copies (the Tensor Memory Accelerator) bring
+ *                         tiles of the R inputs into shared memory, the tile
+ *                         is folded once and bulk-stored to the R outputs;
+ *                         one CTA per SM.  Best for large messages.
+ *   AR_HB_STAGING_DIRECT: one thread per 16-byte vector loads the R inputs
+ *                         into registers, folds them once and stores R copies;
+ *                         as many CTAs as the message needs.  Lower latency
+ *                         for small and mid-sized messages.
+ *   AR_HB_STAGING_AUTO:   per message size: after ar_tune, the one timed
+ *                         faster at that size; before it, and above the
+ *                         largest tuned size, a fixed rule from GB300
+ *                         measurements: with T = 2 * R * n * elem_size bytes
+ *                         moved per call, TMA when R >= 8 and 16 MiB <= T <=
+ *                         64 MiB, or R >= 32 and 256 KiB <= T <= 64 MiB;
+ *                         DIRECT otherwise (including every large message:
+ *                         its many CTAs keep more loads in flight).
+ * Both are the reduce-scatter + all-gather schedule fused per unit (each
+ * unit reduced once, by its shard's owner, and replicated) and give
+ * identical results.  Source: the SGLang guide, section 4.4 (each algorithm
+ * is timed over candidate launch configurations and the fastest kept per
+ * message size). */
+enum ar_hb_staging {
+    AR_HB_STAGING_AUTO = 0,
+    AR_HB_STAGING_TMA = 1,
+    AR_HB_STAGING_DIRECT = 2
+};
+
 enum ar_status_code {
     AR_OK = 0,
     AR_ERR_INVALID = 1,        /* bad argument (null, range, aliasing, device) */
@@ -162,6 +191,7 @@ typedef struct ar_info {
     int ll_staged_ctas_max;    /* CTAs of the staged one-shot LL kernel (every
                                   buffer 8-byte aligned), each serving all R
                                   ranks                                       */
+    int hb_staging;            /* enum ar_hb_staging in force                  */
 } ar_info;
 
 /* Create a handle for R virtual ranks of N elements of `dtype` each, on the
@@ -214,8 +244,9 @@ int ar_allreduce(ar_handle_t h, const void *const in[], void *const out[],
  * ceil(n/R) rounded up to a 16-byte vector).  Buffers need n elements.
  * With AR_ALGO_AUTO and/or AR_PROTO_AUTO the library picks the half left
  * open, per message size: the tuned fastest choice after ar_tune, else a
- * fixed rule from GB300 measurements (HB; one-shot up to 2 MiB / R per rank,
- * two-shot above; with AR_LL forced, one-shot up to 2 MiB).
+ * fixed rule from GB300 measurements (HB; one-shot up to max(64 KiB,
+ * 512 KiB / R) per rank, two-shot above; with AR_LL forced, one-shot up to
+ * 2 MiB).
  * Errors: as ar_allreduce; AR_ERR_INVALID also for n == 0 or n > N. */
 int ar_allreduce_n(ar_handle_t h, const void *const in[], void *const out[], size_t n,
                    int algo, int proto, cudaStream_t stream);
@@ -226,8 +257,10 @@ int ar_allreduce_n(ar_handle_t h, const void *const in[], void *const out[], siz
  * size, rounded up to a power of two and clamped to [512 B, 256 MiB], to the
  * fastest).  Here: each (algo, proto) pair is timed at every power of two
  * from 512 B to min(8 MiB, N * elem_size) bytes per rank as a graph of 10
- * calls, 5 warm-up replays then 20 timed replays; sizes above the largest
- * tuned one use its choice.  Not a hot-path call: it waits for `stream`,
+ * calls, 5 warm-up replays then 20 timed replays, two-shot HB once per
+ * staging (enum ar_hb_staging; the faster is kept for that size and used by
+ * later two-shot HB calls with AR_HB_STAGING_AUTO); sizes above the largest
+ * tuned one use its (algo, proto) choice.  Not a hot-path call: it waits for `stream`,
  * allocates and frees 2 * R temporary buffers, creates a private stream and
  * synchronises.  Returns AR_OK or the first error (including a device-side
  * one, as ar_status would). */
@@ -322,6 +355,16 @@ int ar_set_pdl(ar_handle_t h, int enable);
  * that memory can be HBM or a cluster peer's shared memory.
  * Errors: AR_ERR_INVALID. */
 int ar_set_ll_transport(ar_handle_t h, int transport);
+
+/* Choose how later two-shot HB calls move their data (enum ar_hb_staging;
+ * AR_HB_STAGING_AUTO is the default).  Errors: AR_ERR_INVALID. */
+int ar_set_hb_staging(ar_handle_t h, int staging);
+
+/* The staging (AR_HB_STAGING_TMA or AR_HB_STAGING_DIRECT) a two-shot HB call
+ * of `bytes` per rank (1 .. N * elem_size) on this handle would use now, with
+ * every buffer 16-byte aligned.  Errors: AR_ERR_INVALID (NULL, bytes out of
+ * range). */
+int ar_get_hb_staging(ar_handle_t h, size_t bytes, int *staging);
 
 /* Fault injection for tests: virtual rank `rank` (0..R-1) writes no LL
  * packets in later LL calls, so its peers' polls time out (AR_ERR_TIMEOUT

@@ -91,8 +91,11 @@ def test_clock_rows():
 
 
 def test_traffic_lookup_needs_matching_digest():
-    d = bench.kernel_source_digest("two_shot_hb_r16_n67108864_bf16")
+    d = bench.kernel_source_digest("two_shot_hb_tma_r16_n67108864_bf16")
     assert len(d) == 16
+    # the two stagings of the two-shot HB are different kernels
+    assert bench.kernel_source_digest("two_shot_hb_direct_r16_n67108864_bf16") not in (d, "unknown")
+    assert bench.kernel_source_digest("two_shot_hb_r16_n67108864_bf16") == "unknown"
     assert bench.kernel_source_digest("no_such_kernel") == "unknown"
     assert bench.committed_traffic("no_such_kernel") is None
 
@@ -252,5 +255,9 @@ def test_replay_stats():
 
 def test_bench_options_parse():
     a = bench.make_parser().parse_args(["--no-hbm", "--steps", "3", "--warmup", "3"])
-    assert a.no_hbm and a.workload == "sweep"
+    assert a.no_hbm and a.workload == "sweep" and a.staging == "auto"
     assert bench.HBM_WORKLOADS == ("prefill", "edge")
+    b = bench.make_parser().parse_args(["--workload", "custom", "--staging", "tma"])
+    assert bench.STAGINGS[b.staging] == 1
+    desc, _ = bench.workload_cases("custom", b)
+    assert "staging: tma" in desc

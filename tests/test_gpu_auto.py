@@ -55,9 +55,10 @@ def test_n_out_of_range_rejected():
 
 @pytest.mark.parametrize("R", [4, 8, 16, 32])
 def test_untuned_rule(R):
-    """Before ar_tune: HB, one-shot up to 2 MiB / R per rank, two-shot above."""
+    """Before ar_tune: HB, one-shot up to max(64 KiB, 512 KiB / R) per rank,
+    two-shot above."""
     need_gpu()
-    limit = (2 << 20) // R
+    limit = max(64 << 10, (512 << 10) // R)
     with ar.Handle(R, 1 << 21, "bf16") as h:
         assert ar.ar_get_tuning(h.h, 4096)[:2] == (ar.AR_ONE_SHOT, ar.AR_HB)
         assert ar.ar_get_tuning(h.h, limit)[:2] == (ar.AR_ONE_SHOT, ar.AR_HB)
@@ -119,3 +120,48 @@ def test_auto_in_a_captured_graph():
         for r in range(R):
             assert_bits_equal(outs[r], want, "bf16", "replay %d rank %d" % (rep, r))
     h.close()
+
+
+@pytest.mark.parametrize("R", [2, 4, 8, 16, 32])
+def test_untuned_staging_rule(R):
+    """Before ar_tune, two-shot HB stages with TMA only in the band where it
+    measured faster (R >= 8 and 16-64 MiB moved per call, or R >= 32 and
+    256 KiB-64 MiB), directly elsewhere; a fixed setting overrides it."""
+    need_gpu()
+    MiB = 1 << 20
+    with ar.Handle(R, 64 << 20, "bf16") as h:
+        for nbytes in [1024, 4096, 65536, 1 << 20, 2 << 20, 4 << 20, 8 << 20, 32 << 20, 64 << 20]:
+            T = 2 * R * nbytes
+            band = (R >= 8 and 16 * MiB <= T <= 64 * MiB) or (R >= 32 and 256 * 1024 <= T <= 64 * MiB)
+            want = ar.AR_HB_STAGING_TMA if band else ar.AR_HB_STAGING_DIRECT
+            assert ar.ar_get_hb_staging(h.h, nbytes) == want, (R, nbytes)
+        for fixed in (ar.AR_HB_STAGING_TMA, ar.AR_HB_STAGING_DIRECT):
+            ar.ar_set_hb_staging(h.h, fixed)
+            assert ar.ar_get_hb_staging(h.h, 4096) == fixed
+            assert ar.ar_get_info(h.h)["hb_staging"] == fixed
+        with pytest.raises(ar.ArError):
+            ar.ar_set_hb_staging(h.h, 3)
+        with pytest.raises(ar.ArError):
+            ar.ar_get_hb_staging(h.h, 0)
+
+
+@pytest.mark.parametrize("R,dtype", [(8, "bf16"), (32, "fp32")])
+def test_tune_keeps_the_faster_staging(R, dtype):
+    """ar_tune times two-shot HB with both stagings and keeps one per size;
+    either way the results stay exact."""
+    need_gpu()
+    N = (1 << 20) + 3
+    cpu = wl.make_inputs(73, R, N, dtype, "normal")
+    with ar.Handle(R, N, dtype) as h:
+        ar.ar_tune(h.h)
+        esz = wl.ELEM_SIZE[dtype]
+        seen = set()
+        for lg in range(9, 24):
+            if (1 << lg) > N * esz:
+                break
+            st = ar.ar_get_hb_staging(h.h, 1 << lg)
+            assert st in (ar.AR_HB_STAGING_TMA, ar.AR_HB_STAGING_DIRECT), (lg, st)
+            seen.add(st)
+        assert seen
+        for n in (1000, 70001, N):
+            _prefix_case(h.h, R, N, n, dtype, ar.AR_TWO_SHOT, ar.AR_HB, cpu)

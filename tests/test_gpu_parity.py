@@ -19,7 +19,7 @@ DTYPES = ["bf16", "fp16", "fp32"]
 
 
 def run_case(R, n, dtype, algo, proto, dist="loguniform", config=40, offset=0, inplace=False,
-             transport=None):
+             transport=None, staging=None):
     need_gpu()
     cpu = wl.make_inputs(config, R, n, dtype, dist)
     want = expected(cpu, dtype)
@@ -31,6 +31,8 @@ def run_case(R, n, dtype, algo, proto, dist="loguniform", config=40, offset=0, i
     with ar.Handle(R, n, dtype) as h:
         if transport is not None:
             ar.ar_set_ll_transport(h.h, transport)
+        if staging is not None:
+            ar.ar_set_hb_staging(h.h, staging)
         ar.ar_allreduce(h.h, ins, outs, algo, proto)
         st = ar.ar_status(h.h)
         assert st == ar.AR_OK, ar.ar_strerror(st)
@@ -113,12 +115,35 @@ def test_two_shot_tma_many_items_per_cta(R, n, dtype):
     shared output tiles is reused while earlier bulk stores may still be
     reading: R fixed at compile time (8, 16, 32) and a runtime R (3, 5),
     each with a ragged tail."""
-    run_case(R, n, dtype, ar.AR_TWO_SHOT, ar.AR_HB, dist="normal")
+    run_case(R, n, dtype, ar.AR_TWO_SHOT, ar.AR_HB, dist="normal", staging=ar.AR_HB_STAGING_TMA)
     with ar.Handle(R, n, dtype) as h:
         info = ar.ar_get_info(h.h)
     body = n * wl.ELEM_SIZE[dtype] // 16 * 16
     items = -(-body // info["tma_tile_bytes"])
     assert items >= 5 * info["num_sms"], (items, info["tma_tile_bytes"])
+
+
+STAGINGS = [ar.AR_HB_STAGING_TMA, ar.AR_HB_STAGING_DIRECT]
+STAGING_IDS = ["tma", "direct"]
+
+
+@pytest.mark.parametrize("staging", STAGINGS, ids=STAGING_IDS)
+@pytest.mark.parametrize("dtype", DTYPES)
+@pytest.mark.parametrize("R", [1, 3, 8, 16, 32])
+@pytest.mark.parametrize("n", [1, 9, 100, 4097, 70001, (1 << 20) + 5])
+def test_two_shot_hb_stagings(staging, dtype, R, n):
+    """Two-shot HB with each staging forced: the same bits as the oracle
+    (buffers 16-byte aligned, so the chosen staging runs)."""
+    run_case(R, n, dtype, ar.AR_TWO_SHOT, ar.AR_HB, staging=staging)
+
+
+@pytest.mark.parametrize("staging", STAGINGS, ids=STAGING_IDS)
+@pytest.mark.parametrize("offset", [0, 1])
+def test_two_shot_hb_stagings_in_place(staging, offset):
+    """In place, aligned (the chosen staging) and one element off (element by
+    element whatever the setting)."""
+    run_case(8, 300001, "bf16", ar.AR_TWO_SHOT, ar.AR_HB, offset=offset, inplace=True,
+             staging=staging)
 
 
 @pytest.mark.parametrize("path", ALL_PATHS, ids=PATH_IDS)

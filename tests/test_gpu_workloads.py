@@ -27,12 +27,14 @@ def oracle_single_output(cpu_inputs, dtype):
     return out
 
 
-def run_graph(w, algo, proto, cpu, calls=10, warm=2, transport=ar.AR_LL_AUTO):
+def run_graph(w, algo, proto, cpu, calls=10, warm=2, transport=ar.AR_LL_AUTO,
+              staging=ar.AR_HB_STAGING_AUTO):
     ins = [t.cuda() for t in cpu]
     outs = [torch.full_like(t, float("nan")) for t in ins]
     s = torch.cuda.Stream()
     with ar.Handle(w.R, w.n, w.dtype) as h:
         ar.ar_set_ll_transport(h.h, transport)
+        ar.ar_set_hb_staging(h.h, staging)
         if algo == ar.AR_ALGO_AUTO or proto == ar.AR_PROTO_AUTO:
             ar.ar_tune(h.h, s)                           # as the decode benchmark does
         with torch.cuda.stream(s):
@@ -85,11 +87,15 @@ def prefill():
     return w, cpu, oracle_single_output(cpu, w.dtype)
 
 
-@pytest.mark.parametrize("algo", [ar.AR_TWO_SHOT, ar.AR_ONE_SHOT], ids=["two_shot", "one_shot"])
-def test_prefill_full_size(prefill, algo):
-    """R=16 bf16 [8192, 8192] per rank (128 MiB), HB."""
+@pytest.mark.parametrize("algo,staging", [(ar.AR_TWO_SHOT, ar.AR_HB_STAGING_TMA),
+                                          (ar.AR_TWO_SHOT, ar.AR_HB_STAGING_DIRECT),
+                                          (ar.AR_ONE_SHOT, ar.AR_HB_STAGING_AUTO)],
+                         ids=["two_shot_tma", "two_shot_direct", "one_shot"])
+def test_prefill_full_size(prefill, algo, staging):
+    """R=16 bf16 [8192, 8192] per rank (128 MiB), HB (two-shot with either
+    staging)."""
     w, cpu, want = prefill
-    outs = run_graph(w, algo, ar.AR_HB, cpu, calls=1, warm=1)
+    outs = run_graph(w, algo, ar.AR_HB, cpu, calls=1, warm=1, staging=staging)
     for r in range(w.R):
         assert_bits_equal(outs[r], want, w.dtype, "prefill rank %d" % r)
     del outs
@@ -109,9 +115,13 @@ def test_edge_full_size(w):
             with ar.Handle(w.R, w.n, w.dtype) as h:
                 assert ar.ar_get_info(h.h)["ll_capable"] == 0
             continue
-        outs = run_graph(w, algo, proto, cpu, calls=1, warm=1)
-        for r in range(w.R):
-            assert_bits_equal(outs[r], want, w.dtype, "%s algo %d proto %d rank %d"
-                              % (w.name, algo, proto, r))
-        del outs
-        torch.cuda.empty_cache()
+        stagings = [ar.AR_HB_STAGING_AUTO]
+        if algo == ar.AR_TWO_SHOT and proto == ar.AR_HB:
+            stagings = [ar.AR_HB_STAGING_TMA, ar.AR_HB_STAGING_DIRECT]
+        for staging in stagings:
+            outs = run_graph(w, algo, proto, cpu, calls=1, warm=1, staging=staging)
+            for r in range(w.R):
+                assert_bits_equal(outs[r], want, w.dtype, "%s algo %d proto %d staging %d rank %d"
+                                  % (w.name, algo, proto, staging, r))
+            del outs
+            torch.cuda.empty_cache()
