@@ -23,7 +23,7 @@ constexpr int kTuneMaxLog2 = 23;
 // elsewhere.  T = bytes moved per call, 2 R n elem_size.
 static bool tma_band(int R, uint64_t T) {
     const uint64_t MiB = (uint64_t)1 << 20;
-    return (R >= 8 && T >= 16 * MiB && T <= 64 * MiB) ||
+    return (R >= 16 && T >= 16 * MiB && T <= 64 * MiB) ||
            (R >= 32 && T >= 256 * 1024 && T <= 64 * MiB);
 }
 
@@ -218,11 +218,13 @@ int two_shot_hb(ar_handle *h, const Call &c) {
         return from_cuda(launch_two_shot_tma(a, h->dtype, grid, c.s, h->pdl));
     }
     // direct staging, or unaligned buffers: one thread per 16-byte vector (or
-    // per element) folds the R inputs once and stores R copies
+    // per element) folds the R inputs once and stores R copies; up to 64 MiB
+    // moved per call the vector form runs held to four CTAs per SM
     const HbArgs a = hb_args(h, c);
     const uint64_t units = c.vec16 ? c.n / (16 / h->esz) : c.n;
     const int grid = clamp_grid(ceil_div(units, kRegThreads), h->reg_cap);
-    return from_cuda(launch_reduce(a, h->dtype, c.vec16, false, grid, c.s, h->pdl));
+    const bool occupancy4 = 2 * (uint64_t)h->R * c.n * h->esz <= ((uint64_t)64 << 20);
+    return from_cuda(launch_reduce(a, h->dtype, c.vec16, false, grid, c.s, h->pdl, occupancy4));
 }
 
 // One-shot LL through thread-block clusters (R peers per cluster exchange

@@ -211,11 +211,15 @@ __global__ void __launch_bounds__(1024) k_one_shot_hb(const __grid_constant__ Hb
 // ---------------------------------------------------------------------------
 // Reduce: one thread per unit folds the R inputs once, then stores either to
 // the output of the unit's shard owner only (reduce-scatter step) or to all
-// R outputs (fused two-shot).  The thread reads everything before it writes
-// and no other thread touches its unit, so in place is safe.
+// R outputs (fused two-shot: the direct staging of the two-shot HB).  The
+// thread reads everything before it writes and no other thread touches its
+// unit, so in place is safe.  k_reduce_o4 is the fused vector form held to
+// 64 registers (four CTAs per SM instead of three): more loads in flight,
+// which the direct staging wants up to 64 MiB moved per call (L2-sized work)
+// and not above, where the extra concurrency measured slower.
 // ---------------------------------------------------------------------------
 template <int DT, bool VEC, bool SCATTER>
-__global__ void __launch_bounds__(kRegThreads) k_reduce(const __grid_constant__ HbArgs a) {
+__device__ __forceinline__ void reduce_body(const HbArgs &a) {
     kernel_prologue();
     constexpr int PV = VEC ? Elem<DT>::kPerVec : 1;
     const int R = a.R;
@@ -254,6 +258,16 @@ __global__ void __launch_bounds__(kRegThreads) k_reduce(const __grid_constant__ 
             }
         }
     }
+}
+
+template <int DT, bool VEC, bool SCATTER>
+__global__ void __launch_bounds__(kRegThreads) k_reduce(const __grid_constant__ HbArgs a) {
+    reduce_body<DT, VEC, SCATTER>(a);
+}
+
+template <int DT>
+__global__ void __launch_bounds__(kRegThreads, 4) k_reduce_o4(const __grid_constant__ HbArgs a) {
+    reduce_body<DT, true, false>(a);
 }
 
 // ---------------------------------------------------------------------------
@@ -380,10 +394,12 @@ cudaError_t launch_one_shot_hb(const HbArgs &a, int dtype, bool vec, bool single
 }
 
 template <int DT>
-static cudaError_t reduce_dt(const HbArgs &a, bool vec, bool scatter, int grid, cudaStream_t s,
-                             bool pdl) {
+static cudaError_t reduce_dt(const HbArgs &a, bool vec, bool scatter, bool occupancy4, int grid,
+                             cudaStream_t s, bool pdl) {
     if (vec && scatter)
         return launch_kernel(k_reduce<DT, true, true>, grid, kRegThreads, 0, s, pdl, a);
+    if (vec && occupancy4)
+        return launch_kernel(k_reduce_o4<DT>, grid, kRegThreads, 0, s, pdl, a);
     if (vec)
         return launch_kernel(k_reduce<DT, true, false>, grid, kRegThreads, 0, s, pdl, a);
     if (scatter)
@@ -392,11 +408,11 @@ static cudaError_t reduce_dt(const HbArgs &a, bool vec, bool scatter, int grid, 
 }
 
 cudaError_t launch_reduce(const HbArgs &a, int dtype, bool vec, bool scatter_only, int grid,
-                          cudaStream_t s, bool pdl) {
+                          cudaStream_t s, bool pdl, bool occupancy4) {
     switch (dtype) {
-    case AR_BF16: return reduce_dt<AR_BF16>(a, vec, scatter_only, grid, s, pdl);
-    case AR_FP16: return reduce_dt<AR_FP16>(a, vec, scatter_only, grid, s, pdl);
-    default: return reduce_dt<AR_FP32>(a, vec, scatter_only, grid, s, pdl);
+    case AR_BF16: return reduce_dt<AR_BF16>(a, vec, scatter_only, occupancy4, grid, s, pdl);
+    case AR_FP16: return reduce_dt<AR_FP16>(a, vec, scatter_only, occupancy4, grid, s, pdl);
+    default: return reduce_dt<AR_FP32>(a, vec, scatter_only, occupancy4, grid, s, pdl);
     }
 }
 

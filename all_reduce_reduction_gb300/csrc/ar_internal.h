@@ -171,8 +171,9 @@ cudaError_t one_shot_prepare();                 // opt in to the one-shot ring's
 // `single`: the grid covers the message, every CTA has at most one run
 cudaError_t launch_one_shot_hb(const HbArgs &a, int dtype, bool vec, bool single, int grid,
                                int block, cudaStream_t s, bool pdl = false);
+// occupancy4: the fused form held to four CTAs per SM (vectors only)
 cudaError_t launch_reduce(const HbArgs &a, int dtype, bool vec, bool scatter_only, int grid,
-                          cudaStream_t s, bool pdl = false);
+                          cudaStream_t s, bool pdl = false, bool occupancy4 = false);
 cudaError_t launch_all_gather(const HbArgs &a, int dtype, bool vec, int grid, cudaStream_t s,
                               bool pdl = false);
 cudaError_t launch_round(int dtype, const float *src, void *dst, uint64_t n, int grid,

@@ -310,7 +310,8 @@ KERNEL_SOURCES = {
     "one_shot_ll_cluster": ["ar_ll_cluster.cu"],
     "one_shot_hb": ["ar_hb.cu"],
     "two_shot_hb_tma": ["ar_tma.cu"],
-    "two_shot_hb_direct": [("ar_hb.cu", ["k_reduce", "reduce_dt", "launch_reduce"])],
+    "two_shot_hb_direct": [("ar_hb.cu", ["reduce_body", "k_reduce", "k_reduce_o4", "reduce_dt",
+                                         "launch_reduce"])],
     "combine": ["ar_combine.cu"],
     # a plan's traffic follows its compiled tasks: the compiler counts too
     "plan_": [("ar_plan.cu", ["k_plan", "compile_plan", "builtin_plan", "ar_plan_execute"])],

@@ -142,8 +142,8 @@ enum ar_ll_transport {
  *                         faster at that size; before it, and above the
  *                         largest tuned size, a fixed rule from GB300
  *                         measurements: with T = 2 * R * n * elem_size bytes
- *                         moved per call, TMA when R >= 8 and 16 MiB <= T <=
- *                         64 MiB, or R >= 32 and 256 KiB <= T <= 64 MiB;
+ *                         moved per call, TMA when R >= 16 and 16 MiB <= T
+ *                         <= 64 MiB, or R >= 32 and 256 KiB <= T <= 64 MiB;
  *                         DIRECT otherwise (including every large message:
  *                         its many CTAs keep more loads in flight).
  * Both are the reduce-scatter + all-gather schedule fused per unit (each

@@ -125,14 +125,14 @@ def test_auto_in_a_captured_graph():
 @pytest.mark.parametrize("R", [2, 4, 8, 16, 32])
 def test_untuned_staging_rule(R):
     """Before ar_tune, two-shot HB stages with TMA only in the band where it
-    measured faster (R >= 8 and 16-64 MiB moved per call, or R >= 32 and
+    measured faster (R >= 16 and 16-64 MiB moved per call, or R >= 32 and
     256 KiB-64 MiB), directly elsewhere; a fixed setting overrides it."""
     need_gpu()
     MiB = 1 << 20
     with ar.Handle(R, 64 << 20, "bf16") as h:
         for nbytes in [1024, 4096, 65536, 1 << 20, 2 << 20, 4 << 20, 8 << 20, 32 << 20, 64 << 20]:
             T = 2 * R * nbytes
-            band = (R >= 8 and 16 * MiB <= T <= 64 * MiB) or (R >= 32 and 256 * 1024 <= T <= 64 * MiB)
+            band = (R >= 16 and 16 * MiB <= T <= 64 * MiB) or (R >= 32 and 256 * 1024 <= T <= 64 * MiB)
             want = ar.AR_HB_STAGING_TMA if band else ar.AR_HB_STAGING_DIRECT
             assert ar.ar_get_hb_staging(h.h, nbytes) == want, (R, nbytes)
         for fixed in (ar.AR_HB_STAGING_TMA, ar.AR_HB_STAGING_DIRECT):
