@@ -287,9 +287,10 @@ def staged_path(r, path: str) -> str:
     """The kernel family of a case's path: two-shot HB is named with the
     staging its calls use (its buffers are all 16-byte aligned here)."""
     import all_reduce_reduction_gb300 as ar
+    from all_reduce_reduction_gb300 import workload as wl
     if path != "two_shot_hb":
         return path
-    st = ar.ar_get_hb_staging(r.h.h, r.w.n * {"bf16": 2, "fp16": 2, "fp32": 4}[r.w.dtype])
+    st = ar.ar_get_hb_staging(r.h.h, r.w.n * wl.ELEM_SIZE[r.w.dtype])
     return "two_shot_hb_tma" if st == ar.AR_HB_STAGING_TMA else "two_shot_hb_direct"
 
 
