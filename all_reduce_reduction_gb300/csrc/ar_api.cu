@@ -22,9 +22,14 @@ constexpr int kTuneMaxLog2 = 23;
 // sizes): TMA staging where it measured faster on GB300, direct staging
 // elsewhere.  T = bytes moved per call, 2 R n elem_size.
 static bool tma_band(int R, uint64_t T) {
-    const uint64_t MiB = (uint64_t)1 << 20;
-    return (R >= 16 && T >= 16 * MiB && T <= 64 * MiB) ||
-           (R >= 32 && T >= 256 * 1024 && T <= 64 * MiB);
+    const uint64_t KiB = 1024, MiB = KiB * KiB;
+    if (R >= 32)
+        return T >= 64 * KiB && T <= 128 * MiB;
+    if (R >= 16)
+        return (T >= 128 * KiB && T <= MiB) || (T >= 16 * MiB && T <= 64 * MiB);
+    if (R >= 8)
+        return T >= 16 * MiB && T <= 64 * MiB;
+    return false;
 }
 
 struct ar_handle {
@@ -301,11 +306,11 @@ int bucket_of(uint64_t bytes) {
 
 // Resolve AR_ALGO_AUTO / AR_PROTO_AUTO for a message of `bytes` per rank:
 // the fastest tuned (algo, proto) allowed by the fixed half of the request,
-// or, before ar_tune, a fixed rule from GB300 measurements: one-shot HB up to
-// max(64 KiB, 512 KiB / R) per rank, two-shot HB above (the one-shot's fold
-// work grows with R^2; against the two-shot with its AUTO staging the
-// measured crossovers are about 64 KiB at R = 8, 16 and 32 and 256-512 KiB
-// at R = 4); with LL forced, one-shot up to 2 MiB.
+// or, before ar_tune, a fixed rule from GB300 measurements: HB, one-shot for
+// 5 <= R < 16 up to 64 KiB per rank and for R <= 2 from 8 MiB per rank,
+// two-shot otherwise (against the two-shot with its AUTO staging the
+// one-shot, whose fold work grows with R^2, wins only there); with LL
+// forced, one-shot up to 2 MiB.
 void resolve(const ar_handle *h, uint64_t bytes, int *algo, int *proto) {
     const bool ll_ok = h->slots != nullptr;
     if (h->tuned_max >= 0) {
@@ -336,12 +341,14 @@ void resolve(const ar_handle *h, uint64_t bytes, int *algo, int *proto) {
     if (*proto == AR_PROTO_AUTO)
         *proto = AR_HB;
     if (*algo == AR_ALGO_AUTO) {
-        uint64_t limit = (512u << 10) / (uint64_t)h->R;
-        if (limit < (64u << 10))
-            limit = 64u << 10;
+        bool one;
         if (*proto == AR_LL)
-            limit = 2u << 20;
-        *algo = bytes <= limit ? AR_ONE_SHOT : AR_TWO_SHOT;
+            one = bytes <= (2u << 20);
+        else if (h->R <= 2)
+            one = bytes >= (8u << 20);
+        else
+            one = h->R >= 5 && h->R < 16 && bytes <= (64u << 10);
+        *algo = one ? AR_ONE_SHOT : AR_TWO_SHOT;
     }
 }
 

@@ -12,23 +12,20 @@
 //   producer (warp 0, one thread): R bulk copies global -> shared of the
 //     item's tile of every input into one pipeline stage, completing on the
 //     stage's "full" mbarrier (expect_tx = R * len);
-//   consumers (8 warps): fold the R staged tiles in rank order (binary32),
-//     round, write the reduced tile to one of four shared output tiles, and
-//     release the input stage ("empty" mbarrier); for R = 8, 16 and 32 the
-//     fold is instantiated with R fixed, fully unrolled, its shared-memory
-//     reads issued eight at a time;
-//   one consumer thread: R bulk copies shared -> global of the reduced tile,
-//     one per output (the all-gather step fed from shared memory, so the
-//     reduced shard is never re-read from HBM).
-// One named barrier among the consumers per item, after the fold: the four
-// output tiles give the bulk stores of an item three items' time to read
-// their tile before it is written again.
-// No multicast.  Minimal traffic: R reads + R writes of every byte.
+//   consumers (8 warps): each thread folds its 16-byte vectors of the R
+//     staged tiles in rank order (binary32), rounds, and stores the result
+//     straight from registers to all R outputs (the all-gather step, fed
+//     without re-reading the reduced shard); each warp then releases the
+//     stage ("empty" mbarrier: one arrival per consumer warp).  For R = 8,
+//     16 and 32 the fold is instantiated with R fixed, fully unrolled, its
+//     shared-memory reads issued eight at a time.
+// The consumer warps never wait for one another: no named barrier.  No
+// multicast.  Minimal traffic: R reads + R writes of every byte.
 //
 // Every wait is bounded by the handle's timeout; a timed-out wait records
-// AR_ERR_TIMEOUT and raises a shared abort flag that all consumer threads
-// read at the same named barrier, so they leave together.  Before the CTA
-// exits, bulk copies still in flight are waited for.
+// AR_ERR_TIMEOUT and raises a shared abort flag that every other waiter of
+// the CTA reads, so all of them give up.  Before the CTA exits, bulk loads
+// still in flight are waited for.
 #include "ar_device.cuh"
 
 namespace ar {
@@ -62,47 +59,14 @@ __device__ __forceinline__ void bulk_g2s(uint32_t dst, const void *src, uint32_t
         "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
         :: "r"(dst), "l"(src), "r"(bytes), "r"(bar) : "memory");
 }
-__device__ __forceinline__ void bulk_s2g(void *dst, uint32_t src, uint32_t bytes) {
-    asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;"
-                 :: "l"(dst), "r"(src), "r"(bytes) : "memory");
-}
-__device__ __forceinline__ void bulk_commit() {
-    asm volatile("cp.async.bulk.commit_group;" ::: "memory");
-}
-template <int N> __device__ __forceinline__ void bulk_wait_read() {
-    asm volatile("cp.async.bulk.wait_group.read %0;" :: "n"(N) : "memory");
-}
-__device__ __forceinline__ void bulk_wait_all() {
-    asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
-}
-__device__ __forceinline__ void fence_async_shared() {
-    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-}
 __device__ __forceinline__ void fence_mbar_init() {
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
 }
-// Threads that take part in the consumers' named barrier: every thread of
-// the consumer warps, and no other (the producer warp never joins it).  A
-// count that differed from the threads arriving would never complete.
+// The consumer warps: every thread of the block but the producer warp.  The
+// stages' "empty" barriers count one arrival per consumer warp.
 constexpr int kConsumerThreads = 32 * kTmaConsumerWarps;
 static_assert(kTmaThreads == 32 + kConsumerThreads,
               "the block is one producer warp plus the consumer warps");
-static_assert(kConsumerThreads % 32 == 0 && kConsumerThreads <= 1024 - 32,
-              "a named barrier counts whole warps");
-
-// Barrier 1 among the consumer warps, returning the OR of every consumer's
-// `v`: one uniform decision, whatever each thread saw on its own.
-// Non-aligned form: the warps may arrive diverged.
-__device__ __forceinline__ bool consumer_sync_or(bool v) {
-    uint32_t r;
-    asm volatile(
-        "{\n\t.reg .pred p, q;\n\t"
-        "setp.ne.u32 q, %1, 0;\n\t"
-        "barrier.red.or.pred p, 1, %2, q;\n\t"
-        "selp.u32 %0, 1, 0, p;\n\t}"
-        : "=r"(r) : "r"((uint32_t)v), "n"(kConsumerThreads) : "memory");
-    return r != 0;
-}
 
 // Bounded wait on an mbarrier phase.  Gives up when *abort is raised or the
 // limit passes (then records AR_ERR_TIMEOUT and raises *abort).
@@ -140,14 +104,6 @@ __device__ __forceinline__ bool item_range(const TmaArgs &a, uint64_t i, uint64_
     return true;
 }
 
-// Output tiles: the reduced tile of item i goes to out tile i % kOutTiles.
-// With four, the bulk stores of an item have three items' time to finish
-// reading their tile before it is written again, so one consumer barrier per
-// item suffices: before it, the elected thread waits until the stores of
-// item i - 3 have read their tile (the tile item i + 1 writes).
-constexpr int kOutTiles = 4;
-static_assert(kOutTiles >= 2, "an item's tile must not be the previous item's");
-
 template <int DT, int RC>
 __global__ void __launch_bounds__(kTmaThreads, 1) k_two_shot_tma(const __grid_constant__ TmaArgs a) {
     extern __shared__ __align__(128) uint8_t smem[];
@@ -157,8 +113,7 @@ __global__ void __launch_bounds__(kTmaThreads, 1) k_two_shot_tma(const __grid_co
     const int R = RC ? RC : a.R;
     const int T = a.tile_bytes, S = a.stages;
     uint8_t *in_tiles = smem;                                   // [S][R][T]
-    uint8_t *out_tiles = smem + (size_t)S * R * T;              // [kOutTiles][T]
-    uint64_t *bars = reinterpret_cast<uint64_t *>(out_tiles + kOutTiles * (size_t)T);
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + (size_t)S * R * T);
     const uint32_t full0 = smem_u32(bars), empty0 = smem_u32(bars + S);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const uint64_t items = a.tiles_per_shard * (uint64_t)R;
@@ -212,53 +167,45 @@ __global__ void __launch_bounds__(kTmaThreads, 1) k_two_shot_tma(const __grid_co
             const int stage = (int)(done % S);
             const uint32_t parity = (uint32_t)((done / S) & 1u);
             const bool ok = mbar_wait(full0 + 8 * stage, parity, a.c, abortp);
-            uint8_t *otile = out_tiles + (size_t)(done % kOutTiles) * T;
-            if (ok) {
-                const uint8_t *tile = in_tiles + (size_t)stage * R * T;
-                for (uint32_t p = (uint32_t)ct * 16u; p < len; p += 16u * kConsumerThreads) {
-                    VecAcc<DT> acc;
-                    acc.init(*reinterpret_cast<const uint4 *>(tile + p));
-                    if constexpr (RC > 0) {
+            // leave as a whole warp (a lane that gave up and a lane that saw
+            // the stage land must not part ways: both pass the same
+            // __syncwarp calls)
+            if (__any_sync(0xffffffffu, !ok))
+                break;
+            const uint8_t *tile = in_tiles + (size_t)stage * R * T;
+            for (uint32_t p = (uint32_t)ct * 16u; p < len; p += 16u * kConsumerThreads) {
+                VecAcc<DT> acc;
+                acc.init(*reinterpret_cast<const uint4 *>(tile + p));
+                if constexpr (RC > 0) {
 #pragma unroll
-                        for (int k0 = 1; k0 < RC; k0 += 8) {
-                            uint4 x[8];
+                    for (int k0 = 1; k0 < RC; k0 += 8) {
+                        uint4 x[8];
 #pragma unroll
-                            for (int j = 0; j < 8; ++j)
-                                if (k0 + j < RC)
-                                    x[j] = *reinterpret_cast<const uint4 *>(tile + (size_t)(k0 + j) * T + p);
+                        for (int j = 0; j < 8; ++j)
+                            if (k0 + j < RC)
+                                x[j] = *reinterpret_cast<const uint4 *>(tile + (size_t)(k0 + j) * T + p);
 #pragma unroll
-                            for (int j = 0; j < 8; ++j)
-                                if (k0 + j < RC)
-                                    acc.add(x[j]);
-                        }
-                    } else {
-#pragma unroll 4
-                        for (int k = 1; k < R; ++k)
-                            acc.add(*reinterpret_cast<const uint4 *>(tile + (size_t)k * T + p));
+                        for (int j = 0; j < 8; ++j)
+                            if (k0 + j < RC)
+                                acc.add(x[j]);
                     }
-                    *reinterpret_cast<uint4 *>(otile + p) = acc.result();
+                } else {
+#pragma unroll 4
+                    for (int k = 1; k < R; ++k)
+                        acc.add(*reinterpret_cast<const uint4 *>(tile + (size_t)k * T + p));
                 }
+                const uint4 y = acc.result();
+                for (int r = 0; r < R; ++r)
+                    st_v4(static_cast<uint8_t *>(a.p.out[r]) + off + p, y);
             }
             __syncwarp();
             if (lane == 0)
                 mbar_arrive(empty0 + 8 * stage);
-            fence_async_shared();
-            if (elected)
-                bulk_wait_read<kOutTiles - 2>();   // item done - 3 has read its tile
-            if (consumer_sync_or(!ok || *abortp))
-                break;                             // every consumer leaves at the same item
-            if (elected) {
-                const uint32_t src = smem_u32(otile);
-                for (int r = 0; r < R; ++r)
-                    bulk_s2g(static_cast<uint8_t *>(a.p.out[r]) + off, src, len);
-                bulk_commit();
-            }
             ++done;
         }
-        if (elected) {
-            bulk_wait_all();
+        if (elected)
             consumed_items = done;
-        }
+        __syncwarp();
 
         // Ragged tail (< 16 bytes per rank): block 0, one thread per element,
         // every input read before the outputs are written.
@@ -294,8 +241,7 @@ __global__ void __launch_bounds__(kTmaThreads, 1) k_two_shot_tma(const __grid_co
 }
 
 size_t tma_smem_bytes(int R, int tile_bytes, int stages) {
-    return (size_t)stages * R * tile_bytes + kOutTiles * (size_t)tile_bytes +
-           2 * sizeof(uint64_t) * stages;
+    return (size_t)stages * R * tile_bytes + 2 * sizeof(uint64_t) * stages;
 }
 
 // R fixed at compile time for the rank counts of the workloads (fold fully

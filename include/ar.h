@@ -131,9 +131,10 @@ enum ar_ll_transport {
 /* How two-shot HB calls move their data when every buffer is 16-byte aligned
  * (other buffers always take the direct form, element by element).
  *   AR_HB_STAGING_TMA:    bulk copies (the Tensor Memory Accelerator) bring
- *                         tiles of the R inputs into shared memory, the tile
- *                         is folded once and bulk-stored to the R outputs;
- *                         one CTA per SM.  Best for large messages.
+ *                         tiles of the R inputs into shared memory; each
+ *                         thread folds its vectors of the tile once and
+ *                         stores them to the R outputs; one CTA per SM.
+ *                         Best for mid-sized messages at larger R.
  *   AR_HB_STAGING_DIRECT: one thread per 16-byte vector loads the R inputs
  *                         into registers, folds them once and stores R copies;
  *                         as many CTAs as the message needs.  Lower latency
@@ -142,10 +143,12 @@ enum ar_ll_transport {
  *                         faster at that size; before it, and above the
  *                         largest tuned size, a fixed rule from GB300
  *                         measurements: with T = 2 * R * n * elem_size bytes
- *                         moved per call, TMA when R >= 16 and 16 MiB <= T
- *                         <= 64 MiB, or R >= 32 and 256 KiB <= T <= 64 MiB;
- *                         DIRECT otherwise (including every large message:
- *                         its many CTAs keep more loads in flight).
+ *                         moved per call, TMA for R >= 32 and 64 KiB <= T <=
+ *                         128 MiB; for 16 <= R < 32 and T in [128 KiB, 1 MiB]
+ *                         or [16 MiB, 64 MiB]; for 8 <= R < 16 and T in
+ *                         [16 MiB, 64 MiB]; DIRECT otherwise (including every
+ *                         large message: its many CTAs keep more loads in
+ *                         flight).
  * Both are the reduce-scatter + all-gather schedule fused per unit (each
  * unit reduced once, by its shard's owner, and replicated) and give
  * identical results.  Source: the SGLang guide, section 4.4 (each algorithm
@@ -244,9 +247,9 @@ int ar_allreduce(ar_handle_t h, const void *const in[], void *const out[],
  * ceil(n/R) rounded up to a 16-byte vector).  Buffers need n elements.
  * With AR_ALGO_AUTO and/or AR_PROTO_AUTO the library picks the half left
  * open, per message size: the tuned fastest choice after ar_tune, else a
- * fixed rule from GB300 measurements (HB; one-shot up to max(64 KiB,
- * 512 KiB / R) per rank, two-shot above; with AR_LL forced, one-shot up to
- * 2 MiB).
+ * fixed rule from GB300 measurements (HB; one-shot for 5 <= R < 16 up to
+ * 64 KiB per rank and for R <= 2 from 8 MiB per rank, two-shot otherwise;
+ * with AR_LL forced, one-shot up to 2 MiB).
  * Errors: as ar_allreduce; AR_ERR_INVALID also for n == 0 or n > N. */
 int ar_allreduce_n(ar_handle_t h, const void *const in[], void *const out[], size_t n,
                    int algo, int proto, cudaStream_t stream);

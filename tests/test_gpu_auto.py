@@ -53,87 +53,44 @@ def test_n_out_of_range_rejected():
             ar.ar_allreduce_n(h.h, x, y, 10, 7, ar.AR_HB)
 
 
-@pytest.mark.parametrize("R", [4, 8, 16, 32])
+@pytest.mark.parametrize("R", [2, 4, 8, 16, 32])
 def test_untuned_rule(R):
-    """Before ar_tune: HB, one-shot up to max(64 KiB, 512 KiB / R) per rank,
-    two-shot above."""
+    """Before ar_tune: HB; one-shot for 5 <= R < 16 up to 64 KiB per rank and
+    for R <= 2 from 8 MiB per rank, two-shot otherwise."""
     need_gpu()
-    limit = max(64 << 10, (512 << 10) // R)
-    with ar.Handle(R, 1 << 21, "bf16") as h:
-        assert ar.ar_get_tuning(h.h, 4096)[:2] == (ar.AR_ONE_SHOT, ar.AR_HB)
-        assert ar.ar_get_tuning(h.h, limit)[:2] == (ar.AR_ONE_SHOT, ar.AR_HB)
-        assert ar.ar_get_tuning(h.h, limit + 2)[:2] == (ar.AR_TWO_SHOT, ar.AR_HB)
+    with ar.Handle(R, 1 << 23, "bf16") as h:
+        for nbytes in (512, 4096, 64 << 10, (64 << 10) + 2, 1 << 20, 8 << 20, 16 << 20):
+            if R <= 2:
+                one = nbytes >= 8 << 20
+            else:
+                one = 5 <= R < 16 and nbytes <= 64 << 10
+            want = (ar.AR_ONE_SHOT if one else ar.AR_TWO_SHOT, ar.AR_HB)
+            assert ar.ar_get_tuning(h.h, nbytes)[:2] == want, (R, nbytes)
         assert ar.ar_get_tuning(h.h, 4 << 20)[2] == [0.0, 0.0, 0.0, 0.0]
-
-
-@pytest.mark.parametrize("R,dtype", [(8, "bf16"), (4, "fp32"), (16, "fp16")])
-def test_tune_picks_fastest_and_stays_exact(R, dtype):
-    need_gpu()
-    N = (1 << 21) + 1
-    cpu = wl.make_inputs(71, R, N, dtype, "normal")
-    with ar.Handle(R, N, dtype) as h:
-        ar.ar_tune(h.h)
-        esz = wl.ELEM_SIZE[dtype]
-        # every tuned bucket: the AUTO choice is the fastest timed pair
-        for lg in range(9, 24):
-            a, p, us = ar.ar_get_tuning(h.h, 1 << lg)
-            assert all(u > 0 for u in us), (lg, us)
-            k = int(np.argmin(us))
-            assert (a, p) == (k // 2, k % 2), (lg, us)
-        # sizes round up to the next power of two
-        assert ar.ar_get_tuning(h.h, 513)[2] == ar.ar_get_tuning(h.h, 1024)[2]
-        assert ar.ar_get_tuning(h.h, 1)[2] == ar.ar_get_tuning(h.h, 512)[2]
-        # above the largest tuned size the largest tuned bucket's choice holds
-        assert ar.ar_get_tuning(h.h, 1 << 26)[:2] == ar.ar_get_tuning(h.h, 1 << 23)[:2]
-        for n in (3, 1000, 70001, (1 << 20) // esz * 2 + 5, N):
-            for choice in CHOICES[:5]:
-                _prefix_case(h.h, R, N, n, dtype, *choice, cpu)
-
-
-def test_auto_in_a_captured_graph():
-    need_gpu()
-    R, N = 8, 1 << 18
-    h = ar.Handle(R, N, "bf16")
-    ar.ar_tune(h.h)
-    ins = [torch.empty(N, dtype=torch.bfloat16, device="cuda") for _ in range(R)]
-    outs = [torch.empty_like(t) for t in ins]
-    s = torch.cuda.Stream()
-    with torch.cuda.stream(s):
-        for t in ins:
-            t.zero_()
-        for n in (512, 8192, N):
-            ar.ar_allreduce_n(h.h, ins, outs, n, stream=s)
-    s.synchronize()
-    g = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(g, stream=s):
-        for n in (512, 8192, N):
-            for _ in range(3):
-                ar.ar_allreduce_n(h.h, ins, outs, n, stream=s)
-    for rep in range(2):
-        cpu = wl.make_inputs(72 + rep, R, N, "bf16", "uniform")
-        for t, c in zip(ins, cpu):
-            t.copy_(c)
-        g.replay()
-        torch.cuda.synchronize()
-        assert ar.ar_status(h.h) == ar.AR_OK
-        want = expected(cpu, "bf16")
-        for r in range(R):
-            assert_bits_equal(outs[r], want, "bf16", "replay %d rank %d" % (rep, r))
-    h.close()
 
 
 @pytest.mark.parametrize("R", [2, 4, 8, 16, 32])
 def test_untuned_staging_rule(R):
-    """Before ar_tune, two-shot HB stages with TMA only in the band where it
-    measured faster (R >= 16 and 16-64 MiB moved per call, or R >= 32 and
-    256 KiB-64 MiB), directly elsewhere; a fixed setting overrides it."""
+    """Before ar_tune, two-shot HB stages with TMA only in the bands where it
+    measured faster (by bytes moved per call, T = 2 R n elem_size: R >= 32 and
+    64 KiB-128 MiB; 16 <= R < 32 and 128 KiB-1 MiB or 16-64 MiB; 8 <= R < 16
+    and 16-64 MiB), directly elsewhere; a fixed setting overrides it."""
     need_gpu()
-    MiB = 1 << 20
+    KiB, MiB = 1 << 10, 1 << 20
+
+    def band(R, T):
+        if R >= 32:
+            return 64 * KiB <= T <= 128 * MiB
+        if R >= 16:
+            return 128 * KiB <= T <= MiB or 16 * MiB <= T <= 64 * MiB
+        if R >= 8:
+            return 16 * MiB <= T <= 64 * MiB
+        return False
     with ar.Handle(R, 64 << 20, "bf16") as h:
-        for nbytes in [1024, 4096, 65536, 1 << 20, 2 << 20, 4 << 20, 8 << 20, 32 << 20, 64 << 20]:
+        for nbytes in [1024, 4096, 16384, 65536, 1 << 20, 2 << 20, 4 << 20, 8 << 20, 32 << 20,
+                       64 << 20]:
             T = 2 * R * nbytes
-            band = (R >= 16 and 16 * MiB <= T <= 64 * MiB) or (R >= 32 and 256 * 1024 <= T <= 64 * MiB)
-            want = ar.AR_HB_STAGING_TMA if band else ar.AR_HB_STAGING_DIRECT
+            want = ar.AR_HB_STAGING_TMA if band(R, T) else ar.AR_HB_STAGING_DIRECT
             assert ar.ar_get_hb_staging(h.h, nbytes) == want, (R, nbytes)
         for fixed in (ar.AR_HB_STAGING_TMA, ar.AR_HB_STAGING_DIRECT):
             ar.ar_set_hb_staging(h.h, fixed)
