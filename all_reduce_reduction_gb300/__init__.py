@@ -304,8 +304,8 @@ def ar_allreduce_ll_static(R: int, N: int, dtype, ins, outs, stream=None) -> Non
     hook that cannot pay for cudaMalloc's device-wide synchronisation.  The
     packet scratch is a static array inside the library (at most
     AR_NOALLOC_SCRATCH_BYTES of packets, else AR_ERR_UNSUPPORTED); the first
-    call on a device sets it up and must precede any stream capture; calls
-    that overlap on the GPU race on the shared array."""
+    call on a device sets it up and waits for that to finish; calls that
+    overlap on the GPU race on the shared array."""
     dt = DTYPES[dtype] if isinstance(dtype, str) else dtype
     _check(load_library().ar_allreduce_ll_static(R, N, dt, _ptr_array(ins), _ptr_array(outs),
                                                  _stream(stream)), "ar_allreduce_ll_static")

@@ -503,8 +503,8 @@ int ar_plan_destroy(ar_plan_t p);
  * and nothing is enqueued.  It calls no cudaMalloc/cudaFree and no
  * allocating library routine.
  * The first call on each device sets the array up (resolves its device
- * address, zeroes its control words and waits for that): make that first
- * call, with the device current, before any stream capture.
+ * address, zeroes its control words and waits for that to finish, so that
+ * call synchronises the device); make it with that device current.
  * All calls share the one array and it keeps the last call's contents, so
  * calls whose kernels overlap on the GPU race: order them on one stream (or
  * with events).  Device-side wait limits are fixed at one second and a
