@@ -51,13 +51,18 @@ def run_graph(w, algo, proto, cpu, calls=10, warm=2, transport=ar.AR_LL_AUTO,
     return outs
 
 
-@pytest.mark.parametrize("transport", [ar.AR_LL_AUTO, ar.AR_LL_GLOBAL], ids=["auto", "global"])
-@pytest.mark.parametrize("path", ALL_PATHS, ids=PATH_IDS)
+# every path with the default LL transport, and the LL paths again with the
+# HBM-slot transport forced (the transport setting applies to LL only)
+SWEEP_CASES = ([(p, ar.AR_LL_AUTO, i + "-auto") for p, i in zip(ALL_PATHS, PATH_IDS)]
+               + [(p, ar.AR_LL_GLOBAL, i + "-global") for p, i in zip(ALL_PATHS, PATH_IDS)
+                  if p[1] == ar.AR_LL])
+
+
+@pytest.mark.parametrize("path,transport", [c[:2] for c in SWEEP_CASES],
+                         ids=[c[2] for c in SWEEP_CASES])
 def test_ll_sweep_sizes(path, transport):
     """R=8 bf16, N = 2^9..2^18, uniform [-1, 1), 10 calls per graph."""
     need_gpu()
-    if transport != ar.AR_LL_AUTO and path[1] != ar.AR_LL:
-        pytest.skip("transport applies to LL only")
     for w in wl.LL_SWEEP:
         cpu = w.inputs()
         want = oracle_single_output(cpu, w.dtype)
