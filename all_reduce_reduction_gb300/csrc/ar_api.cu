@@ -224,12 +224,23 @@ int two_shot_hb(ar_handle *h, const Call &c) {
     }
     // direct staging, or unaligned buffers: one thread per 16-byte vector (or
     // per element) folds the R inputs once and stores R copies; up to 64 MiB
-    // moved per call the vector form runs held to four CTAs per SM
+    // moved per call the vector form runs held to four CTAs per SM; above
+    // that, binary32 vectors run in kWideThreads-thread CTAs (768 threads per
+    // SM, as the 16-bit forms) when that grid fills its cap, the same thread
+    // count as the 256-thread grid's (a partly filled last wave of the wider
+    // CTAs measured slower)
     const HbArgs a = hb_args(h, c);
     const uint64_t units = c.vec16 ? c.n / (16 / h->esz) : c.n;
-    const int grid = clamp_grid(ceil_div(units, kRegThreads), h->reg_cap);
     const bool occupancy4 = 2 * (uint64_t)h->R * c.n * h->esz <= ((uint64_t)64 << 20);
-    return from_cuda(launch_reduce(a, h->dtype, c.vec16, false, grid, c.s, h->pdl, occupancy4));
+    if (c.vec16 && !occupancy4 && h->dtype == AR_FP32) {
+        const int wide_cap = h->reg_cap * kRegThreads / kWideThreads;
+        if (wide_cap > 0 && ceil_div(units, kWideThreads) >= (uint64_t)wide_cap)
+            return from_cuda(launch_reduce(a, h->dtype, true, false, wide_cap, c.s, h->pdl,
+                                           kReduceWide));
+    }
+    const int grid = clamp_grid(ceil_div(units, kRegThreads), h->reg_cap);
+    return from_cuda(launch_reduce(a, h->dtype, c.vec16, false, grid, c.s, h->pdl,
+                                   occupancy4 ? kReduceOcc4 : kReducePlain));
 }
 
 // One-shot LL through thread-block clusters (R peers per cluster exchange

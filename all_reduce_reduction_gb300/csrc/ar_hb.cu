@@ -270,6 +270,15 @@ __global__ void __launch_bounds__(kRegThreads, 4) k_reduce_o4(const __grid_const
     reduce_body<DT, true, false>(a);
 }
 
+// The fused form in kWideThreads-thread CTAs, for binary32.  Its fold needs
+// fewer registers than the 16-bit ones (no widening), so four 256-thread CTAs
+// fit on an SM (1024 threads); two of these fit (768 threads, as three
+// 256-thread CTAs of the 16-bit forms), which streams large messages faster.
+template <int DT>
+__global__ void __launch_bounds__(kWideThreads) k_reduce_wide(const __grid_constant__ HbArgs a) {
+    reduce_body<DT, true, false>(a);
+}
+
 // ---------------------------------------------------------------------------
 // All-gather: every unit of shard j is read once from out[j] and stored to
 // the R - 1 other outputs (a copy: bits unchanged).
@@ -394,11 +403,17 @@ cudaError_t launch_one_shot_hb(const HbArgs &a, int dtype, bool vec, bool single
 }
 
 template <int DT>
-static cudaError_t reduce_dt(const HbArgs &a, bool vec, bool scatter, bool occupancy4, int grid,
+static cudaError_t reduce_dt(const HbArgs &a, bool vec, bool scatter, int form, int grid,
                              cudaStream_t s, bool pdl) {
     if (vec && scatter)
         return launch_kernel(k_reduce<DT, true, true>, grid, kRegThreads, 0, s, pdl, a);
-    if (vec && occupancy4)
+    if (vec && form == kReduceWide) {
+        if constexpr (DT == AR_FP32)
+            return launch_kernel(k_reduce_wide<DT>, grid, kWideThreads, 0, s, pdl, a);
+        else
+            return cudaErrorInvalidValue;
+    }
+    if (vec && form == kReduceOcc4)
         return launch_kernel(k_reduce_o4<DT>, grid, kRegThreads, 0, s, pdl, a);
     if (vec)
         return launch_kernel(k_reduce<DT, true, false>, grid, kRegThreads, 0, s, pdl, a);
@@ -408,11 +423,11 @@ static cudaError_t reduce_dt(const HbArgs &a, bool vec, bool scatter, bool occup
 }
 
 cudaError_t launch_reduce(const HbArgs &a, int dtype, bool vec, bool scatter_only, int grid,
-                          cudaStream_t s, bool pdl, bool occupancy4) {
+                          cudaStream_t s, bool pdl, int form) {
     switch (dtype) {
-    case AR_BF16: return reduce_dt<AR_BF16>(a, vec, scatter_only, occupancy4, grid, s, pdl);
-    case AR_FP16: return reduce_dt<AR_FP16>(a, vec, scatter_only, occupancy4, grid, s, pdl);
-    default: return reduce_dt<AR_FP32>(a, vec, scatter_only, occupancy4, grid, s, pdl);
+    case AR_BF16: return reduce_dt<AR_BF16>(a, vec, scatter_only, form, grid, s, pdl);
+    case AR_FP16: return reduce_dt<AR_FP16>(a, vec, scatter_only, form, grid, s, pdl);
+    default: return reduce_dt<AR_FP32>(a, vec, scatter_only, form, grid, s, pdl);
     }
 }
 

@@ -20,6 +20,8 @@ constexpr int kEpochWords = 2048;
 
 // Threads per CTA of the register (non-TMA) kernels and the LL kernels.
 constexpr int kRegThreads = 256;
+// Threads per CTA of the fused two-shot's wide form (binary32, large calls).
+constexpr int kWideThreads = 384;
 constexpr int kLlThreads = 128;
 constexpr int kLlStagedThreads = 256;   // one-shot LL with shared receive staging
 
@@ -171,9 +173,12 @@ cudaError_t one_shot_prepare();                 // opt in to the one-shot ring's
 // `single`: the grid covers the message, every CTA has at most one run
 cudaError_t launch_one_shot_hb(const HbArgs &a, int dtype, bool vec, bool single, int grid,
                                int block, cudaStream_t s, bool pdl = false);
-// occupancy4: the fused form held to four CTAs per SM (vectors only)
+// Launch forms of the fused two-shot (vectors, not scatter_only): 256-thread
+// CTAs as the registers allow, 256-thread CTAs held to four per SM, or
+// kWideThreads-thread CTAs (binary32 only; `grid` then counts those).
+enum ReduceForm { kReducePlain = 0, kReduceOcc4 = 1, kReduceWide = 2 };
 cudaError_t launch_reduce(const HbArgs &a, int dtype, bool vec, bool scatter_only, int grid,
-                          cudaStream_t s, bool pdl = false, bool occupancy4 = false);
+                          cudaStream_t s, bool pdl = false, int form = kReducePlain);
 cudaError_t launch_all_gather(const HbArgs &a, int dtype, bool vec, int grid, cudaStream_t s,
                               bool pdl = false);
 cudaError_t launch_round(int dtype, const float *src, void *dst, uint64_t n, int grid,

@@ -309,10 +309,11 @@ KERNEL_SOURCES = {
     "one_shot_ll_global": [("ar_ll.cu", ["k_ll_staged", "launch_ll_staged"])],
     "two_shot_ll": [("ar_ll.cu", ["k_ll2_staged", "launch_ll_staged"])],
     "one_shot_ll_cluster": ["ar_ll_cluster.cu"],
-    "one_shot_hb": ["ar_hb.cu"],
+    "one_shot_hb": [("ar_hb.cu", ["k_one_shot_hb", "one_shot_smem", "one_shot_dt",
+                                  "one_shot_prepare_dt", "one_shot_prepare", "launch_one_shot_hb"])],
     "two_shot_hb_tma": ["ar_tma.cu"],
-    "two_shot_hb_direct": [("ar_hb.cu", ["reduce_body", "k_reduce", "k_reduce_o4", "reduce_dt",
-                                         "launch_reduce"])],
+    "two_shot_hb_direct": [("ar_hb.cu", ["reduce_body", "k_reduce", "k_reduce_o4", "k_reduce_wide",
+                                         "reduce_dt", "launch_reduce"])],
     "combine": ["ar_combine.cu"],
     # a plan's traffic follows its compiled tasks: the compiler counts too
     "plan_": [("ar_plan.cu", ["k_plan", "compile_plan", "builtin_plan", "ar_plan_execute"])],

@@ -111,10 +111,10 @@ def test_many_tiles_ragged_tail(path, dtype, R):
                                        (5, (2 << 20) + 1, "fp32")],
                          ids=["r8_bf16", "r16_fp16", "r32_fp32", "r3_bf16", "r5_fp32"])
 def test_two_shot_tma_many_items_per_cta(R, n, dtype):
-    """Two-shot HB with every CTA folding 5 to 14 items, so each of the four
-    shared output tiles is reused while earlier bulk stores may still be
-    reading: R fixed at compile time (8, 16, 32) and a runtime R (3, 5),
-    each with a ragged tail."""
+    """Two-shot HB with every CTA folding 5 to 14 items, so each shared-memory
+    stage is refilled by the producer many times while the consumers fold and
+    store the items before it: R fixed at compile time (8, 16, 32) and a
+    runtime R (3, 5), each with a ragged tail."""
     run_case(R, n, dtype, ar.AR_TWO_SHOT, ar.AR_HB, dist="normal", staging=ar.AR_HB_STAGING_TMA)
     with ar.Handle(R, n, dtype) as h:
         info = ar.ar_get_info(h.h)
@@ -144,6 +144,29 @@ def test_two_shot_hb_stagings_in_place(staging, offset):
     element whatever the setting)."""
     run_case(8, 300001, "bf16", ar.AR_TWO_SHOT, ar.AR_HB, offset=offset, inplace=True,
              staging=staging)
+
+
+def wide_threshold_units():
+    """16-byte vectors per rank from which a binary32 two-shot HB call moving
+    more than 64 MiB runs its direct staging in 384-thread CTAs: the grid of
+    those reaches the thread count of the 256-thread grid (8 CTAs per SM)."""
+    with ar.Handle(1, 1, "fp32") as h:
+        sms = ar.ar_get_info(h.h)["num_sms"]
+    cap = sms * 8 * 256 // 384
+    return (cap - 1) * 384 + 1
+
+
+@pytest.mark.parametrize("R,extra", [(8, -1), (8, 0), (32, 0), (3, None)],
+                         ids=["r8_below", "r8_from", "r32_from", "r3_many_waves"])
+def test_two_shot_direct_fp32_wide_form(R, extra):
+    """binary32, direct staging, more than 64 MiB moved: one vector below the
+    384-thread form's threshold (256-thread CTAs), from it with a ragged tail
+    of 3 elements, and far above it (every thread folding several vectors);
+    the same bits as the oracle."""
+    units = wide_threshold_units() + extra if extra is not None else 2 << 20
+    n = units * 4 + (3 if extra == 0 else 0)
+    assert 2 * R * n * 4 > (64 << 20)
+    run_case(R, n, "fp32", ar.AR_TWO_SHOT, ar.AR_HB, dist="normal", staging=ar.AR_HB_STAGING_DIRECT)
 
 
 @pytest.mark.parametrize("path", ALL_PATHS, ids=PATH_IDS)
