@@ -198,6 +198,43 @@ def test_plan_misaligned_buffers_and_rejections():
 
 
 @pytest.mark.parametrize("algo", ["one_shot", "two_shot"])
+def test_builtin_plan_default_chunks(algo):
+    """With chunks_per_rank 0 a large two-shot message (R >= 8) is cut into a
+    whole number of chunks per CTA, each about 8 KiB of a rank buffer; the
+    one-shot plan keeps one chunk per CTA.  Both stay the oracle's bit for
+    bit (ragged tail included)."""
+    need_gpu()
+    R, n, dtype = 8, (8 << 20) + 3, "bf16"
+    with ar.Handle(R, 1000, dtype) as h:          # one chunk per CTA there: gives the CTA count
+        p = ar.ar_plan_builtin(h.h, algo)
+        tasks, _, _ = ar.ar_plan_stats(p)
+        ar.ar_plan_destroy(p)
+    per_chunk = R if algo == "one_shot" else 1     # tasks per chunk after fusion
+    G = tasks // (R * per_chunk)
+    assert G * R * per_chunk == tasks and G >= 1
+    cpu = wl.make_inputs(87, R, n, dtype, "normal")
+    ins = device_inputs(cpu)
+    outs = _outs(R, n, dtype)
+    with ar.Handle(R, n, dtype) as h:
+        p = ar.ar_plan_builtin(h.h, algo)
+        tasks, _, _ = ar.ar_plan_stats(p)
+        K = tasks // (R * per_chunk)
+        assert K * R * per_chunk == tasks
+        if algo == "one_shot":
+            assert K == G, (K, G)
+        else:
+            assert K % G == 0 and G < K <= 16 * G, (K, G)
+            chunk_bytes = -(-n // (R * K)) * wl.ELEM_SIZE[dtype]
+            assert 4096 <= chunk_bytes <= 12288, chunk_bytes
+        ar.ar_plan_execute(p, ins, outs)
+        assert ar.ar_status(h.h) == ar.AR_OK
+        ar.ar_plan_destroy(p)
+    want = expected(cpu, dtype)
+    for r in range(R):
+        assert_bits_equal(outs[r], want, dtype, "rank %d" % r)
+
+
+@pytest.mark.parametrize("algo", ["one_shot", "two_shot"])
 def test_builtin_plan_fills_the_gpu_by_default(algo):
     need_gpu()
     R, n, dtype = 8, (1 << 19) + 3, "bf16"
