@@ -118,6 +118,8 @@ SIGNATURES = {
     "ar_set_ll_transport": ([_VP, _I], _I),
     "ar_set_hb_staging": ([_VP, _I], _I),
     "ar_get_hb_staging": ([_VP, _SZ, ctypes.POINTER(_I)], _I),
+    "ar_set_grid_divisor": ([_VP, _I], _I),
+    "ar_get_grid_divisor": ([_VP, _SZ, _I, _I, ctypes.POINTER(_I)], _I),
     "ar_set_pdl": ([_VP, _I], _I),
     "ar_round": ([_I, _VP, _VP, _SZ, _VP], _I),
     "ar_get_info": ([_VP, ctypes.POINTER(ar_info)], _I),
@@ -279,6 +281,22 @@ def ar_get_hb_staging(h: int, nbytes: int) -> int:
     `nbytes` per rank (16-byte-aligned buffers) would use now."""
     out = ctypes.c_int(0)
     _check(load_library().ar_get_hb_staging(h, nbytes, ctypes.byref(out)), "ar_get_hb_staging")
+    return out.value
+
+
+def ar_set_grid_divisor(h: int, divisor: int) -> None:
+    """Force the CTA-cap divisor of later calls (1, 2, 4, 8; 0 = tuned)."""
+    _check(load_library().ar_set_grid_divisor(h, divisor), "ar_set_grid_divisor")
+
+
+def ar_get_grid_divisor(h: int, nbytes: int, algo, proto) -> int:
+    """The CTA-cap divisor a call of `nbytes` per rank with this algo and
+    proto would use now."""
+    algo = ALGOS[algo] if isinstance(algo, str) else algo
+    proto = PROTOS[proto] if isinstance(proto, str) else proto
+    out = ctypes.c_int(0)
+    _check(load_library().ar_get_grid_divisor(h, nbytes, algo, proto, ctypes.byref(out)),
+           "ar_get_grid_divisor")
     return out.value
 
 

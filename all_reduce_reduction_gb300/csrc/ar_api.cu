@@ -18,6 +18,10 @@ constexpr int kMaxBucketLog2 = 28;
 constexpr int kBuckets = kMaxBucketLog2 - kMinBucketLog2 + 1;
 // ar_tune times 15 sizes, 2^9 .. 2^23 bytes per rank (the page's [2^9, 2^24)).
 constexpr int kTuneMaxLog2 = 23;
+// CTA-cap divisors ar_tune times for every path (the launch-shape dimension).
+constexpr int kTuneDiv[] = {1, 2, 4};
+constexpr int kTuneDivs = 3;
+constexpr float kTuneDivMargin = 0.02f;
 // Two-shot HB with AR_HB_STAGING_AUTO before ar_tune (and above the tuned
 // sizes): TMA staging where it measured faster on GB300, direct staging
 // elsewhere.  T = bytes moved per call, 2 R n elem_size.
@@ -59,6 +63,10 @@ struct ar_handle {
     // two-shot HB staging per bucket, timed by ar_tune: enum ar_hb_staging,
     // AR_HB_STAGING_AUTO = not timed
     int tuned_hb2[kBuckets];
+    // divisor of each path's CTA cap per bucket, timed by ar_tune (1: the
+    // full cap); [bucket][algo][proto]
+    int tuned_div[kBuckets][2][2];
+    int grid_div;           // forced divisor (ar_set_grid_divisor), 0 = tuned
     int pdl;                // launch with programmatic dependent launch
     int ll_transport;       // enum ar_ll_transport
     int hb_staging;         // enum ar_hb_staging
@@ -177,17 +185,37 @@ int from_cuda(cudaError_t e) {
 
 // ---- the four all-reduce paths ---------------------------------------------
 
+int bucket_of(uint64_t bytes);
+
+// Divisor of a path's CTA cap for a message of n elements per rank (the
+// launch-shape dimension of the tuner): the handle's forced one, else the one
+// ar_tune timed fastest at the message's size bucket, else 1.  Threads per
+// CTA are fixed per kernel by its launch bounds.
+int grid_div(const ar_handle *h, uint64_t n, int algo, int proto) {
+    if (h->grid_div > 0)
+        return h->grid_div;
+    if (h->tuned_max >= 0) {
+        const int b = bucket_of(n * h->esz);
+        if (b <= h->tuned_max)
+            return h->tuned_div[b][algo][proto];
+    }
+    return 1;
+}
+
+int div_cap(int cap, int div) {
+    const int c = cap / div;
+    return c > 0 ? c : 1;
+}
+
 int one_shot_hb(ar_handle *h, const Call &c) {
     const HbArgs a = hb_args(h, c);
     const uint64_t units = c.vec16 ? c.n / (16 / h->esz) : c.n;
     const uint64_t per_blk = (uint64_t)(h->one_shot_warps / h->R) * 32;
     const uint64_t runs = ceil_div(units, per_blk);
-    const int grid = clamp_grid(runs, h->one_shot_cap);
+    const int grid = clamp_grid(runs, div_cap(h->one_shot_cap, grid_div(h, c.n, AR_ONE_SHOT, AR_HB)));
     return from_cuda(launch_one_shot_hb(a, h->dtype, c.vec16, runs <= (uint64_t)grid, grid,
                                         32 * h->one_shot_warps, c.s, h->pdl));
 }
-
-int bucket_of(uint64_t bytes);
 
 // Staging of a two-shot HB call of n elements per rank whose buffers are all
 // 16-byte aligned: the handle's setting; with AR_HB_STAGING_AUTO the faster
@@ -206,6 +234,7 @@ int hb2_staging(const ar_handle *h, uint64_t n) {
 }
 
 int two_shot_hb(ar_handle *h, const Call &c) {
+    const int div = grid_div(h, c.n, AR_TWO_SHOT, AR_HB);
     const uint64_t body = (c.n * h->esz) / 16 * 16;
     if (c.vec16 && body > 0 && hb2_staging(h, c.n) == AR_HB_STAGING_TMA) {
         TmaArgs a;
@@ -219,7 +248,7 @@ int two_shot_hb(ar_handle *h, const Call &c) {
         a.stages = h->tma_stages;
         a.c = h->ctl;
         const uint64_t items = ceil_div(body, (uint64_t)h->tma_tile) + (uint64_t)h->R;
-        const int grid = clamp_grid(items, h->num_sms);
+        const int grid = clamp_grid(items, div_cap(h->num_sms, div));
         return from_cuda(launch_two_shot_tma(a, h->dtype, grid, c.s, h->pdl));
     }
     // direct staging, or unaligned buffers: one thread per 16-byte vector (or
@@ -235,10 +264,10 @@ int two_shot_hb(ar_handle *h, const Call &c) {
     if (c.vec16 && !occupancy4 && h->dtype == AR_FP32) {
         const int wide_cap = h->reg_cap * kRegThreads / kWideThreads;
         if (wide_cap > 0 && ceil_div(units, kWideThreads) >= (uint64_t)wide_cap)
-            return from_cuda(launch_reduce(a, h->dtype, true, false, wide_cap, c.s, h->pdl,
-                                           kReduceWide));
+            return from_cuda(launch_reduce(a, h->dtype, true, false, div_cap(wide_cap, div), c.s,
+                                           h->pdl, kReduceWide));
     }
-    const int grid = clamp_grid(ceil_div(units, kRegThreads), h->reg_cap);
+    const int grid = clamp_grid(ceil_div(units, kRegThreads), div_cap(h->reg_cap, div));
     return from_cuda(launch_reduce(a, h->dtype, c.vec16, false, grid, c.s, h->pdl,
                                    occupancy4 ? kReduceOcc4 : kReducePlain));
 }
@@ -257,6 +286,7 @@ int ll_cluster(ar_handle *h, const Call &c) {
     int cap = h->cluster_max;
     if (cap > kEpochWords / h->R)
         cap = kEpochWords / h->R;
+    cap = div_cap(cap, grid_div(h, c.n, AR_ONE_SHOT, AR_LL));
     return from_cuda(launch_ll_cluster(a, h->dtype, clamp_grid(nchunks, cap), c.s, h->pdl));
 }
 
@@ -285,6 +315,7 @@ int ll(ar_handle *h, const Call &c, bool two) {
             cap = kEpochWords;
         if (cap < 1)
             return AR_ERR_UNSUPPORTED;
+        cap = div_cap(cap, grid_div(h, c.n, two ? AR_TWO_SHOT : AR_ONE_SHOT, AR_LL));
         a.G = 0;
         const int ctas = clamp_grid(ceil_div(nbytes / 8, ub), cap);
         return from_cuda(launch_ll_staged(a, h->dtype, two, ctas, c.s, h->pdl));
@@ -296,6 +327,7 @@ int ll(ar_handle *h, const Call &c, bool two) {
         gmax = kEpochWords / h->R;
     if (gmax < 1)
         return AR_ERR_UNSUPPORTED;                 // cannot keep R CTAs resident
+    gmax = div_cap(gmax, grid_div(h, c.n, two ? AR_TWO_SHOT : AR_ONE_SHOT, AR_LL));
     a.G = clamp_grid(ceil_div(work, kLlThreads), gmax);
     return from_cuda(launch_ll(a, h->dtype, two, c.s, h->pdl));
 }
@@ -473,10 +505,13 @@ int ar_create(int R, size_t N, int dtype, ar_handle_t *out) {
     h->tuned_max = -1;                       // AUTO uses the fixed rule until ar_tune
     for (int b = 0; b < kBuckets; ++b) {
         for (int a = 0; a < 2; ++a)
-            for (int p = 0; p < 2; ++p)
+            for (int p = 0; p < 2; ++p) {
                 h->tuned_us[b][a][p] = 0.f;
+                h->tuned_div[b][a][p] = 1;
+            }
         h->tuned_hb2[b] = AR_HB_STAGING_AUTO;
     }
+    h->grid_div = 0;
     h->pdl = 1;
     h->ll_transport = AR_LL_AUTO;
     h->hb_staging = AR_HB_STAGING_AUTO;
@@ -701,34 +736,55 @@ int ar_tune(ar_handle_t h, cudaStream_t stream) {
             cudaGraphDestroy(g);
             return okc ? ms * 1000.f / 200.f : -1.f;
         };
+        // every (algo, proto) with each CTA-cap divisor, and two-shot HB with
+        // both stagings (the buffers here are 16-byte aligned); the fastest
+        // launch is kept for this size
+        const int user_div = h->grid_div, user_staging = h->hb_staging;
         for (int a = 0; a < 2 && rc == AR_OK; ++a)
             for (int p = 0; p < 2 && rc == AR_OK; ++p) {
                 h->tuned_us[b][a][p] = 0.f;
+                h->tuned_div[b][a][p] = 1;
                 if (p == AR_LL && !h->slots)
                     continue;
-                if (a == AR_TWO_SHOT && p == AR_HB) {
-                    // both stagings (the buffers here are 16-byte aligned);
-                    // the faster is kept for this size
-                    const int user = h->hb_staging;
-                    h->hb_staging = AR_HB_STAGING_TMA;
-                    const float t_tma = time_path(a, p);
-                    h->hb_staging = AR_HB_STAGING_DIRECT;
-                    const float t_dir = t_tma < 0.f ? -1.f : time_path(a, p);
-                    h->hb_staging = user;
-                    if (t_tma < 0.f || t_dir < 0.f) {
-                        rc = AR_ERR_CUDA;
-                        break;
+                const bool stagings = a == AR_TWO_SHOT && p == AR_HB;
+                float best = -1.f;
+                int best_div = 1, best_staging = AR_HB_STAGING_AUTO;
+                for (int k = 0; k < kTuneDivs && rc == AR_OK; ++k) {
+                    // the fastest staging at this divisor; a larger divisor
+                    // is kept only when it beats the smaller ones by more
+                    // than kTuneDivMargin (where the message never reaches
+                    // the cap the launches are the same, and only noise
+                    // would tell them apart)
+                    float us_k = -1.f;
+                    int staging_k = AR_HB_STAGING_AUTO;
+                    for (int st = 0; st < (stagings ? 2 : 1); ++st) {
+                        h->grid_div = kTuneDiv[k];
+                        if (stagings)
+                            h->hb_staging = st == 0 ? AR_HB_STAGING_TMA : AR_HB_STAGING_DIRECT;
+                        const float us = time_path(a, p);
+                        if (us < 0.f) {
+                            rc = AR_ERR_CUDA;
+                            break;
+                        }
+                        if (us_k < 0.f || us < us_k) {
+                            us_k = us;
+                            staging_k = h->hb_staging;
+                        }
                     }
-                    h->tuned_hb2[b] = t_dir < t_tma ? AR_HB_STAGING_DIRECT : AR_HB_STAGING_TMA;
-                    h->tuned_us[b][a][p] = t_dir < t_tma ? t_dir : t_tma;
-                    continue;
+                    if (rc == AR_OK && (best < 0.f || us_k < best * (1.f - kTuneDivMargin))) {
+                        best = us_k;
+                        best_div = kTuneDiv[k];
+                        best_staging = staging_k;
+                    }
                 }
-                const float us = time_path(a, p);
-                if (us < 0.f) {
-                    rc = AR_ERR_CUDA;
+                h->grid_div = user_div;
+                h->hb_staging = user_staging;
+                if (rc != AR_OK)
                     break;
-                }
-                h->tuned_us[b][a][p] = us;
+                h->tuned_us[b][a][p] = best;
+                h->tuned_div[b][a][p] = best_div;
+                if (stagings)
+                    h->tuned_hb2[b] = best_staging;
             }
         if (rc == AR_OK)
             last = b;
@@ -855,6 +911,21 @@ int ar_get_hb_staging(ar_handle_t h, size_t bytes, int *staging) {
     if (!h || !staging || bytes == 0 || bytes > h->N * h->esz)
         return AR_ERR_INVALID;
     *staging = hb2_staging(h, bytes / h->esz > 0 ? bytes / h->esz : 1);
+    return AR_OK;
+}
+
+int ar_set_grid_divisor(ar_handle_t h, int divisor) {
+    if (!h || (divisor != 0 && divisor != 1 && divisor != 2 && divisor != 4 && divisor != 8))
+        return AR_ERR_INVALID;
+    h->grid_div = divisor;
+    return AR_OK;
+}
+
+int ar_get_grid_divisor(ar_handle_t h, size_t bytes, int algo, int proto, int *divisor) {
+    if (!h || !divisor || bytes == 0 || bytes > h->N * h->esz ||
+        (algo != AR_ONE_SHOT && algo != AR_TWO_SHOT) || (proto != AR_LL && proto != AR_HB))
+        return AR_ERR_INVALID;
+    *divisor = grid_div(h, bytes / h->esz > 0 ? bytes / h->esz : 1, algo, proto);
     return AR_OK;
 }
 

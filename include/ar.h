@@ -369,6 +369,25 @@ int ar_set_hb_staging(ar_handle_t h, int staging);
  * range). */
 int ar_get_hb_staging(ar_handle_t h, size_t bytes, int *staging);
 
+/* Launch shape: the number of CTAs.  The SGLang guide's tuner (section 4.4)
+ * times launch configurations (blocks, threads per block) for each
+ * algorithm; here the threads per CTA are fixed per kernel by its launch
+ * bounds, and the CTA count is the path's cap (what the message needs, at
+ * most the co-resident or per-SM limit the path uses) divided by a divisor.
+ * ar_tune times divisors 1, 2 and 4 for every (algo, proto) at each tuned
+ * size and keeps the fastest; calls of any algo/proto then use it.
+ *
+ * Force the divisor for later calls: 1, 2, 4 or 8; 0 (the default) uses the
+ * tuned divisor, or 1 before ar_tune and above the tuned sizes.  Results are
+ * the same bits whatever the divisor.  Errors: AR_ERR_INVALID. */
+int ar_set_grid_divisor(ar_handle_t h, int divisor);
+
+/* The divisor a call of `bytes` per rank (1 .. N * elem_size) with this algo
+ * (AR_ONE_SHOT or AR_TWO_SHOT) and proto (AR_LL or AR_HB) would use now.
+ * Errors: AR_ERR_INVALID (NULL, bytes out of range, AUTO or unknown
+ * algo/proto). */
+int ar_get_grid_divisor(ar_handle_t h, size_t bytes, int algo, int proto, int *divisor);
+
 /* Fault injection for tests: virtual rank `rank` (0..R-1) writes no LL
  * packets in later LL calls, so its peers' polls time out (AR_ERR_TIMEOUT
  * from ar_status) and the kernel returns.  -1 turns it off.  The pages

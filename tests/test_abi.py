@@ -64,6 +64,9 @@ def test_null_handle_paths(lib):
     assert lib.ar_status(None, None) == ar.AR_ERR_INVALID
     assert lib.ar_set_timeout(None, 5) == ar.AR_ERR_INVALID
     assert lib.ar_debug_drop_rank(None, 0) == ar.AR_ERR_INVALID
+    assert lib.ar_set_grid_divisor(None, 1) == ar.AR_ERR_INVALID
+    out = ctypes.c_int(0)
+    assert lib.ar_get_grid_divisor(None, 16, 0, 1, ctypes.byref(out)) == ar.AR_ERR_INVALID
     assert lib.ar_get_info(None, None) == ar.AR_ERR_INVALID
     assert lib.ar_destroy(None) == ar.AR_OK
 

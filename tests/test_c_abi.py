@@ -41,6 +41,8 @@ int main(void) {
     ar_set_ll_transport(h, AR_LL_AUTO);
     ar_set_hb_staging(h, AR_HB_STAGING_AUTO);
     ar_get_hb_staging(h, 4096, &a);
+    ar_set_grid_divisor(h, 0);
+    ar_get_grid_divisor(h, 4096, AR_TWO_SHOT, AR_HB, &a);
     ar_debug_drop_rank(h, -1);
     ar_round(AR_FP16, (const float *)in[0], out[0], 1, 0);
     ar_get_info(h, &info);

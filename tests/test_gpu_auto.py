@@ -122,3 +122,81 @@ def test_tune_keeps_the_faster_staging(R, dtype):
         assert seen
         for n in (1000, 70001, N):
             _prefix_case(h.h, R, N, n, dtype, ar.AR_TWO_SHOT, ar.AR_HB, cpu)
+
+
+PATHS = [(ar.AR_ONE_SHOT, ar.AR_HB), (ar.AR_TWO_SHOT, ar.AR_HB), (ar.AR_ONE_SHOT, ar.AR_LL),
+         (ar.AR_TWO_SHOT, ar.AR_LL)]
+PATH_IDS = ["one_shot_hb", "two_shot_hb", "one_shot_ll", "two_shot_ll"]
+
+
+def _divided_case(R, n, dtype, algo, proto, divisor, offset=0, staging=None):
+    from gpu_helpers import device_inputs
+    cpu = wl.make_inputs(74, R, n, dtype, "loguniform")
+    want = expected(cpu, dtype)
+    ins = device_inputs(cpu, offset)
+    bufs, outs = guarded_outputs(R, n, dtype, offset)
+    with ar.Handle(R, n, dtype) as h:
+        ar.ar_set_grid_divisor(h.h, divisor)
+        if staging is not None:
+            ar.ar_set_hb_staging(h.h, staging)
+        assert ar.ar_get_grid_divisor(h.h, n * wl.ELEM_SIZE[dtype], algo, proto) == divisor
+        ar.ar_allreduce(h.h, ins, outs, algo, proto)
+        assert ar.ar_status(h.h) == ar.AR_OK
+    for r in range(R):
+        assert_bits_equal(outs[r], want, dtype, "R=%d n=%d div=%d rank %d" % (R, n, divisor, r))
+    check_guards(bufs, n, dtype, offset)
+
+
+@pytest.mark.parametrize("divisor", [2, 4, 8])
+@pytest.mark.parametrize("path", PATHS, ids=PATH_IDS)
+def test_grid_divisor_every_path(path, divisor):
+    """Every path with its CTA cap divided (each CTA serving more of the
+    message): sizes large enough to reach the caps, a ragged tail, and
+    buffers off 16- and 8-byte alignment (the element-wise and per-rank
+    kernels); the same bits as the oracle."""
+    need_gpu()
+    algo, proto = path
+    _divided_case(8, (1 << 18) + 3, "bf16", algo, proto, divisor)
+    _divided_case(5, (1 << 17) + 1, "bf16", algo, proto, divisor, offset=1)
+    if proto == ar.AR_HB:
+        _divided_case(16, (1 << 20) + 5, "fp16", algo, proto, divisor)
+
+
+@pytest.mark.parametrize("divisor", [2, 4])
+@pytest.mark.parametrize("staging", [ar.AR_HB_STAGING_TMA, ar.AR_HB_STAGING_DIRECT],
+                         ids=["tma", "direct"])
+def test_grid_divisor_two_shot_stagings(staging, divisor):
+    """Two-shot HB with each staging and a divided grid, up to the binary32
+    wide form (more than 64 MiB moved, 384-thread CTAs)."""
+    need_gpu()
+    _divided_case(8, (4 << 20) + 1, "fp32", ar.AR_TWO_SHOT, ar.AR_HB, divisor, staging=staging)
+    _divided_case(32, (1 << 16) + 7, "bf16", ar.AR_TWO_SHOT, ar.AR_HB, divisor, staging=staging)
+
+
+def test_grid_divisor_setting_and_tuning():
+    """The forced divisor is reported for every path and rejected outside
+    0, 1, 2, 4, 8; ar_tune picks 1, 2 or 4 per size and path, and calls
+    after tuning (forced paths and AUTO) stay exact."""
+    need_gpu()
+    R, N, dtype = 8, (1 << 20) + 3, "bf16"
+    cpu = wl.make_inputs(75, R, N, dtype, "normal")
+    with ar.Handle(R, N, dtype) as h:
+        for a, p in PATHS:
+            assert ar.ar_get_grid_divisor(h.h, 4096, a, p) == 1
+        for bad in (-1, 3, 16):
+            with pytest.raises(ar.ArError):
+                ar.ar_set_grid_divisor(h.h, bad)
+        for a, p, nbytes in ((ar.AR_ALGO_AUTO, ar.AR_HB, 16), (ar.AR_ONE_SHOT, 5, 16),
+                             (ar.AR_ONE_SHOT, ar.AR_HB, 0), (ar.AR_ONE_SHOT, ar.AR_HB, 2 * N + 1)):
+            with pytest.raises(ar.ArError):
+                ar.ar_get_grid_divisor(h.h, nbytes, a, p)
+        ar.ar_set_grid_divisor(h.h, 4)
+        assert ar.ar_get_grid_divisor(h.h, 4096, ar.AR_TWO_SHOT, ar.AR_LL) == 4
+        ar.ar_set_grid_divisor(h.h, 0)
+        ar.ar_tune(h.h)
+        for lg in range(9, 22):
+            for a, p in PATHS:
+                assert ar.ar_get_grid_divisor(h.h, 1 << lg, a, p) in (1, 2, 4), (lg, a, p)
+        for choice in [(ar.AR_ALGO_AUTO, ar.AR_PROTO_AUTO)] + PATHS:
+            for n in (1000, 70001, (1 << 19) + 7, N):
+                _prefix_case(h.h, R, N, n, dtype, *choice, cpu)
