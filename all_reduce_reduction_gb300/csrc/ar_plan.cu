@@ -29,7 +29,8 @@
 //     plan's all-gather copies fuse into the shard reductions this way: no
 //     re-read of the reduced shards, and no semaphores left.
 //   * A dependency inside one CTA needs nothing beyond program order (the
-//     CTA syncs its threads between tasks).  One across CTAs gets a
+//     CTA syncs its threads between tasks, except between tasks of one step
+//     on different chunks, which share no region).  One across CTAs gets a
 //     semaphore: the producer task signals it once per run, the consumer
 //     waits for it.  Every wait targets a task earlier in program order, and
 //     all CTAs are resident at once (cooperative launch), so every wait ends.
@@ -147,8 +148,11 @@ __device__ void run_task(const PlanArgs &a, const TaskPtrs &t, uint64_t chunk) {
     }
 }
 
+// Occupancy as measured: binary32 held to 64 registers (four CTAs per SM;
+// the compiler takes 80 otherwise), the 16-bit forms to three CTAs per SM
 template <int DT>
-__global__ void __launch_bounds__(kRegThreads) k_plan(const __grid_constant__ PlanArgs a) {
+__global__ void __launch_bounds__(kRegThreads, DT == AR_FP32 ? 4 : 3)
+    k_plan(const __grid_constant__ PlanArgs a) {
     __shared__ int give_up;
     __shared__ TaskPtrs tp;
     kernel_prologue();
@@ -158,8 +162,29 @@ __global__ void __launch_bounds__(kRegThreads) k_plan(const __grid_constant__ Pl
         give_up = 0;
     __syncthreads();
     const int i0 = a.start[blockIdx.x], i1 = a.start[blockIdx.x + 1];
+    // the (step, extra-destination list) resolved into tp, and whether a task
+    // has run since the last CTA barrier (all of these are uniform per CTA)
+    int res_step = -1, res_x = -2;
+    bool pending = false;
+    // Skipping the barrier lets a CTA's warps drift apart across its chunks.
+    // With short chunks (under 8 passes of the CTA) the barrier keeps them on
+    // one contiguous chunk, which measured faster (two-shot plan, 8 KiB
+    // chunks); with long chunks skipping it measured faster (one-shot plans).
+    const bool may_skip = a.chunk >= (uint64_t)8 * blockDim.x * Elem<DT>::kPerVec;
     for (int i = i0; i < i1; ++i) {
         const int4 in = a.instr[i];
+        // A task of the step and list already in tp, right after another task,
+        // needs no barrier and no resolving: a step covers each chunk once, so
+        // it works on chunks that the tasks run since the last barrier (the
+        // same step on other chunks) neither read nor wrote, and tp stays.
+        // Anything else (or any task, with short chunks) first waits for every
+        // thread's part of those tasks.
+        const bool same =
+            may_skip && in.x == kInstrTask && pending && in.y == res_step && in.w == res_x;
+        if (pending && !same) {
+            __syncthreads();
+            pending = false;
+        }
         if (in.x == kInstrWait) {
             if (threadIdx.x == 0 && !give_up) {
                 // bounded acquire-poll of the producer's semaphore
@@ -193,25 +218,31 @@ __global__ void __launch_bounds__(kRegThreads) k_plan(const __grid_constant__ Pl
             __syncthreads();
         } else if (in.x == kInstrTask) {
             if (!give_up) {
-                const PlanStep &st = a.steps[in.y];
-                const int nx = in.w >= 0 ? a.xdst[in.w] : 0;
-                if (threadIdx.x < (unsigned)st.nsrc)
-                    tp.src[threadIdx.x] = buf_ptr(a, st.src[threadIdx.x]);
-                if (threadIdx.x < (unsigned)nx)
-                    tp.xdst[threadIdx.x] = const_cast<void *>(buf_ptr(a, a.xdst[in.w + 1 + threadIdx.x]));
-                if (threadIdx.x == 0) {
-                    tp.dst = const_cast<void *>(buf_ptr(a, st.dst));
-                    tp.kind = st.kind;
-                    tp.nsrc = st.nsrc;
-                    tp.nx = nx;
+                if (!same) {
+                    const PlanStep &st = a.steps[in.y];
+                    const int nx = in.w >= 0 ? a.xdst[in.w] : 0;
+                    if (threadIdx.x < (unsigned)st.nsrc)
+                        tp.src[threadIdx.x] = buf_ptr(a, st.src[threadIdx.x]);
+                    if (threadIdx.x < (unsigned)nx)
+                        tp.xdst[threadIdx.x] =
+                            const_cast<void *>(buf_ptr(a, a.xdst[in.w + 1 + threadIdx.x]));
+                    if (threadIdx.x == 0) {
+                        tp.dst = const_cast<void *>(buf_ptr(a, st.dst));
+                        tp.kind = st.kind;
+                        tp.nsrc = st.nsrc;
+                        tp.nx = nx;
+                    }
+                    __syncthreads();
+                    res_step = in.y;
+                    res_x = in.w;
                 }
-                __syncthreads();
                 run_task<DT>(a, tp, (uint64_t)in.z);
+                pending = true;
             }
-            __syncthreads();
         } else {
-            // every thread's writes of the task are done (barrier above);
-            // make them visible GPU-wide, then count the task complete
+            // every thread's writes of the tasks before are done (the barrier
+            // at the top of this iteration); make them visible GPU-wide, then
+            // count the task complete
             if (threadIdx.x == 0 && !give_up) {
                 __threadfence();
                 asm volatile("red.release.gpu.global.add.u32 [%0], 1;" :: "l"(a.sems + in.y) : "memory");
@@ -451,9 +482,12 @@ static int compile_plan(ar_handle_t h, const ar_op *ops, int nops, int nchunks,
         if (tasks[id].signals)
             tasks[id].sem = nsems++;
     // one instruction stream per CTA, in program order; the extra
-    // destination lists go to a table of their own
+    // destination lists go to a table of their own, each distinct list once
+    // (tasks of one step on different chunks usually share theirs, and the
+    // interpreter keeps a resolved (step, list) across such tasks)
     std::vector<std::vector<int4>> prog(ctas);
     std::vector<int> xtable;
+    std::map<std::vector<int>, int> xseen;
     for (int id : live) {
         const Task &t = tasks[id];
         for (int d : t.deps) {
@@ -462,9 +496,15 @@ static int compile_plan(ar_handle_t h, const ar_op *ops, int nops, int nchunks,
         }
         int x = -1;
         if (!t.xdst.empty()) {
-            x = (int)xtable.size();
-            xtable.push_back((int)t.xdst.size());
-            xtable.insert(xtable.end(), t.xdst.begin(), t.xdst.end());
+            const auto found = xseen.find(t.xdst);
+            if (found != xseen.end()) {
+                x = found->second;
+            } else {
+                x = (int)xtable.size();
+                xtable.push_back((int)t.xdst.size());
+                xtable.insert(xtable.end(), t.xdst.begin(), t.xdst.end());
+                xseen.emplace(t.xdst, x);
+            }
         }
         prog[t.cta].push_back(make_int4(kInstrTask, t.step, t.chunk, x));
         if (t.signals)
