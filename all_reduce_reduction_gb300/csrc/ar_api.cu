@@ -22,11 +22,17 @@ constexpr int kTuneMaxLog2 = 23;
 constexpr int kTuneDiv[] = {1, 2, 4};
 constexpr int kTuneDivs = 3;
 constexpr float kTuneDivMargin = 0.02f;
+// Two-shot HB calls moving at least this many bytes (with R >= 4) run the
+// TMA staging in its one-stage form.
+constexpr uint64_t kTmaLargeBytes = (uint64_t)1 << 30;
 // Two-shot HB with AR_HB_STAGING_AUTO before ar_tune (and above the tuned
 // sizes): TMA staging where it measured faster on GB300, direct staging
 // elsewhere.  T = bytes moved per call, 2 R n elem_size.
 static bool tma_band(int R, uint64_t T) {
     const uint64_t KiB = 1024, MiB = KiB * KiB;
+    if (R >= 4 && R <= 16 && T >= kTmaLargeBytes)
+        return true;                         // the one-stage form (at R = 32 the
+                                             // direct staging measured as fast or faster)
     if (R >= 32)
         return T >= 64 * KiB && T <= 128 * MiB;
     if (R >= 16)
@@ -56,6 +62,8 @@ struct ar_handle {
     int reg_cap;            // CTAs of the 256-thread kernels per launch
     int tma_tile;
     int tma_stages;
+    int tma_tile_large;     // per-rank tile of the one-stage form for calls
+                            // moving >= kTmaLargeBytes, 0 = not used
     // AUTO choice per message-size bucket (bucket b: messages of at most
     // 2^(9+b) bytes per rank), timed by ar_tune; us[algo][proto], 0 = untimed
     float tuned_us[kBuckets][2][2];
@@ -237,18 +245,25 @@ int two_shot_hb(ar_handle *h, const Call &c) {
     const int div = grid_div(h, c.n, AR_TWO_SHOT, AR_HB);
     const uint64_t body = (c.n * h->esz) / 16 * 16;
     if (c.vec16 && body > 0 && hb2_staging(h, c.n) == AR_HB_STAGING_TMA) {
+        // far beyond L2 (>= 1 GiB moved) one stage of 128 KiB per CTA and two
+        // CTAs per SM in turn streamed faster than several stages filling the
+        // SM's shared memory (R = 16 x 128 MiB: 635 against 676 us); below
+        // that, the handle's stages
+        const bool large =
+            h->tma_tile_large > 0 && 2 * (uint64_t)h->R * c.n * h->esz >= kTmaLargeBytes;
+        const int tile = large ? h->tma_tile_large : h->tma_tile;
         TmaArgs a;
         fill_ptrs(h, c.in, c.out, &a.p);
         a.n = c.n;
         a.body_bytes = body;
         a.shard_bytes = c.shard * h->esz;
-        a.tiles_per_shard = ceil_div(a.shard_bytes, (uint64_t)h->tma_tile);
+        a.tiles_per_shard = ceil_div(a.shard_bytes, (uint64_t)tile);
         a.R = h->R;
-        a.tile_bytes = h->tma_tile;
-        a.stages = h->tma_stages;
+        a.tile_bytes = tile;
+        a.stages = large ? 1 : h->tma_stages;
         a.c = h->ctl;
-        const uint64_t items = ceil_div(body, (uint64_t)h->tma_tile) + (uint64_t)h->R;
-        const int grid = clamp_grid(items, div_cap(h->num_sms, div));
+        const uint64_t items = ceil_div(body, (uint64_t)tile) + (uint64_t)h->R;
+        const int grid = clamp_grid(items, div_cap((large ? 2 : 1) * h->num_sms, div));
         return from_cuda(launch_two_shot_tma(a, h->dtype, grid, c.s, h->pdl));
     }
     // direct staging, or unaligned buffers: one thread per 16-byte vector (or
@@ -501,6 +516,11 @@ int ar_create(int R, size_t N, int dtype, ar_handle_t *out) {
         tile -= 1024;
     h->tma_tile = tile;
     h->tma_stages = stages;
+    // calls moving kTmaLargeBytes or more: one stage of 128 KiB over R ranks
+    // (R >= 4: where it measured), two CTAs per SM in turn
+    const int large = (int)((128 * 1024 / R) / 16 * 16);
+    h->tma_tile_large =
+        R >= 4 && tma_smem_bytes(R, large, 1) <= (size_t)smem_limit ? large : 0;
 
     h->tuned_max = -1;                       // AUTO uses the fixed rule until ar_tune
     for (int b = 0; b < kBuckets; ++b) {

@@ -311,9 +311,12 @@ KERNEL_SOURCES = {
     "one_shot_ll_cluster": ["ar_ll_cluster.cu"],
     "one_shot_hb": [("ar_hb.cu", ["k_one_shot_hb", "one_shot_smem", "one_shot_dt",
                                   "one_shot_prepare_dt", "one_shot_prepare", "launch_one_shot_hb"])],
-    "two_shot_hb_tma": ["ar_tma.cu"],
+    # the two-shot launcher picks each staging's form (tile, stages, grid;
+    # CTA width) by message size: it counts too
+    "two_shot_hb_tma": ["ar_tma.cu", ("ar_api.cu", ["two_shot_hb"])],
     "two_shot_hb_direct": [("ar_hb.cu", ["reduce_body", "k_reduce", "k_reduce_o4", "k_reduce_wide",
-                                         "reduce_dt", "launch_reduce"])],
+                                         "reduce_dt", "launch_reduce"]),
+                           ("ar_api.cu", ["two_shot_hb"])],
     "combine": ["ar_combine.cu"],
     # a plan's traffic follows its compiled tasks: the compiler counts too
     "plan_": [("ar_plan.cu", ["k_plan", "compile_plan", "builtin_plan", "ar_plan_execute"])],
@@ -403,8 +406,8 @@ def kernel_source_digest(kernel_key: str) -> str:
         if funcs is None:
             h.update(text.encode())
             continue
-        first = text.find("__global__")
-        h.update(text[:first if first >= 0 else len(text)].encode())
+        first = text.find("__global__")     # a kernel file's helpers precede its kernels
+        h.update(text[:first if first >= 0 else 0].encode())
         for f in funcs:
             h.update(function_source(text, f).encode())
     return h.hexdigest()[:16]

@@ -133,8 +133,11 @@ enum ar_ll_transport {
  *   AR_HB_STAGING_TMA:    bulk copies (the Tensor Memory Accelerator) bring
  *                         tiles of the R inputs into shared memory; each
  *                         thread folds its vectors of the tile once and
- *                         stores them to the R outputs; one CTA per SM.
- *                         Best for mid-sized messages at larger R.
+ *                         stores them to the R outputs; one CTA per SM with
+ *                         several stages, or, for R >= 4 and calls moving
+ *                         1 GiB or more, one stage of 128 KiB and two CTAs
+ *                         per SM in turn.  Best for mid-sized messages at
+ *                         larger R and for messages far beyond L2.
  *   AR_HB_STAGING_DIRECT: one thread per 16-byte vector loads the R inputs
  *                         into registers, folds them once and stores R copies;
  *                         as many CTAs as the message needs.  Lower latency
@@ -143,12 +146,11 @@ enum ar_ll_transport {
  *                         faster at that size; before it, and above the
  *                         largest tuned size, a fixed rule from GB300
  *                         measurements: with T = 2 * R * n * elem_size bytes
- *                         moved per call, TMA for R >= 32 and 64 KiB <= T <=
- *                         128 MiB; for 16 <= R < 32 and T in [128 KiB, 1 MiB]
- *                         or [16 MiB, 64 MiB]; for 8 <= R < 16 and T in
- *                         [16 MiB, 64 MiB]; DIRECT otherwise (including every
- *                         large message: its many CTAs keep more loads in
- *                         flight).
+ *                         moved per call, TMA for 4 <= R <= 16 and
+ *                         T >= 1 GiB; for R >= 32 and 64 KiB <= T <= 128 MiB;
+ *                         for 16 <= R < 32 and T in [128 KiB, 1 MiB] or
+ *                         [16 MiB, 64 MiB]; for 8 <= R < 16 and T in
+ *                         [16 MiB, 64 MiB]; DIRECT otherwise.
  * Both are the reduce-scatter + all-gather schedule fused per unit (each
  * unit reduced once, by its shard's owner, and replicated) and give
  * identical results.  Source: the SGLang guide, section 4.4 (each algorithm

@@ -72,13 +72,16 @@ def test_untuned_rule(R):
 @pytest.mark.parametrize("R", [2, 4, 8, 16, 32])
 def test_untuned_staging_rule(R):
     """Before ar_tune, two-shot HB stages with TMA only in the bands where it
-    measured faster (by bytes moved per call, T = 2 R n elem_size: R >= 32 and
-    64 KiB-128 MiB; 16 <= R < 32 and 128 KiB-1 MiB or 16-64 MiB; 8 <= R < 16
-    and 16-64 MiB), directly elsewhere; a fixed setting overrides it."""
+    measured faster (by bytes moved per call, T = 2 R n elem_size: 4 <= R <= 16
+    and T >= 1 GiB; R >= 32 and 64 KiB-128 MiB; 16 <= R < 32 and 128 KiB-1 MiB or
+    16-64 MiB; 8 <= R < 16 and 16-64 MiB), directly elsewhere; a fixed
+    setting overrides it."""
     need_gpu()
     KiB, MiB = 1 << 10, 1 << 20
 
     def band(R, T):
+        if 4 <= R <= 16 and T >= 1 << 30:
+            return True
         if R >= 32:
             return 64 * KiB <= T <= 128 * MiB
         if R >= 16:
@@ -86,9 +89,9 @@ def test_untuned_staging_rule(R):
         if R >= 8:
             return 16 * MiB <= T <= 64 * MiB
         return False
-    with ar.Handle(R, 64 << 20, "bf16") as h:
+    with ar.Handle(R, 64 << 20, "bf16") as h:          # 128 MiB per rank
         for nbytes in [1024, 4096, 16384, 65536, 1 << 20, 2 << 20, 4 << 20, 8 << 20, 32 << 20,
-                       64 << 20]:
+                       64 << 20, 128 << 20]:
             T = 2 * R * nbytes
             want = ar.AR_HB_STAGING_TMA if band(R, T) else ar.AR_HB_STAGING_DIRECT
             assert ar.ar_get_hb_staging(h.h, nbytes) == want, (R, nbytes)

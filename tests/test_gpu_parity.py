@@ -146,6 +146,17 @@ def test_two_shot_hb_stagings_in_place(staging, offset):
              staging=staging)
 
 
+@pytest.mark.parametrize("R,n,dtype", [(5, (1 << 26) + 3, "bf16"), (4, (1 << 25) + 1, "fp32")],
+                         ids=["r5_bf16", "r4_fp32"])
+def test_two_shot_tma_one_stage_form(R, n, dtype):
+    """Two-shot HB with TMA staging on calls moving 1 GiB or more (one stage
+    of 128 KiB per CTA, two CTAs per SM in turn): a runtime rank count and
+    R = 4 (32 KiB tiles), each with a ragged tail; the same bits as the
+    oracle."""
+    assert 2 * R * n * wl.ELEM_SIZE[dtype] >= 1 << 30
+    run_case(R, n, dtype, ar.AR_TWO_SHOT, ar.AR_HB, dist="normal", staging=ar.AR_HB_STAGING_TMA)
+
+
 def wide_threshold_units():
     """16-byte vectors per rank from which a binary32 two-shot HB call moving
     more than 64 MiB runs its direct staging in 384-thread CTAs: the grid of
