@@ -173,14 +173,15 @@ __global__ void __launch_bounds__(kRegThreads, DT == AR_FP32 ? 4 : 3)
     const bool may_skip = a.chunk >= (uint64_t)8 * blockDim.x * Elem<DT>::kPerVec;
     for (int i = i0; i < i1; ++i) {
         const int4 in = a.instr[i];
-        // A task of the step and list already in tp, right after another task,
-        // needs no barrier and no resolving: a step covers each chunk once, so
-        // it works on chunks that the tasks run since the last barrier (the
-        // same step on other chunks) neither read nor wrote, and tp stays.
-        // Anything else (or any task, with short chunks) first waits for every
-        // thread's part of those tasks.
-        const bool same =
-            may_skip && in.x == kInstrTask && pending && in.y == res_step && in.w == res_x;
+        // A task of the step and list already in tp needs no resolving (tp is
+        // written only to resolve another).  Right after another task it also
+        // needs no barrier: a step covers each chunk once, so it works on
+        // chunks that the tasks run since the last barrier (the same step on
+        // other chunks) neither read nor wrote.  Anything else (or any task,
+        // with short chunks) first waits for every thread's part of those
+        // tasks.
+        const bool same_desc = in.x == kInstrTask && in.y == res_step && in.w == res_x;
+        const bool same = may_skip && same_desc && pending;
         if (pending && !same) {
             __syncthreads();
             pending = false;
@@ -218,7 +219,7 @@ __global__ void __launch_bounds__(kRegThreads, DT == AR_FP32 ? 4 : 3)
             __syncthreads();
         } else if (in.x == kInstrTask) {
             if (!give_up) {
-                if (!same) {
+                if (!same_desc) {
                     const PlanStep &st = a.steps[in.y];
                     const int nx = in.w >= 0 ? a.xdst[in.w] : 0;
                     if (threadIdx.x < (unsigned)st.nsrc)
