@@ -262,13 +262,16 @@ int ar_allreduce_n(ar_handle_t h, const void *const in[], void *const out[], siz
  * size, rounded up to a power of two and clamped to [512 B, 256 MiB], to the
  * fastest).  Here: each (algo, proto) pair is timed at every power of two
  * from 512 B to min(8 MiB, N * elem_size) bytes per rank as a graph of 10
- * calls, 5 warm-up replays then 20 timed replays, two-shot HB once per
- * staging (enum ar_hb_staging; the faster is kept for that size and used by
- * later two-shot HB calls with AR_HB_STAGING_AUTO); sizes above the largest
- * tuned one use its (algo, proto) choice.  Not a hot-path call: it waits for `stream`,
- * allocates and frees 2 * R temporary buffers, creates a private stream and
- * synchronises.  Returns AR_OK or the first error (including a device-side
- * one, as ar_status would). */
+ * calls, 5 warm-up replays then 20 timed replays, with each CTA-cap divisor
+ * 1, 2 and 4 (see ar_set_grid_divisor; a larger one is kept only when more
+ * than 2% faster) and two-shot HB also once per staging (enum ar_hb_staging).
+ * The fastest launch of each pair is kept for that size: its divisor for
+ * later calls of that pair, its staging for later two-shot HB calls with
+ * AR_HB_STAGING_AUTO; sizes above the largest tuned one use its (algo, proto)
+ * choice.  Not a hot-path call: it waits for `stream`, allocates and frees
+ * 2 * R temporary buffers, creates a private stream and synchronises.
+ * Returns AR_OK or the first error (including a device-side one, as
+ * ar_status would). */
 int ar_tune(ar_handle_t h, cudaStream_t stream);
 
 /* The AUTO choice for a message of `bytes` per rank (*algo, *proto) and,
