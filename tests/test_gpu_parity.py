@@ -146,15 +146,18 @@ def test_two_shot_hb_stagings_in_place(staging, offset):
              staging=staging)
 
 
-@pytest.mark.parametrize("R,n,dtype", [(5, (1 << 26) + 3, "bf16"), (4, (1 << 25) + 1, "fp32")],
-                         ids=["r5_bf16", "r4_fp32"])
-def test_two_shot_tma_one_stage_form(R, n, dtype):
+@pytest.mark.parametrize("R,n,dtype,inplace", [(5, (1 << 26) + 3, "bf16", False),
+                                               (4, (1 << 25) + 1, "fp32", False),
+                                               (4, (1 << 25) + 1, "fp32", True)],
+                         ids=["r5_bf16", "r4_fp32", "r4_fp32_in_place"])
+def test_two_shot_tma_one_stage_form(R, n, dtype, inplace):
     """Two-shot HB with TMA staging on calls moving 1 GiB or more (one stage
     of 128 KiB per CTA, two CTAs per SM in turn): a runtime rank count and
-    R = 4 (32 KiB tiles), each with a ragged tail; the same bits as the
-    oracle."""
+    R = 4 (32 KiB tiles), each with a ragged tail, and in place; the same
+    bits as the oracle."""
     assert 2 * R * n * wl.ELEM_SIZE[dtype] >= 1 << 30
-    run_case(R, n, dtype, ar.AR_TWO_SHOT, ar.AR_HB, dist="normal", staging=ar.AR_HB_STAGING_TMA)
+    run_case(R, n, dtype, ar.AR_TWO_SHOT, ar.AR_HB, dist="normal", inplace=inplace,
+             staging=ar.AR_HB_STAGING_TMA)
 
 
 def wide_threshold_units():
