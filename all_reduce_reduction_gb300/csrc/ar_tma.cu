@@ -20,7 +20,10 @@
 //     16 and 32 the fold is instantiated with R fixed, fully unrolled, its
 //     shared-memory reads issued eight at a time.
 // The consumer warps never wait for one another: no named barrier.  No
-// multicast.  Minimal traffic: R reads + R writes of every byte.
+// multicast.  Minimal traffic: R reads + R writes of every byte.  The tile
+// size, the number of stages and the grid come from the launcher per call:
+// several stages on one CTA per SM, or, for calls moving 1 GiB or more, one
+// stage of 128 KiB on two CTAs per SM that run one after the other.
 //
 // Every wait is bounded by the handle's timeout; a timed-out wait records
 // AR_ERR_TIMEOUT and raises a shared abort flag that every other waiter of
