@@ -199,7 +199,8 @@ int bucket_of(uint64_t bytes);
 // launch-shape dimension of the tuner): the handle's forced one, else the one
 // ar_tune timed fastest at the message's size bucket, else 1.  Threads per
 // CTA are fixed per kernel by its launch bounds.
-int grid_div(const ar_handle *h, uint64_t n, int algo, int proto) {
+// 0 when the handle neither forces a divisor nor has one tuned for the size.
+int grid_div_set(const ar_handle *h, uint64_t n, int algo, int proto) {
     if (h->grid_div > 0)
         return h->grid_div;
     if (h->tuned_max >= 0) {
@@ -207,7 +208,12 @@ int grid_div(const ar_handle *h, uint64_t n, int algo, int proto) {
         if (b <= h->tuned_max)
             return h->tuned_div[b][algo][proto];
     }
-    return 1;
+    return 0;
+}
+
+int grid_div(const ar_handle *h, uint64_t n, int algo, int proto) {
+    const int d = grid_div_set(h, n, algo, proto);
+    return d > 0 ? d : 1;
 }
 
 int div_cap(int cap, int div) {
@@ -215,12 +221,36 @@ int div_cap(int cap, int div) {
     return c > 0 ? c : 1;
 }
 
+// One-shot HB: runs of the message (a run: 32 units of every rank for one
+// CTA's warps) and the divisor of the CTA cap.  Without a forced or tuned
+// divisor, a message of R <= 16 ranks with more runs than a quarter of the
+// cap and at most twice the cap runs on a quarter of the cap: at up to one
+// run per CTA the full grid folds without the shared-memory ring, and at up
+// to two it keeps too few runs in each ring; a quarter of the cap measured
+// 3-30% faster (R = 4 at 512 KiB-2 MiB per rank, R = 8 at 256 KiB-1 MiB,
+// R = 16 at 128-512 KiB) and slower beyond twice the cap.  Above 16 ranks
+// the one-run form stages its inputs once and keeps the full grid.
+uint64_t one_shot_runs(const ar_handle *h, uint64_t n, bool vec16) {
+    const uint64_t units = vec16 ? n / (16 / h->esz) : n;
+    const uint64_t per_blk = (uint64_t)(h->one_shot_warps / h->R) * 32;
+    return ceil_div(units, per_blk);
+}
+
+int one_shot_div(const ar_handle *h, uint64_t n, bool vec16) {
+    const int d = grid_div_set(h, n, AR_ONE_SHOT, AR_HB);
+    if (d > 0)
+        return d;
+    const uint64_t runs = one_shot_runs(h, n, vec16);
+    if (h->R <= 16 && runs <= 2 * (uint64_t)h->one_shot_cap &&
+        runs > (uint64_t)(h->one_shot_cap / 4))
+        return 4;
+    return 1;
+}
+
 int one_shot_hb(ar_handle *h, const Call &c) {
     const HbArgs a = hb_args(h, c);
-    const uint64_t units = c.vec16 ? c.n / (16 / h->esz) : c.n;
-    const uint64_t per_blk = (uint64_t)(h->one_shot_warps / h->R) * 32;
-    const uint64_t runs = ceil_div(units, per_blk);
-    const int grid = clamp_grid(runs, div_cap(h->one_shot_cap, grid_div(h, c.n, AR_ONE_SHOT, AR_HB)));
+    const uint64_t runs = one_shot_runs(h, c.n, c.vec16);
+    const int grid = clamp_grid(runs, div_cap(h->one_shot_cap, one_shot_div(h, c.n, c.vec16)));
     return from_cuda(launch_one_shot_hb(a, h->dtype, c.vec16, runs <= (uint64_t)grid, grid,
                                         32 * h->one_shot_warps, c.s, h->pdl));
 }
@@ -945,7 +975,9 @@ int ar_get_grid_divisor(ar_handle_t h, size_t bytes, int algo, int proto, int *d
     if (!h || !divisor || bytes == 0 || bytes > h->N * h->esz ||
         (algo != AR_ONE_SHOT && algo != AR_TWO_SHOT) || (proto != AR_LL && proto != AR_HB))
         return AR_ERR_INVALID;
-    *divisor = grid_div(h, bytes / h->esz > 0 ? bytes / h->esz : 1, algo, proto);
+    const uint64_t n = bytes / h->esz > 0 ? bytes / h->esz : 1;
+    *divisor = algo == AR_ONE_SHOT && proto == AR_HB ? one_shot_div(h, n, true)
+                                                     : grid_div(h, n, algo, proto);
     return AR_OK;
 }
 

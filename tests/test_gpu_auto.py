@@ -203,3 +203,33 @@ def test_grid_divisor_setting_and_tuning():
         for choice in [(ar.AR_ALGO_AUTO, ar.AR_PROTO_AUTO)] + PATHS:
             for n in (1000, 70001, (1 << 19) + 7, N):
                 _prefix_case(h.h, R, N, n, dtype, *choice, cpu)
+
+
+@pytest.mark.parametrize("R,sizes", [
+    (8, [128 << 10, 256 << 10, 512 << 10, 1 << 20, 2 << 20]),
+    (16, [64 << 10, 128 << 10, 256 << 10, 512 << 10, 1 << 20]),
+    (4, [256 << 10, 512 << 10, 1 << 20, 2 << 20, 4 << 20]),
+    (32, [64 << 10, 256 << 10])], ids=["r8", "r16", "r4", "r32"])
+def test_one_shot_hb_untuned_divisor(R, sizes):
+    """Before ar_tune, one-shot HB runs a quarter of its CTA cap where the
+    full cap would give every CTA at most two runs of a mid-sized message
+    (R <= 16: more runs than a quarter of the cap, at most twice the cap; a
+    run is 32 16-byte units of every rank for one CTA of 8 warps, or R warps
+    above 8 ranks, and the cap fills 2048 threads per SM), the full cap
+    elsewhere; a forced divisor overrides it.  On 152 SMs the middle three
+    sizes of R = 4, 8 and 16 take the quarter."""
+    need_gpu()
+    with ar.Handle(R, 2 << 20, "bf16") as h:
+        sms = ar.ar_get_info(h.h)["num_sms"]
+        warps = R * ((8 + R - 1) // R) if R <= 8 else R
+        cap = sms * (2048 // (32 * warps))
+        per_run = (warps // R) * 32
+        for nbytes in sizes:
+            runs = -(-(nbytes // 16) // per_run)
+            want = 4 if R <= 16 and cap // 4 < runs <= 2 * cap else 1
+            got = ar.ar_get_grid_divisor(h.h, nbytes, ar.AR_ONE_SHOT, ar.AR_HB)
+            assert got == want, (R, nbytes, got)
+            assert ar.ar_get_grid_divisor(h.h, nbytes, ar.AR_TWO_SHOT, ar.AR_HB) == 1
+        ar.ar_set_grid_divisor(h.h, 1)
+        for nbytes in sizes:
+            assert ar.ar_get_grid_divisor(h.h, nbytes, ar.AR_ONE_SHOT, ar.AR_HB) == 1
