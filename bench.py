@@ -471,6 +471,7 @@ class CaseRunner:
             self.h = ar.Handle(w.R, w.n, w.dtype)
         ar.ar_set_ll_transport(self.h.h, c.get("transport", ar.AR_LL_AUTO))
         ar.ar_set_hb_staging(self.h.h, c.get("staging", ar.AR_HB_STAGING_AUTO))
+        ar.ar_set_grid_divisor(self.h.h, c.get("grid_divisor", 0))
         ar.ar_set_pdl(self.h.h, c.get("pdl", 1))
         self.algo, self.proto = ar.ALGOS.get(c["algo"], 0), ar.PROTOS[c["proto"]]
         self.choice = "combine" if c.get("combine") else None
@@ -536,9 +537,12 @@ def run_ours(args, dist: Dist):
         if not cases:
             raise SystemExit("--only %d matches no case of the workload" % args.only)
         desc += " (only the case of %d elements per rank)" % args.only
+    if args.grid_divisor:
+        desc += " (CTA-cap divisor %d)" % args.grid_divisor
     for c in cases:
         c["transport"] = TRANSPORTS[args.ll_transport]
         c["staging"] = STAGINGS[args.staging]
+        c["grid_divisor"] = args.grid_divisor
         c["pdl"] = 0 if args.no_pdl else 1
     stream = torch.cuda.Stream()
     runners = [CaseRunner(c, stream) for c in cases]
@@ -1174,11 +1178,14 @@ def make_parser() -> argparse.ArgumentParser:
     p.add_argument("--calls", type=int, default=10)
     p.add_argument("--plan", default=None, choices=["one_shot", "two_shot"],
                    help="custom workload: run the built-in plan of that algorithm")
-    p.add_argument("--plan-chunks", type=int, default=0, help="0: one chunk per CTA")
+    p.add_argument("--plan-chunks", type=int, default=0,
+                   help="0: the library's default (ar_plan_builtin)")
     p.add_argument("--plan-ctas", type=int, default=0, help="0: fill the resident capacity")
     p.add_argument("--ll-transport", default="auto", choices=["auto", "global", "cluster"])
     p.add_argument("--staging", default="auto", choices=["auto", "tma", "direct"],
                    help="two-shot HB staging (enum ar_hb_staging)")
+    p.add_argument("--grid-divisor", type=int, default=0, choices=[0, 1, 2, 4, 8],
+                   help="divisor of every path's CTA cap (ar_set_grid_divisor); 0: tuned or default")
     p.add_argument("--no-pdl", action="store_true",
                    help="launch without programmatic dependent launch")
     p.add_argument("--impl", default="ours", choices=["ours", "reference"])
