@@ -309,7 +309,7 @@ KERNEL_SOURCES = {
     "one_shot_ll_global": [("ar_ll.cu", ["k_ll_staged", "launch_ll_staged"])],
     "two_shot_ll": [("ar_ll.cu", ["k_ll2_staged", "launch_ll_staged"])],
     "one_shot_ll_cluster": ["ar_ll_cluster.cu"],
-    "one_shot_hb": [("ar_hb.cu", ["k_one_shot_hb", "one_shot_smem", "one_shot_dt",
+    "one_shot_hb": [("ar_hb.cu", ["k_one_shot_hb", "one_shot_smem", "one_shot_unrolled", "one_shot_dt",
                                   "one_shot_prepare_dt", "one_shot_prepare", "launch_one_shot_hb"])],
     # the two-shot launcher picks each staging's form (tile, stages, grid;
     # CTA width) by message size: it counts too
