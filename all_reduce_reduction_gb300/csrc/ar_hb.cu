@@ -350,27 +350,34 @@ static size_t one_shot_smem(bool vec, bool single, int R, int block) {
     return (size_t)(single ? 1 : kOneShotStages) * block * sizeof(uint4);
 }
 
-// Rank counts whose ring instantiation folds with R fixed (unrolled).
-static bool one_shot_unrolled(int R) { return R == 2 || R == 8 || R == 16; }
+// Rank counts whose ring instantiation folds with R fixed (unrolled); R = 4
+// only for one run per CTA (with several, the loop over R measured faster).
+static bool one_shot_unrolled(int R, bool single) {
+    return R == 2 || R == 8 || R == 16 || (R == 4 && single);
+}
 
 // `single`: the grid covers the message (one run per CTA at most).  The
 // one-run form then runs only for rank counts without an unrolled ring: with
 // one run per CTA the unrolled ring (each input staged once, the fold
 // unrolled) measured 8-23% faster than folding through L1 over a runtime R
-// (R = 2, 8, 16 at 1-64 KiB per rank), while at R = 4 the one-run form kept
-// its lead over the ring's runtime-R loop.
+// (R = 2, 8, 16 at 1-64 KiB per rank); the ring's runtime-R loop did not.
 template <int DT>
 static cudaError_t one_shot_dt(const HbArgs &a, bool vec, bool single, int grid, int block,
                                cudaStream_t s, bool pdl) {
-    const bool one_run = vec && single && !one_shot_unrolled(a.R);
+    const bool one_run = vec && single && !one_shot_unrolled(a.R, single);
     const size_t smem = one_shot_smem(vec, one_run, a.R, block);
     if (one_run)
         return launch_kernel(k_one_shot_hb<DT, true, true>, grid, block, smem, s, pdl, a);
     if (vec) {
         // rank counts with an unrolled fold: those where it measured faster
-        // (R = 4 measured slower unrolled and keeps the loop)
+        // (R = 4 only with one run per CTA: with several runs the loop
+        // measured faster)
         switch (a.R) {
         case 2: return launch_kernel(k_one_shot_hb<DT, true, false, 2>, grid, block, smem, s, pdl, a);
+        case 4:
+            if (single)
+                return launch_kernel(k_one_shot_hb<DT, true, false, 4>, grid, block, smem, s, pdl, a);
+            return launch_kernel(k_one_shot_hb<DT, true, false>, grid, block, smem, s, pdl, a);
         case 8: return launch_kernel(k_one_shot_hb<DT, true, false, 8>, grid, block, smem, s, pdl, a);
         case 16: return launch_kernel(k_one_shot_hb<DT, true, false, 16>, grid, block, smem, s, pdl, a);
         default: return launch_kernel(k_one_shot_hb<DT, true, false>, grid, block, smem, s, pdl, a);
@@ -382,6 +389,7 @@ static cudaError_t one_shot_dt(const HbArgs &a, bool vec, bool single, int grid,
 template <int DT> static cudaError_t one_shot_prepare_dt(int bytes) {
     const void *fns[] = {reinterpret_cast<const void *>(&k_one_shot_hb<DT, true, false>),
                          reinterpret_cast<const void *>(&k_one_shot_hb<DT, true, false, 2>),
+                         reinterpret_cast<const void *>(&k_one_shot_hb<DT, true, false, 4>),
                          reinterpret_cast<const void *>(&k_one_shot_hb<DT, true, false, 8>),
                          reinterpret_cast<const void *>(&k_one_shot_hb<DT, true, false, 16>)};
     for (const void *f : fns) {
