@@ -395,11 +395,13 @@ int bucket_of(uint64_t bytes) {
 // Resolve AR_ALGO_AUTO / AR_PROTO_AUTO for a message of `bytes` per rank:
 // the fastest tuned (algo, proto) allowed by the fixed half of the request,
 // or, before ar_tune, a fixed rule from GB300 measurements (10-call graphs,
-// L2 flushed): LL only for the one-shot at R >= 32 up to 4 KiB per rank,
-// HB otherwise; with HB, one-shot for R <= 2 at every size, for R = 4 up to
-// 256 KiB per rank and for 5 <= R <= 16 up to 64 KiB, two-shot otherwise
-// (against the two-shot with its AUTO staging the one-shot, whose fold work
-// grows with R^2, wins only there); with LL forced, one-shot up to 2 MiB.
+// L2 flushed; R = 2 to 32): LL only for the one-shot at R >= 24 up to 4 KiB
+// per rank, HB otherwise; with HB, one-shot for R <= 2 at every size, for
+// R = 4 up to 256 KiB per rank and for 8 <= R <= 24 up to 64 KiB, two-shot
+// otherwise (against the two-shot with its AUTO staging the one-shot, whose
+// fold work grows with R^2, wins only there; R = 3, 5 and 6, without an
+// unrolled ring, were faster or tied two-shot); with LL forced, one-shot up
+// to 2 MiB.
 void resolve(const ar_handle *h, uint64_t bytes, int *algo, int *proto) {
     const bool ll_ok = h->slots != nullptr;
     if (h->tuned_max >= 0) {
@@ -428,7 +430,7 @@ void resolve(const ar_handle *h, uint64_t bytes, int *algo, int *proto) {
         }
     }
     if (*proto == AR_PROTO_AUTO)
-        *proto = ll_ok && h->R >= 32 && bytes <= (4u << 10) && *algo != AR_TWO_SHOT ? AR_LL
+        *proto = ll_ok && h->R >= 24 && bytes <= (4u << 10) && *algo != AR_TWO_SHOT ? AR_LL
                                                                                   : AR_HB;
     if (*algo == AR_ALGO_AUTO) {
         bool one;
@@ -439,7 +441,7 @@ void resolve(const ar_handle *h, uint64_t bytes, int *algo, int *proto) {
         else if (h->R == 4)
             one = bytes <= (256u << 10);
         else
-            one = h->R >= 5 && h->R <= 16 && bytes <= (64u << 10);
+            one = h->R >= 8 && h->R <= 24 && bytes <= (64u << 10);
         *algo = one ? AR_ONE_SHOT : AR_TWO_SHOT;
     }
 }

@@ -53,16 +53,16 @@ def test_n_out_of_range_rejected():
             ar.ar_allreduce_n(h.h, x, y, 10, 7, ar.AR_HB)
 
 
-@pytest.mark.parametrize("R", [2, 3, 4, 8, 16, 32])
+@pytest.mark.parametrize("R", [2, 3, 4, 6, 8, 16, 24, 32])
 def test_untuned_rule(R):
-    """Before ar_tune: LL only for the one-shot at R >= 32 up to 4 KiB per
+    """Before ar_tune: LL only for the one-shot at R >= 24 up to 4 KiB per
     rank, HB otherwise; with HB one-shot for R <= 2 at every size, for R = 4
-    up to 256 KiB and for 5 <= R <= 16 up to 64 KiB, two-shot otherwise."""
+    up to 256 KiB and for 8 <= R <= 24 up to 64 KiB, two-shot otherwise."""
     need_gpu()
     with ar.Handle(R, 1 << 23, "bf16") as h:
         for nbytes in (512, 4096, 4098, 64 << 10, (64 << 10) + 2, 256 << 10, (256 << 10) + 2,
                        1 << 20, 8 << 20, 16 << 20):
-            if R >= 32 and nbytes <= 4 << 10:
+            if R >= 24 and nbytes <= 4 << 10:
                 want = (ar.AR_ONE_SHOT, ar.AR_LL)
             else:
                 if R <= 2:
@@ -70,14 +70,15 @@ def test_untuned_rule(R):
                 elif R == 4:
                     one = nbytes <= 256 << 10
                 else:
-                    one = 5 <= R <= 16 and nbytes <= 64 << 10
+                    one = 8 <= R <= 24 and nbytes <= 64 << 10
                 want = (ar.AR_ONE_SHOT if one else ar.AR_TWO_SHOT, ar.AR_HB)
             assert ar.ar_get_tuning(h.h, nbytes)[:2] == want, (R, nbytes)
         assert ar.ar_get_tuning(h.h, 4 << 20)[2] == [0.0, 0.0, 0.0, 0.0]
-    if R >= 32:
-        with ar.Handle(R, (128 << 20) // 2, "bf16") as h:      # beyond the LL limit
+    if R >= 24:
+        with ar.Handle(R, (128 << 20) // 2, "bf16") as h:      # beyond the LL limit: HB's rule
             assert ar.ar_get_info(h.h)["ll_capable"] == 0
-            assert ar.ar_get_tuning(h.h, 1024)[:2] == (ar.AR_TWO_SHOT, ar.AR_HB)
+            want = ar.AR_ONE_SHOT if R <= 24 else ar.AR_TWO_SHOT
+            assert ar.ar_get_tuning(h.h, 1024)[:2] == (want, ar.AR_HB)
 
 
 @pytest.mark.parametrize("R", [2, 4, 8, 16, 32])
