@@ -351,9 +351,10 @@ static size_t one_shot_smem(bool vec, bool single, int R, int block) {
 }
 
 // Rank counts whose ring instantiation folds with R fixed (unrolled); R = 4
-// only for one run per CTA (with several, the loop over R measured faster).
+// and 32 only for one run per CTA (with several, the loop over R measured
+// faster at R = 4; at R = 32 the one-shot is not the schedule for them).
 static bool one_shot_unrolled(int R, bool single) {
-    return R == 2 || R == 8 || R == 16 || (R == 4 && single);
+    return R == 2 || R == 8 || R == 16 || ((R == 4 || R == 32) && single);
 }
 
 // `single`: the grid covers the message (one run per CTA at most).  The
@@ -370,13 +371,16 @@ static cudaError_t one_shot_dt(const HbArgs &a, bool vec, bool single, int grid,
         return launch_kernel(k_one_shot_hb<DT, true, true>, grid, block, smem, s, pdl, a);
     if (vec) {
         // rank counts with an unrolled fold: those where it measured faster
-        // (R = 4 only with one run per CTA: with several runs the loop
-        // measured faster)
+        // (R = 4 and 32 only with one run per CTA)
         switch (a.R) {
         case 2: return launch_kernel(k_one_shot_hb<DT, true, false, 2>, grid, block, smem, s, pdl, a);
         case 4:
             if (single)
                 return launch_kernel(k_one_shot_hb<DT, true, false, 4>, grid, block, smem, s, pdl, a);
+            return launch_kernel(k_one_shot_hb<DT, true, false>, grid, block, smem, s, pdl, a);
+        case 32:
+            if (single)
+                return launch_kernel(k_one_shot_hb<DT, true, false, 32>, grid, block, smem, s, pdl, a);
             return launch_kernel(k_one_shot_hb<DT, true, false>, grid, block, smem, s, pdl, a);
         case 8: return launch_kernel(k_one_shot_hb<DT, true, false, 8>, grid, block, smem, s, pdl, a);
         case 16: return launch_kernel(k_one_shot_hb<DT, true, false, 16>, grid, block, smem, s, pdl, a);
@@ -390,6 +394,7 @@ template <int DT> static cudaError_t one_shot_prepare_dt(int bytes) {
     const void *fns[] = {reinterpret_cast<const void *>(&k_one_shot_hb<DT, true, false>),
                          reinterpret_cast<const void *>(&k_one_shot_hb<DT, true, false, 2>),
                          reinterpret_cast<const void *>(&k_one_shot_hb<DT, true, false, 4>),
+                         reinterpret_cast<const void *>(&k_one_shot_hb<DT, true, false, 32>),
                          reinterpret_cast<const void *>(&k_one_shot_hb<DT, true, false, 8>),
                          reinterpret_cast<const void *>(&k_one_shot_hb<DT, true, false, 16>)};
     for (const void *f : fns) {
