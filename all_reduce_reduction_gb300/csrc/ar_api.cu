@@ -397,8 +397,8 @@ int bucket_of(uint64_t bytes) {
 // or, before ar_tune, a fixed rule from GB300 measurements (10-call graphs,
 // L2 flushed; R = 2 to 32): LL only for the one-shot at R >= 24 up to 4 KiB
 // per rank, HB otherwise; with HB, one-shot for R <= 2 at every size, for
-// R = 4 up to 256 KiB per rank and for 8 <= R <= 24 up to 64 KiB, two-shot
-// otherwise (against the two-shot with its AUTO staging the one-shot, whose
+// R = 4 up to 256 KiB per rank, for R = 16 up to 128 KiB and for
+// 8 <= R <= 24 otherwise up to 64 KiB, two-shot otherwise (against the two-shot with its AUTO staging the one-shot, whose
 // fold work grows with R^2, wins only there; R = 3, 5 and 6, without an
 // unrolled ring, were faster or tied two-shot); with LL forced, one-shot up
 // to 2 MiB.
@@ -440,6 +440,8 @@ void resolve(const ar_handle *h, uint64_t bytes, int *algo, int *proto) {
             one = true;
         else if (h->R == 4)
             one = bytes <= (256u << 10);
+        else if (h->R == 16)
+            one = bytes <= (128u << 10);
         else
             one = h->R >= 8 && h->R <= 24 && bytes <= (64u << 10);
         *algo = one ? AR_ONE_SHOT : AR_TWO_SHOT;

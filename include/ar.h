@@ -251,9 +251,9 @@ int ar_allreduce(ar_handle_t h, const void *const in[], void *const out[],
  * open, per message size: the tuned fastest choice after ar_tune, else a
  * fixed rule from GB300 measurements (LL only for the one-shot at R >= 24
  * up to 4 KiB per rank on an LL-capable handle, HB otherwise; with HB,
- * one-shot for R <= 2 at every size, for R = 4 up to 256 KiB per rank and for
- * 8 <= R <= 24 up to 64 KiB, two-shot otherwise; with AR_LL forced, one-shot
- * up to 2 MiB).
+ * one-shot for R <= 2 at every size, for R = 4 up to 256 KiB per rank, for
+ * R = 16 up to 128 KiB and for other 8 <= R <= 24 up to 64 KiB, two-shot
+ * otherwise; with AR_LL forced, one-shot up to 2 MiB).
  * Errors: as ar_allreduce; AR_ERR_INVALID also for n == 0 or n > N. */
 int ar_allreduce_n(ar_handle_t h, const void *const in[], void *const out[], size_t n,
                    int algo, int proto, cudaStream_t stream);

@@ -57,11 +57,12 @@ def test_n_out_of_range_rejected():
 def test_untuned_rule(R):
     """Before ar_tune: LL only for the one-shot at R >= 24 up to 4 KiB per
     rank, HB otherwise; with HB one-shot for R <= 2 at every size, for R = 4
-    up to 256 KiB and for 8 <= R <= 24 up to 64 KiB, two-shot otherwise."""
+    up to 256 KiB, for R = 16 up to 128 KiB and for other 8 <= R <= 24 up to
+    64 KiB, two-shot otherwise."""
     need_gpu()
     with ar.Handle(R, 1 << 23, "bf16") as h:
-        for nbytes in (512, 4096, 4098, 64 << 10, (64 << 10) + 2, 256 << 10, (256 << 10) + 2,
-                       1 << 20, 8 << 20, 16 << 20):
+        for nbytes in (512, 4096, 4098, 64 << 10, (64 << 10) + 2, 128 << 10, (128 << 10) + 2,
+                       256 << 10, (256 << 10) + 2, 1 << 20, 8 << 20, 16 << 20):
             if R >= 24 and nbytes <= 4 << 10:
                 want = (ar.AR_ONE_SHOT, ar.AR_LL)
             else:
@@ -69,6 +70,8 @@ def test_untuned_rule(R):
                     one = True
                 elif R == 4:
                     one = nbytes <= 256 << 10
+                elif R == 16:
+                    one = nbytes <= 128 << 10
                 else:
                     one = 8 <= R <= 24 and nbytes <= 64 << 10
                 want = (ar.AR_ONE_SHOT if one else ar.AR_TWO_SHOT, ar.AR_HB)
