@@ -241,9 +241,9 @@ int one_shot_div(const ar_handle *h, uint64_t n, bool vec16) {
     if (d > 0)
         return d;
     const uint64_t runs = one_shot_runs(h, n, vec16);
-    if (h->R <= 16 && runs <= 2 * (uint64_t)h->one_shot_cap &&
+    if (vec16 && h->R <= 16 && runs <= 2 * (uint64_t)h->one_shot_cap &&
         runs > (uint64_t)(h->one_shot_cap / 4))
-        return 4;
+        return 4;                            // measured with 16-byte vectors only
     return 1;
 }
 
