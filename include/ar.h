@@ -367,13 +367,16 @@ int ar_set_pdl(ar_handle_t h, int enable);
 int ar_set_ll_transport(ar_handle_t h, int transport);
 
 /* Choose how later two-shot HB calls move their data (enum ar_hb_staging;
- * AR_HB_STAGING_AUTO is the default).  Errors: AR_ERR_INVALID. */
+ * AR_HB_STAGING_AUTO is the default).  The HB protocol is the bulk row of the
+ * MemoryChannel's protocol table (MSCCL++ summary, section "MemoryChannel");
+ * the pages name no staging for it: a library choice, identical bits either
+ * way.  Errors: AR_ERR_INVALID. */
 int ar_set_hb_staging(ar_handle_t h, int staging);
 
 /* The staging (AR_HB_STAGING_TMA or AR_HB_STAGING_DIRECT) a two-shot HB call
  * of `bytes` per rank (1 .. N * elem_size) on this handle would use now, with
- * every buffer 16-byte aligned.  Errors: AR_ERR_INVALID (NULL, bytes out of
- * range). */
+ * every buffer 16-byte aligned.  The pages define no such query: library
+ * plumbing.  Errors: AR_ERR_INVALID (NULL, bytes out of range). */
 int ar_get_hb_staging(ar_handle_t h, size_t bytes, int *staging);
 
 /* Launch shape: the number of CTAs.  The SGLang guide's tuner (section 4.4)
