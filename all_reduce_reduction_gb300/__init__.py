@@ -104,6 +104,7 @@ SIGNATURES = {
     "ar_destroy": ([_VP], _I),
     "ar_allreduce": ([_VP, _VPP, _VPP, _I, _I, _VP], _I),
     "ar_allreduce_n": ([_VP, _VPP, _VPP, _SZ, _I, _I, _VP], _I),
+    "ar_allreduce_host": ([_VP, _VPP, _VPP, _SZ, _I, _I, _VP], _I),
     "ar_tune": ([_VP, _VP], _I),
     "ar_combine": ([_VP, _VPP, _VP, _VP, _SZ, _SZ, _VP], _I),
     "ar_get_tuning": ([_VP, _SZ, ctypes.POINTER(_I), ctypes.POINTER(_I),
@@ -216,6 +217,14 @@ def ar_allreduce_n(h: int, ins, outs, n: int, algo=AR_ALGO_AUTO, proto=AR_PROTO_
     proto = PROTOS[proto] if isinstance(proto, str) else proto
     _check(load_library().ar_allreduce_n(h, _ptr_array(ins), _ptr_array(outs), n, algo, proto,
                                          _stream(stream)), "ar_allreduce_n")
+
+
+def ar_allreduce_host(h: int, ins, outs, n: int, algo=AR_ALGO_AUTO, proto=AR_PROTO_AUTO,
+                      stream=None) -> None:
+    algo = ALGOS[algo] if isinstance(algo, str) else algo
+    proto = PROTOS[proto] if isinstance(proto, str) else proto
+    _check(load_library().ar_allreduce_host(h, _ptr_array(ins), _ptr_array(outs), n, algo, proto,
+                                            _stream(stream)), "ar_allreduce_host")
 
 
 def ar_combine(h: int, ys, w, out, T: int, H: int, stream=None) -> None:

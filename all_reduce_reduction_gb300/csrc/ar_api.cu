@@ -165,6 +165,7 @@ struct Call {
     uint64_t n;
     uint64_t shard;         // two-shot shard of n elements
     bool vec16, vec8, inplace;
+    bool host = false;      // some buffer is page-locked host memory
     cudaStream_t s;
 };
 
@@ -249,9 +250,12 @@ int one_shot_div(const ar_handle *h, uint64_t n, bool vec16) {
 
 int one_shot_hb(ar_handle *h, const Call &c) {
     const HbArgs a = hb_args(h, c);
-    const uint64_t runs = one_shot_runs(h, c.n, c.vec16);
-    const int grid = clamp_grid(runs, div_cap(h->one_shot_cap, one_shot_div(h, c.n, c.vec16)));
-    return from_cuda(launch_one_shot_hb(a, h->dtype, c.vec16, runs <= (uint64_t)grid, grid,
+    // host memory: the element-wise form, whose loads and stores are plain
+    // ones (the vector forms stage their inputs with cp.async)
+    const bool vec = c.vec16 && !c.host;
+    const uint64_t runs = one_shot_runs(h, c.n, vec);
+    const int grid = clamp_grid(runs, div_cap(h->one_shot_cap, one_shot_div(h, c.n, vec)));
+    return from_cuda(launch_one_shot_hb(a, h->dtype, vec, runs <= (uint64_t)grid, grid,
                                         32 * h->one_shot_warps, c.s, h->pdl));
 }
 
@@ -274,7 +278,7 @@ int hb2_staging(const ar_handle *h, uint64_t n) {
 int two_shot_hb(ar_handle *h, const Call &c) {
     const int div = grid_div(h, c.n, AR_TWO_SHOT, AR_HB);
     const uint64_t body = (c.n * h->esz) / 16 * 16;
-    if (c.vec16 && body > 0 && hb2_staging(h, c.n) == AR_HB_STAGING_TMA) {
+    if (c.vec16 && !c.host && body > 0 && hb2_staging(h, c.n) == AR_HB_STAGING_TMA) {
         // far beyond L2 (>= 1 GiB moved) one stage of 128 KiB per CTA and two
         // CTAs per SM in turn streamed faster than several stages filling the
         // SM's shared memory (R = 16 x 128 MiB: 635 against 676 us); below
@@ -340,7 +344,7 @@ int ll_cluster(ar_handle *h, const Call &c) {
 int ll(ar_handle *h, const Call &c, bool two) {
     if (!h->slots)
         return AR_ERR_UNSUPPORTED;
-    if (!two && c.vec16 && h->cluster_ok && h->ll_transport == AR_LL_CLUSTER)
+    if (!two && c.vec16 && !c.host && h->cluster_ok && h->ll_transport == AR_LL_CLUSTER)
         return ll_cluster(h, c);
     LlArgs a;
     fill_ptrs(h, c.in, c.out, &a.p);
@@ -635,6 +639,72 @@ int ar_allreduce_n(ar_handle_t h, const void *const in[], void *const out[], siz
     c.s = stream;
     if (algo == AR_ALGO_AUTO || proto == AR_PROTO_AUTO)
         resolve(h, n * h->esz, &algo, &proto);
+    return run_path(h, c, algo, proto);
+}
+
+// Every buffer must be memory the device reaches at the buffer's own
+// address: device memory of the handle's device, managed memory, or
+// page-locked host memory mapped at its host address.  *host tells whether
+// any buffer is host memory.  Pageable host memory is refused.
+static int check_reachable(const ar_handle *h, const void *const in[], void *const out[],
+                           bool *host) {
+    *host = false;
+    for (int r = 0; r < h->R; ++r) {
+        const void *ptrs[2] = {in[r], out[r]};
+        for (const void *p : ptrs) {
+            cudaPointerAttributes at;
+            if (cudaPointerGetAttributes(&at, p) != cudaSuccess) {
+                (void)cudaGetLastError();
+                return AR_ERR_INVALID;
+            }
+            if (at.type == cudaMemoryTypeHost) {
+                if (at.devicePointer != p)
+                    return AR_ERR_INVALID;
+                *host = true;
+            } else if (at.type == cudaMemoryTypeDevice) {
+                if (at.device != h->device)
+                    return AR_ERR_INVALID;
+            } else if (at.type != cudaMemoryTypeManaged) {
+                return AR_ERR_INVALID;
+            }
+        }
+    }
+    return AR_OK;
+}
+
+int ar_allreduce_host(ar_handle_t h, const void *const in[], void *const out[], size_t n,
+                      int algo, int proto, cudaStream_t stream) {
+    if (!in || !h || n < 1 || n > h->N)
+        return AR_ERR_INVALID;
+    if (algo != AR_ONE_SHOT && algo != AR_TWO_SHOT && algo != AR_ALGO_AUTO)
+        return AR_ERR_INVALID;
+    if (proto != AR_LL && proto != AR_HB && proto != AR_PROTO_AUTO)
+        return AR_ERR_INVALID;
+    Call c;
+    int rc = check_buffers(h, in, out, n, &c.vec16, &c.vec8, &c.inplace);
+    if (rc != AR_OK)
+        return rc;
+    rc = check_reachable(h, in, out, &c.host);
+    if (rc != AR_OK)
+        return rc;
+    c.in = in;
+    c.out = out;
+    c.n = n;
+    c.shard = shard_of(n, h->R, h->esz);
+    c.s = stream;
+    if (!c.host) {
+        if (algo == AR_ALGO_AUTO || proto == AR_PROTO_AUTO)
+            resolve(h, n * h->esz, &algo, &proto);
+        return run_path(h, c, algo, proto);
+    }
+    // AUTO with host buffers (R = 8 bf16, 1 KiB to 512 KiB per rank, the
+    // kernels reading and writing host memory: the two-shot HB took 0.91-1.00
+    // of the one-shot LL's time): the two-shot HB, or the one-shot LL when
+    // LL is asked for
+    if (algo == AR_ALGO_AUTO)
+        algo = proto == AR_LL ? AR_ONE_SHOT : AR_TWO_SHOT;
+    if (proto == AR_PROTO_AUTO)
+        proto = algo == AR_ONE_SHOT && h->slots ? AR_LL : AR_HB;
     return run_path(h, c, algo, proto);
 }
 

@@ -517,6 +517,19 @@ class CaseRunner:
         for r, t in enumerate(self.cpu_inputs):
             self.pinned_in[r * self.stride:r * self.stride + n].copy_(t)
         self.pinned_out = torch.empty(self.out_block.shape, dtype=self.out_block.dtype).pin_memory()
+        self.host_bytes = (nin * n * self.pinned_in.element_size(),
+                           nout * n * self.pinned_out.element_size())
+        self.host_call = None
+        if not c.get("combine") and not self.plan:
+            # the same all-reduce on the page-locked host buffers themselves
+            hins = [self.pinned_in[r * self.stride:r * self.stride + n] for r in range(nin)]
+            houts = [self.pinned_out[r * self.stride:r * self.stride + n] for r in range(nout)]
+
+            def host_call():
+                ar.ar_allreduce_host(self.h.h, hins, houts, n, self.algo, self.proto,
+                                     stream=stream)
+
+            self.host_call = host_call
 
     def close(self):
         import all_reduce_reduction_gb300 as ar
@@ -664,37 +677,54 @@ def run_ours(args, dist: Dist):
             sweep[str(r.w.n)]["auto_choice"] = r.choice
 
     # end to end, one host round trip per all-reduce: every step, each case's
-    # R inputs are copied in from pinned host memory, one all-reduce runs
-    # through the library's public call, and all R outputs are copied back to
-    # pinned host memory; events on the stream bracket the three.  The three
-    # are captured once per case as a one-call CUDA graph (the copies are
-    # graph nodes, the call the library's own launch), so the GPU runs them
-    # back to back; the eager form, with the host enqueueing each of the three
-    # in turn, is reported beside it.
+    # R inputs come from page-locked host memory and all its outputs go back
+    # to page-locked host memory, one all-reduce per case.  Two forms, each
+    # captured once per case as a one-call CUDA graph and replayed, with CUDA
+    # events on the stream around each replay:
+    #   host:   the library's host-buffer call (ar_allreduce_host): its
+    #           kernels read the inputs from and write the outputs to host
+    #           memory through the CPU-GPU link;
+    #   copies: the inputs copied in, the device-buffer call, the outputs
+    #           copied back (two copy nodes around the call).
+    # The host form is the headline where every case has it (plans and the
+    # combine have no host-buffer call).  The host form enqueued eagerly is
+    # reported beside them.
     e2e_steps = max(3, min(args.steps, 50))
-    for r in runners:                   # warm the eager path of every case first
+    host_form = all(r.host_call is not None for r in runners)
+    for r in runners:                   # warm the eager paths of every case first
         with torch.cuda.stream(stream):
             r.in_block.copy_(r.pinned_in, non_blocking=True)
             r.call()
             r.pinned_out.copy_(r.out_block, non_blocking=True)
+            if host_form:
+                r.host_call()
     torch.cuda.synchronize()
     for r in runners:
-        r.e2e_graph = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(r.e2e_graph, stream=stream):
+        r.e2e_graphs = {}
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
             r.in_block.copy_(r.pinned_in, non_blocking=True)
             r.call()
             r.pinned_out.copy_(r.out_block, non_blocking=True)
-        r.pinned_out.zero_()
-        r.e2e_graph.replay()
-    torch.cuda.synchronize()
-    for r in runners:                   # the graph's copies really move the data
-        if not torch.equal(r.pinned_out, r.out_block.cpu()):
-            raise SystemExit("e2e graph: host outputs differ from the device outputs")
-    h2d = sum(r.pinned_in.numel() * r.pinned_in.element_size() for r in runners)
-    d2h = sum(r.pinned_out.numel() * r.pinned_out.element_size() for r in runners)
+        r.e2e_graphs["copies"] = g
+        if host_form:
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=stream):
+                r.host_call()
+            r.e2e_graphs["host"] = g
+    for form in list(runners[0].e2e_graphs):    # each form really moves the data
+        for r in runners:
+            r.pinned_out.zero_()
+            r.e2e_graphs[form].replay()
+        torch.cuda.synchronize()
+        for r in runners:
+            if not torch.equal(r.pinned_out, r.out_block.cpu()):
+                raise SystemExit("e2e (%s): host outputs differ from the device outputs" % form)
+    if ar.ar_status(runners[0].h.h) != ar.AR_OK:
+        raise SystemExit("e2e: device status " + ar.ar_strerror(ar.ar_status(runners[0].h.h)))
     e2e_bytes = sum(r.bytes for r in runners)          # one call per case per step
 
-    def round_trips(graph: bool) -> float:
+    def round_trips(form: str, graph: bool = True) -> float:
         ms = 0.0
         dist.barrier()
         torch.cuda.synchronize()
@@ -705,41 +735,51 @@ def run_ours(args, dist: Dist):
                     e1 = torch.cuda.Event(enable_timing=True)
                     e0.record(stream)
                     if graph:
-                        r.e2e_graph.replay()
+                        r.e2e_graphs[form].replay()
                     else:
-                        r.in_block.copy_(r.pinned_in, non_blocking=True)
-                        r.call()
-                        r.pinned_out.copy_(r.out_block, non_blocking=True)
+                        r.host_call()
                     e1.record(stream)
                 e1.synchronize()
                 ms += e0.elapsed_time(e1)
         return dist.max(ms / e2e_steps)
 
-    e2e_ms = round_trips(graph=True)
-    e2e_value = dist.sum(e2e_bytes) / (e2e_ms * 1e-3) / 1e9
-    eager_e2e_ms = round_trips(graph=False)
-    eager_e2e_value = dist.sum(e2e_bytes) / (eager_e2e_ms * 1e-3) / 1e9
-    for r in runners:
-        r.e2e_graph = None
+    def rate(ms: float) -> float:
+        return dist.sum(e2e_bytes) / (ms * 1e-3) / 1e9
 
-    # the earlier form, for comparison: one host round trip per case around
-    # the case's whole graph (`calls` all-reduces)
-    batched_ms = 0.0
-    torch.cuda.synchronize()
-    for _ in range(e2e_steps):
-        for r in runners:
-            with torch.cuda.stream(stream):
-                e0 = torch.cuda.Event(enable_timing=True)
-                e1 = torch.cuda.Event(enable_timing=True)
-                e0.record(stream)
-                r.in_block.copy_(r.pinned_in, non_blocking=True)
-                r.graph.replay()
-                r.pinned_out.copy_(r.out_block, non_blocking=True)
-                e1.record(stream)
-            e1.synchronize()
-            batched_ms += e0.elapsed_time(e1)
-    batched_ms = dist.max(batched_ms / e2e_steps)
-    batched_value = dist.sum(bytes_step) / (batched_ms * 1e-3) / 1e9
+    copies_ms = round_trips("copies")
+    if host_form:
+        e2e_ms = round_trips("host")
+        eager_ms = round_trips("host", graph=False)
+        h2d = sum(r.host_bytes[0] for r in runners)
+        d2h = sum(r.host_bytes[1] for r in runners)
+    else:
+        e2e_ms, eager_ms = copies_ms, None
+        h2d = sum(r.pinned_in.numel() * r.pinned_in.element_size() for r in runners)
+        d2h = sum(r.pinned_out.numel() * r.pinned_out.element_size() for r in runners)
+    for r in runners:
+        r.e2e_graphs = None
+    e2e = {"value": round(rate(e2e_ms), 2), "unit": "GB/s", "h2d_bytes_per_step": h2d,
+           "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms, 5),
+           "calls_per_step": len(runners), "method": "host" if host_form else "copies",
+           "note": ("one all-reduce per case per step through the library's host-buffer call "
+                    "(ar_allreduce_host): the kernels read the case's R inputs from page-locked "
+                    "host memory and write its outputs to page-locked host memory; one-call "
+                    "CUDA graph per case, CUDA events on the stream around each replay; "
+                    "minimal bytes of the step's calls / that time"
+                    if host_form else
+                    "one all-reduce per case per step, each with its own host round trip: "
+                    "the inputs copied in from page-locked host memory, the call, the outputs "
+                    "copied back, captured as a one-call CUDA graph per case; CUDA events "
+                    "around each replay; minimal bytes of the step's calls / that time"),
+           "copies": {"value": round(rate(copies_ms), 2), "unit": "GB/s",
+                      "ms_per_step": round(copies_ms, 5),
+                      "note": "the same round trips with copies: inputs copied in, the "
+                              "device-buffer call, outputs copied back (one graph per case)"}}
+    if eager_ms is not None:
+        e2e["eager"] = {"value": round(rate(eager_ms), 2), "unit": "GB/s",
+                        "ms_per_step": round(eager_ms, 5),
+                        "note": "the host-buffer call enqueued eagerly, the host's enqueue "
+                                "gaps inside the timed events"}
 
     hbm = None
     if args.workload == "sweep" and not args.no_hbm:
@@ -780,24 +820,7 @@ def run_ours(args, dist: Dist):
                    "parallelism": "replicas" if dist.world > 1 else "single GPU"},
         "roofline": roofline,
         "cpu_baseline": cpu,
-        "e2e": {"value": round(e2e_value, 2), "unit": "GB/s", "h2d_bytes_per_step": h2d,
-                "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms, 5),
-                "calls_per_step": len(runners),
-                "note": "one all-reduce per case per step, each with its own host round trip: "
-                        "the case's R inputs copied in from pinned host memory, one "
-                        "ar_allreduce call, all R outputs copied back to pinned host memory, "
-                        "the three captured once per case as a one-call CUDA graph and "
-                        "replayed; CUDA events on the stream around each replay; minimal "
-                        "bytes of the step's calls / that time",
-                "eager": {"value": round(eager_e2e_value, 2), "unit": "GB/s",
-                          "ms_per_step": round(eager_e2e_ms, 5),
-                          "note": "the same round trips enqueued one by one from the host "
-                                  "(two copies and one eager ar_allreduce call per case), "
-                                  "the host's enqueue gaps inside the timed events"},
-                "graph_batched": {"value": round(batched_value, 2), "unit": "GB/s",
-                                  "note": "the earlier form: one host round trip per case "
-                                          "around the case's whole %d-call graph"
-                                          % cases[0]["calls"]}},
+        "e2e": e2e,
         "gpu_launches": launches,
         "clocks": clocks, "clocks_remeasured": remeasured,
         "sweep": sweep,

@@ -258,6 +258,27 @@ int ar_allreduce(ar_handle_t h, const void *const in[], void *const out[],
 int ar_allreduce_n(ar_handle_t h, const void *const in[], void *const out[], size_t n,
                    int algo, int proto, cudaStream_t stream);
 
+/* ar_allreduce_n whose buffers may be in host memory: each of the 2R
+ * pointers is device memory of the handle's device, managed memory, or
+ * page-locked host memory that the device reaches at the same address
+ * (cudaHostAlloc, cudaMallocHost or cudaHostRegister on a system with
+ * unified addressing; on GB300 the kernels then read and write it through
+ * the CPU-GPU link, so no copy is enqueued).  The pages' collective runs on
+ * GPU buffers (MSCCL++ summary, section "第一层：Collective API"); host
+ * buffers are a library addition for callers whose data sits in host memory.
+ * With some buffer in host memory the call takes only kernels whose loads
+ * and stores are plain ones: the two-shot HB in its direct staging, the
+ * one-shot HB in its element-wise form, and the LL protocol over HBM packet
+ * slots.  AUTO then picks the two-shot HB (the one-shot LL when AR_LL is
+ * asked for; with AR_ONE_SHOT, LL on an LL-capable handle).  With every
+ * buffer in device memory the call is ar_allreduce_n.  Results are the same
+ * bits either way.  Each call queries every pointer
+ * (cudaPointerGetAttributes).
+ * Errors: as ar_allreduce_n; AR_ERR_INVALID also for pageable host memory,
+ * host memory mapped at another address, or another device's memory. */
+int ar_allreduce_host(ar_handle_t h, const void *const in[], void *const out[], size_t n,
+                      int algo, int proto, cudaStream_t stream);
+
 /* Autotune AUTO for this handle (SGLang guide, section 4.4: every
  * (algorithm, configuration) is timed inside a CUDA graph at 15
  * power-of-two message sizes in [2^9, 2^24) bytes, and later calls map their

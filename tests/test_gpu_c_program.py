@@ -1,9 +1,10 @@
 """The C ABI driven by a plain C11 program, with no Python or torch in the
 loop: device buffers from cudaMalloc, a stream from cudaStreamCreate, every
 schedule x protocol through ar_allreduce, and AUTO through ar_allreduce_n
-captured in a CUDA graph and replayed.  The program reads its inputs from a
-file (drawn here by the seeded generator) and writes every path's outputs to
-a file, which this test compares with the oracle bit for bit."""
+captured in a CUDA graph and replayed, then ar_allreduce_host on buffers
+from cudaMallocHost.  The program reads its inputs from a file (drawn here by
+the seeded generator) and writes every path's outputs to a file, which this
+test compares with the oracle bit for bit."""
 import os
 import shutil
 import subprocess
@@ -101,6 +102,28 @@ int main(int argc, char **argv) {
         if (fwrite(host, 1, (size_t)R * bytes, fo) != (size_t)R * bytes)
             return 1;
     }
+    /* page-locked host buffers, read and written by the kernels in place */
+    void *hin[AR_MAX_RANKS] = {0};
+    void *hout[AR_MAX_RANKS] = {0};
+    FILE *fi = fopen(argv[4], "rb");
+    if (!fi)
+        return 1;
+    for (int r = 0; r < R; ++r) {
+        CHECK_CUDA(cudaMallocHost(&hin[r], bytes));
+        CHECK_CUDA(cudaMallocHost(&hout[r], bytes));
+        if (fread(hin[r], 1, bytes, fi) != bytes)
+            return 1;
+        in[r] = hin[r];
+    }
+    fclose(fi);
+    CHECK_AR(ar_allreduce_host(h, in, hout, n, AR_ALGO_AUTO, AR_PROTO_AUTO, s));
+    CHECK_AR(ar_status(h, s));
+    for (int r = 0; r < R; ++r) {
+        if (fwrite(hout[r], 1, bytes, fo) != bytes)
+            return 1;
+        CHECK_CUDA(cudaFreeHost(hin[r]));
+        CHECK_CUDA(cudaFreeHost(hout[r]));
+    }
     fclose(fo);
     CHECK_AR(ar_destroy(h));
     CHECK_CUDA(cudaStreamDestroy(s));
@@ -158,9 +181,10 @@ def test_c_program_every_path_bit_exact(c_program, tmp_path, dtype, R, n):
     assert res.returncode == 0, res.stderr
     want = oracle.allreduce(bits, wl.DTYPE_CODE[dtype])[0]
     u = np.uint32 if dtype == "fp32" else np.uint16
-    got = np.fromfile(outp, dtype=u).reshape(5, R, n)
-    names = ["one_shot_hb", "two_shot_hb", "one_shot_ll", "two_shot_ll", "auto_graph"]
-    for p in range(5):
+    got = np.fromfile(outp, dtype=u).reshape(6, R, n)
+    names = ["one_shot_hb", "two_shot_hb", "one_shot_ll", "two_shot_ll", "auto_graph",
+             "host_buffers"]
+    for p in range(6):
         for r in range(R):
             bad = np.nonzero(got[p, r] != np.ascontiguousarray(want).view(u))[0]
             assert bad.size == 0, "%s rank %d: %d elements differ, first at %d" % (
