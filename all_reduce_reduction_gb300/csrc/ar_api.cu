@@ -697,14 +697,31 @@ int ar_allreduce_host(ar_handle_t h, const void *const in[], void *const out[], 
             resolve(h, n * h->esz, &algo, &proto);
         return run_path(h, c, algo, proto);
     }
-    // AUTO with host buffers (R = 8 bf16, 1 KiB to 512 KiB per rank, the
-    // kernels reading and writing host memory: the two-shot HB took 0.91-1.00
-    // of the one-shot LL's time): the two-shot HB, or the one-shot LL when
-    // LL is asked for
-    if (algo == AR_ALGO_AUTO)
-        algo = proto == AR_LL ? AR_ONE_SHOT : AR_TWO_SHOT;
-    if (proto == AR_PROTO_AUTO)
-        proto = algo == AR_ONE_SHOT && h->slots ? AR_LL : AR_HB;
+    // AUTO with host buffers, a fixed rule from GB300 measurements (one-call
+    // graphs, bf16, R = 2 to 32, 1 KiB to 4 MiB per rank, the kernels
+    // reading and writing host memory): the one-shot LL for R >= 24 up to
+    // 16 KiB per rank (R = 32, 1 KiB: 7.7 against 9.9 us), the one-shot HB
+    // for R <= 4 from 1 MiB (7-9% faster), the two-shot HB otherwise (R = 8:
+    // 0.91-1.00 of the one-shot LL's time from 1 to 512 KiB; R = 2 and 4 up
+    // to 128 KiB: 5.8 against 7.2-7.9 us).  A half fixed by the caller is
+    // kept: with AR_LL the one-shot, with AR_ONE_SHOT LL on an LL-capable
+    // handle (HB for R <= 4 from 1 MiB), with AR_TWO_SHOT HB.
+    const uint64_t bytes = n * h->esz;
+    const bool ll_ok = h->slots != nullptr;
+    const bool one_hb = h->R <= 4 && bytes >= ((uint64_t)1 << 20);
+    if (algo == AR_ALGO_AUTO && proto == AR_PROTO_AUTO) {
+        if (ll_ok && h->R >= 24 && bytes <= 16384) {
+            algo = AR_ONE_SHOT;
+            proto = AR_LL;
+        } else {
+            algo = one_hb ? AR_ONE_SHOT : AR_TWO_SHOT;
+            proto = AR_HB;
+        }
+    } else if (algo == AR_ALGO_AUTO) {
+        algo = proto == AR_LL || one_hb ? AR_ONE_SHOT : AR_TWO_SHOT;
+    } else if (proto == AR_PROTO_AUTO) {
+        proto = algo == AR_ONE_SHOT && ll_ok && !one_hb ? AR_LL : AR_HB;
+    }
     return run_path(h, c, algo, proto);
 }
 

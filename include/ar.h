@@ -269,8 +269,11 @@ int ar_allreduce_n(ar_handle_t h, const void *const in[], void *const out[], siz
  * With some buffer in host memory the call takes only kernels whose loads
  * and stores are plain ones: the two-shot HB in its direct staging, the
  * one-shot HB in its element-wise form, and the LL protocol over HBM packet
- * slots.  AUTO then picks the two-shot HB (the one-shot LL when AR_LL is
- * asked for; with AR_ONE_SHOT, LL on an LL-capable handle).  With every
+ * slots.  AUTO then follows a fixed rule from GB300 measurements: the
+ * one-shot LL for R >= 24 up to 16 KiB per rank, the one-shot HB for R <= 4
+ * from 1 MiB, the two-shot HB otherwise (a half fixed by the caller is kept:
+ * with AR_LL the one-shot; with AR_ONE_SHOT LL on an LL-capable handle, HB
+ * for R <= 4 from 1 MiB; with AR_TWO_SHOT HB).  With every
  * buffer in device memory the call is ar_allreduce_n.  Results are the same
  * bits either way.  Each call queries every pointer
  * (cudaPointerGetAttributes).
