@@ -620,23 +620,32 @@ int ar_destroy(ar_handle_t h) {
     return rc;
 }
 
-int ar_allreduce_n(ar_handle_t h, const void *const in[], void *const out[], size_t n, int algo,
-                   int proto, cudaStream_t stream) {
+// The checks and the Call shared by ar_allreduce_n and ar_allreduce_host.
+static int prepare_call(ar_handle_t h, const void *const in[], void *const out[], size_t n,
+                        int algo, int proto, cudaStream_t stream, Call *c) {
     if (!in || !h || n < 1 || n > h->N)
         return AR_ERR_INVALID;
     if (algo != AR_ONE_SHOT && algo != AR_TWO_SHOT && algo != AR_ALGO_AUTO)
         return AR_ERR_INVALID;
     if (proto != AR_LL && proto != AR_HB && proto != AR_PROTO_AUTO)
         return AR_ERR_INVALID;
-    Call c;
-    const int rc = check_buffers(h, in, out, n, &c.vec16, &c.vec8, &c.inplace);
+    const int rc = check_buffers(h, in, out, n, &c->vec16, &c->vec8, &c->inplace);
     if (rc != AR_OK)
         return rc;
-    c.in = in;
-    c.out = out;
-    c.n = n;
-    c.shard = shard_of(n, h->R, h->esz);
-    c.s = stream;
+    c->in = in;
+    c->out = out;
+    c->n = n;
+    c->shard = shard_of(n, h->R, h->esz);
+    c->s = stream;
+    return AR_OK;
+}
+
+int ar_allreduce_n(ar_handle_t h, const void *const in[], void *const out[], size_t n, int algo,
+                   int proto, cudaStream_t stream) {
+    Call c;
+    const int rc = prepare_call(h, in, out, n, algo, proto, stream, &c);
+    if (rc != AR_OK)
+        return rc;
     if (algo == AR_ALGO_AUTO || proto == AR_PROTO_AUTO)
         resolve(h, n * h->esz, &algo, &proto);
     return run_path(h, c, algo, proto);
@@ -674,24 +683,13 @@ static int check_reachable(const ar_handle *h, const void *const in[], void *con
 
 int ar_allreduce_host(ar_handle_t h, const void *const in[], void *const out[], size_t n,
                       int algo, int proto, cudaStream_t stream) {
-    if (!in || !h || n < 1 || n > h->N)
-        return AR_ERR_INVALID;
-    if (algo != AR_ONE_SHOT && algo != AR_TWO_SHOT && algo != AR_ALGO_AUTO)
-        return AR_ERR_INVALID;
-    if (proto != AR_LL && proto != AR_HB && proto != AR_PROTO_AUTO)
-        return AR_ERR_INVALID;
     Call c;
-    int rc = check_buffers(h, in, out, n, &c.vec16, &c.vec8, &c.inplace);
+    int rc = prepare_call(h, in, out, n, algo, proto, stream, &c);
     if (rc != AR_OK)
         return rc;
     rc = check_reachable(h, in, out, &c.host);
     if (rc != AR_OK)
         return rc;
-    c.in = in;
-    c.out = out;
-    c.n = n;
-    c.shard = shard_of(n, h->R, h->esz);
-    c.s = stream;
     if (!c.host) {
         if (algo == AR_ALGO_AUTO || proto == AR_PROTO_AUTO)
             resolve(h, n * h->esz, &algo, &proto);
