@@ -58,10 +58,10 @@ def run_host(h, ins, outs, n, algo, proto):
 @pytest.mark.parametrize("path", PATHS, ids=PATH_IDS)
 @pytest.mark.parametrize("R,n,dtype", [(8, 1 << 18, "bf16"), (8, 1001, "bf16"), (2, 65539, "fp32"),
                                        (5, 4097, "fp16"), (32, 777, "bf16"), (1, 300, "fp32"),
-                                       (4, (1 << 19) + 3, "bf16")],
+                                       (4, (1 << 19) + 3, "bf16"), (16, (1 << 20) + 5, "bf16")],
                          ids=["r8_n262144_bf16", "r8_n1001_bf16", "r2_n65539_fp32",
                               "r5_n4097_fp16", "r32_n777_bf16", "r1_n300_fp32",
-                              "r4_n524291_bf16"])
+                              "r4_n524291_bf16", "r16_n1048581_bf16"])
 @pytest.mark.parametrize("offset", [0, 1, 4], ids=["aligned", "off2or4", "off8or16"])
 def test_host_buffers_match_oracle(path, R, n, dtype, offset):
     need_gpu()
