@@ -796,9 +796,7 @@ def run_ours(args, dist: Dist):
     if args.workload in ("sweep", "decode") and not args.no_variants:
         variants = measure_variants(runners, stream, flush, max(20, args.steps // 10))
 
-    eager = None
-    if args.workload in ("sweep", "decode"):
-        eager = measure_eager(runners, stream, flush)
+    eager = measure_eager(runners, stream, flush)
 
     cpu = None
     if dist.world == 1 and not args.no_cpu_baseline:
