@@ -399,13 +399,16 @@ int bucket_of(uint64_t bytes) {
 // Resolve AR_ALGO_AUTO / AR_PROTO_AUTO for a message of `bytes` per rank:
 // the fastest tuned (algo, proto) allowed by the fixed half of the request,
 // or, before ar_tune, a fixed rule from GB300 measurements (10-call graphs,
-// L2 flushed; R = 2 to 32): LL only for the one-shot at R >= 24 up to 4 KiB
-// per rank, HB otherwise; with HB, one-shot for R <= 2 at every size, for
-// R = 4 up to 256 KiB per rank, for R = 16 up to 128 KiB and for
-// 8 <= R <= 24 otherwise up to 64 KiB, two-shot otherwise (against the two-shot with its AUTO staging the one-shot, whose
-// fold work grows with R^2, wins only there; R = 3, 5 and 6, without an
-// unrolled ring, were faster or tied two-shot); with LL forced, one-shot up
-// to 2 MiB.
+// L2 flushed; R = 2 to 32):
+//   - LL only for the one-shot at R >= 24 up to 4 KiB per rank, HB
+//     otherwise;
+//   - with HB, the one-shot for R <= 2 at every size, for R = 4 up to
+//     256 KiB per rank, for R = 16 up to 128 KiB and for the other
+//     8 <= R <= 24 up to 64 KiB, the two-shot otherwise.  Against the
+//     two-shot with its AUTO staging the one-shot, whose fold work grows
+//     with R^2, wins only there; R = 3, 5 and 6, without an unrolled ring,
+//     were faster or tied two-shot;
+//   - with LL forced, the one-shot up to 2 MiB.
 void resolve(const ar_handle *h, uint64_t bytes, int *algo, int *proto) {
     const bool ll_ok = h->slots != nullptr;
     if (h->tuned_max >= 0) {
