@@ -30,7 +30,9 @@
  *   - The return value is an ar_status_code; AR_OK is 0.
  *   - "Device pointer": memory the current CUDA device can read/write with
  *     ordinary loads and stores (cudaMalloc, torch CUDA tensors, ...).  The
- *     library does not check that a pointer is a device pointer.
+ *     library does not check that a pointer is a device pointer.  Buffers
+ *     in page-locked host memory go through ar_allreduce_host, which checks
+ *     them and keeps them off the kernels that copy with TMA or cp.async.
  *   - "Host array": a plain C array in host memory, read during the call only.
  *   - Work is enqueued on `stream` and nothing waits for it, except in
  *     ar_create, ar_destroy and ar_status.  No entry point used on the hot
