@@ -514,7 +514,8 @@ int ar_plan_compile(ar_handle_t h, const ar_op *ops, int nops, int nchunks,
  * Same results as ar_allreduce.  chunks_per_rank == 0 picks ctas_per_rank
  * chunks, except for AR_TWO_SHOT with R >= 8: there a multiple of
  * ctas_per_rank (1 to 16 per CTA) that makes a chunk about 8 KiB of a rank
- * buffer.  ctas_per_rank == 0 fills the resident capacity.  Errors as
+ * buffer.  ctas_per_rank == 0 fills the resident capacity, except for
+ * AR_TWO_SHOT with R >= 16: there two CTAs per SM.  Errors as
  * ar_plan_compile. */
 int ar_plan_builtin(ar_handle_t h, int algo, int chunks_per_rank, int ctas_per_rank,
                     ar_plan_t *out);

@@ -251,3 +251,33 @@ def test_builtin_plan_fills_the_gpu_by_default(algo):
     want = expected(cpu, dtype)
     for r in range(R):
         assert_bits_equal(outs[r], want, dtype, "rank %d" % r)
+
+
+@pytest.mark.parametrize("R", [16, 32])
+def test_builtin_two_shot_plan_two_ctas_per_sm_from_r16(R):
+    """From R = 16 the built-in two-shot plan runs two CTAs per SM by
+    default (the one-shot plan and smaller R fill the resident capacity);
+    the results stay the oracle's bit for bit."""
+    need_gpu()
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    with ar.Handle(R, 1000, "bf16") as h:              # one chunk per CTA: gives the CTA count
+        p = ar.ar_plan_builtin(h.h, "two_shot")
+        tasks, _, _ = ar.ar_plan_stats(p)
+        ar.ar_plan_destroy(p)
+        assert tasks == R * (2 * sms // R)
+        p = ar.ar_plan_builtin(h.h, "one_shot")
+        tasks, _, _ = ar.ar_plan_stats(p)
+        ar.ar_plan_destroy(p)
+        assert tasks // (R * R) > 2 * sms // R          # more CTAs: the resident capacity
+    n = (1 << 20) + 5
+    cpu = wl.make_inputs(88, R, n, "bf16", "normal")
+    ins = device_inputs(cpu)
+    outs = _outs(R, n, "bf16")
+    with ar.Handle(R, n, "bf16") as h:
+        p = ar.ar_plan_builtin(h.h, "two_shot")
+        ar.ar_plan_execute(p, ins, outs)
+        assert ar.ar_status(h.h) == ar.AR_OK
+        ar.ar_plan_destroy(p)
+    want = expected(cpu, "bf16")
+    for r in range(R):
+        assert_bits_equal(outs[r], want, "bf16", "rank %d" % r)
